@@ -1,0 +1,475 @@
+/*
+ * CPU oracle for the routed mixture-of-experts layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, obviously-correct
+ * statement of what the GPU library computes.  Only the test-suite, the smoke
+ * check and the benchmark's CPU-baseline leg may load it; the product path
+ * never does.  It shares no code, header, table or constant generator with
+ * the CUDA library.
+ *
+ * Source of the method: the vLLM-Ascend "Kimi K3 MoE Forward Insight" page:
+ *   - Runner Initialization: routing settings are grouped top-k,
+ *     renormalisation, scoring function, correction bias, routed scaling;
+ *     expert ids are two-level (logical -> physical through log2phy).
+ *   - Stage 2 (Select Experts): softmax / sigmoid / sqrtsoftplus scoring,
+ *     hash routing through tid2eid indexed by input_ids, then grouped top-k,
+ *     correction bias, top-k, renormalisation, routed scaling.
+ *   - Stage 4 (Dispatch, MLP, Combine): map topk_ids through log2phy, sort
+ *     tokens by expert and return expert token counts (AllGather mode), grouped
+ *     gate/up matmul -> SwiGLU -> grouped down matmul, then restore token order
+ *     and apply the routing probabilities.
+ *   - Stage 6 (Dynamic EPLB): per-expert token counts accumulated into moe_load.
+ *   - Forward Skeleton / shared experts: the always-on shared expert's output is
+ *     added to the routed output.
+ *
+ * Readings where the page is silent (each also listed in the design notes):
+ *   R1 router logit l[t,e] = sum_h x[t,h]*Wr[e,h] in fp32 with a pinned order:
+ *      32 partial sums, partial j accumulates h = j, j+32, ... ascending with a
+ *      fused multiply-add, then the pairwise tree s = 16,8,4,2,1
+ *      (p[i] += p[i+s], i < s); an optional router bias is added last.
+ *   R2 scores use this file's own elementary functions: exp by Cody-Waite
+ *      reduction (ln2 split hi/lo) and the degree-7 Taylor polynomial;
+ *      log1p(y) = 2 atanh(y/(2+y)) by its odd power series; sigmoid =
+ *      1/(1+exp(-l)); sqrtsoftplus = sqrt(max(l,0) + log1p(exp(-|l|)));
+ *      softmax normalises by a sum taken in the R1 order over experts.
+ *      Division and sqrt are IEEE correctly rounded.
+ *   R3 selection score = score + correction bias (when given); the bias never
+ *      enters the routing weights.
+ *   R4 grouped top-k: E experts in n_group contiguous groups; group score = max
+ *      of the group's selection scores, or the sum of its two largest; the
+ *      topk_group best groups are kept, the others' experts are excluded.
+ *   R5 ties: the lower expert (group) index wins; slots are filled in pick
+ *      order (descending selection score).
+ *   R6 weights: w_j = (s_j / sum_j s_j) * routed_scaling with the sum taken in
+ *      slot order (renormalise on), else s_j * routed_scaling.
+ *   R7 hash: ids = tid2eid[input_ids[t]][0..k-1]; weights from the scoring
+ *      function at those experts.
+ *   R8 replica of logical e for token t: log2phy[e][t mod replica_cnt[e]].
+ *   R9 permutation: stable counting sort of the flat index f = t*k + j by
+ *      physical expert; row r = offsets[p] + rank of f among equal p.
+ *   R10 rounding points: act = bf16(silu(g) * u) with g, u held in fp32;
+ *      y = bf16(act . Wd); shared ys = bf16(...); out = bf16(sum_j w_j y_j + ys).
+ *      Dot products of the expert MLP accumulate in double (exact products).
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared -pthread
+ * (-ffp-contract=off keeps every a*b+c below as two rounded operations unless
+ * written as fmaf).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ bf16 */
+static inline float bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+static inline uint16_t f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+uint16_t orc_f32_to_bf16(float f) { return f32_to_bf16(f); }
+
+/* -------------------------------------------------- elementary functions */
+/* ln 2 split so that n*LN2_HI is exact for |n| <= 256: LN2_HI is ln 2 rounded
+ * to 16 significant bits (45426 / 2^16), LN2_LO = fp32(ln 2 - LN2_HI). */
+#define ORC_LN2_HI 0.693145751953125f
+#define ORC_LN2_LO 1.428606820309417e-06f
+#define ORC_LOG2E 1.44269502162933349609375f /* fp32(1 / ln 2) */
+
+static inline float pow2i(int n) { /* 2^n for -126 <= n <= 127 */
+    uint32_t u = (uint32_t)(n + 127) << 23;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* exp(x): Cody-Waite range reduction x = n ln2 + r, |r| <~ ln2/2, then the
+ * Taylor polynomial of e^r to degree 7 by Horner's rule, then 2^n applied as
+ * two exact power-of-two scalings.  Results below 2^-126 flush to zero. */
+float orc_exp(float x) {
+    if (x != x) return x;
+    if (x > 88.72283935546875f) return INFINITY;
+    if (x < -87.33654022216797f) return 0.0f;
+    float nf = rintf(x * ORC_LOG2E);
+    int n = (int)nf;
+    float r = fmaf(-nf, ORC_LN2_HI, x);
+    r = fmaf(-nf, ORC_LN2_LO, r);
+    float p = 1.0f / 5040.0f;          /* 1/7! */
+    p = fmaf(p, r, 1.0f / 720.0f);     /* 1/6! */
+    p = fmaf(p, r, 1.0f / 120.0f);     /* 1/5! */
+    p = fmaf(p, r, 1.0f / 24.0f);      /* 1/4! */
+    p = fmaf(p, r, 1.0f / 6.0f);       /* 1/3! */
+    p = fmaf(p, r, 0.5f);              /* 1/2! */
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    int n1 = n / 2;
+    int n2 = n - n1;
+    return (p * pow2i(n1)) * pow2i(n2);
+}
+
+/* log(1+y) for 0 <= y <= 1: 2 atanh(z), z = y/(2+y) <= 1/3, with the series
+ * z + z^3/3 + ... + z^17/17 (next term below 2e-10 relative). */
+float orc_log1p(float y) {
+    float z = y / (2.0f + y);
+    float w = z * z;
+    float q = 1.0f / 17.0f;
+    q = fmaf(q, w, 1.0f / 15.0f);
+    q = fmaf(q, w, 1.0f / 13.0f);
+    q = fmaf(q, w, 1.0f / 11.0f);
+    q = fmaf(q, w, 1.0f / 9.0f);
+    q = fmaf(q, w, 1.0f / 7.0f);
+    q = fmaf(q, w, 1.0f / 5.0f);
+    q = fmaf(q, w, 1.0f / 3.0f);
+    float zw = z * w;
+    float a = fmaf(zw, q, z);
+    return 2.0f * a;
+}
+
+float orc_sigmoid(float l) {
+    float e = orc_exp(-l);
+    float d = 1.0f + e;
+    return 1.0f / d;
+}
+
+float orc_sqrtsoftplus(float l) {
+    float a = fabsf(l);
+    float sp = fmaxf(l, 0.0f) + orc_log1p(orc_exp(-a));
+    return sqrtf(sp);
+}
+
+/* ------------------------------------------------------------- routing */
+enum { ORC_SOFTMAX = 0, ORC_SIGMOID = 1, ORC_SQRTSOFTPLUS = 2 };
+enum { ORC_GROUP_MAX = 0, ORC_GROUP_TOP2SUM = 1 };
+
+typedef struct {
+    int E;            /* logical experts */
+    int P;            /* physical slots */
+    int k;            /* experts per token */
+    int n_group;
+    int topk_group;
+    int scoring;      /* ORC_SOFTMAX / ORC_SIGMOID / ORC_SQRTSOFTPLUS */
+    int group_score;  /* ORC_GROUP_MAX / ORC_GROUP_TOP2SUM */
+    int renormalize;
+    float routed_scaling;
+    int use_hash;
+} orc_route_cfg;
+
+/* R1: one router logit in the pinned order. */
+float orc_router_logit(const uint16_t* x, const float* w, int H) {
+    float p[32];
+    for (int j = 0; j < 32; ++j) p[j] = 0.0f;
+    for (int h = 0; h < H; ++h) p[h & 31] = fmaf(bf16_to_f32(x[h]), w[h], p[h & 31]);
+    for (int s = 16; s >= 1; s >>= 1)
+        for (int i = 0; i < s; ++i) p[i] = p[i] + p[i + s];
+    return p[0];
+}
+
+/* logits [T, E]; router_bias may be NULL */
+void oracle_router_logits(const uint16_t* x, int T, int H, const float* w_router, int E,
+                          const float* router_bias, float* logits) {
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            float l = orc_router_logit(x + (size_t)t * H, w_router + (size_t)e * H, H);
+            if (router_bias) l = l + router_bias[e];
+            logits[(size_t)t * E + e] = l;
+        }
+}
+
+/* R2: scores of all E experts of one token. */
+void orc_scores(const float* l, int E, int scoring, float* score) {
+    if (scoring == ORC_SOFTMAX) {
+        float m = l[0];
+        for (int e = 1; e < E; ++e) m = fmaxf(m, l[e]);
+        float q[32];
+        for (int j = 0; j < 32; ++j) q[j] = 0.0f;
+        for (int e = 0; e < E; ++e) {
+            score[e] = orc_exp(l[e] - m);
+            q[e & 31] = q[e & 31] + score[e];
+        }
+        for (int s = 16; s >= 1; s >>= 1)
+            for (int i = 0; i < s; ++i) q[i] = q[i] + q[i + s];
+        for (int e = 0; e < E; ++e) score[e] = score[e] / q[0];
+    } else if (scoring == ORC_SIGMOID) {
+        for (int e = 0; e < E; ++e) score[e] = orc_sigmoid(l[e]);
+    } else {
+        for (int e = 0; e < E; ++e) score[e] = orc_sqrtsoftplus(l[e]);
+    }
+}
+
+/* R3-R5: the k chosen logical experts of one token, in pick order. */
+int orc_select(const orc_route_cfg* c, const float* score, const float* corr_bias,
+               int32_t* chosen) {
+    const int E = c->E;
+    float* sel = (float*)malloc(sizeof(float) * E);
+    unsigned char* allowed = (unsigned char*)malloc(E);
+    if (!sel || !allowed) { free(sel); free(allowed); return -1; }
+    for (int e = 0; e < E; ++e) {
+        sel[e] = corr_bias ? score[e] + corr_bias[e] : score[e];
+        allowed[e] = 1;
+    }
+    if (c->n_group > 1) {
+        const int G = c->n_group, gs = E / G;
+        float gscore[1024];
+        unsigned char gkeep[1024];
+        for (int g = 0; g < G; ++g) {
+            float best = -INFINITY, second = -INFINITY;
+            for (int e = g * gs; e < (g + 1) * gs; ++e) {
+                if (sel[e] > best) { second = best; best = sel[e]; }
+                else if (sel[e] > second) second = sel[e];
+            }
+            gscore[g] = (c->group_score == ORC_GROUP_TOP2SUM && gs > 1) ? best + second : best;
+            gkeep[g] = 0;
+        }
+        for (int r = 0; r < c->topk_group; ++r) {
+            int bg = -1;
+            for (int g = 0; g < G; ++g)
+                if (!gkeep[g] && (bg < 0 || gscore[g] > gscore[bg])) bg = g;
+            gkeep[bg] = 1;
+        }
+        for (int e = 0; e < E; ++e) allowed[e] = gkeep[e / gs];
+    }
+    for (int j = 0; j < c->k; ++j) {
+        int be = -1;
+        for (int e = 0; e < E; ++e)
+            if (allowed[e] && (be < 0 || sel[e] > sel[be])) be = e;
+        chosen[j] = be;
+        allowed[be] = 0;
+    }
+    free(sel);
+    free(allowed);
+    return 0;
+}
+
+/*
+ * Routing of T tokens from their logits [T, E].
+ * corr_bias [E] or NULL; input_ids [T] + tid2eid [V, k] when c->use_hash;
+ * log2phy [E, R] + replica_cnt [E] or NULL (identity placement).
+ * Outputs ids_log / ids_phys int32 [T, k], weights fp32 [T, k].
+ * Returns 0, or -2 for an out-of-range token id, -3 for an out-of-range
+ * table entry, -4 for a bad placement table.
+ */
+int oracle_route(const orc_route_cfg* c, const float* logits, int T,
+                 const float* corr_bias, const int32_t* input_ids, const int32_t* tid2eid,
+                 int64_t V, const int32_t* log2phy, const int32_t* replica_cnt, int R,
+                 int32_t* ids_log, int32_t* ids_phys, float* weights) {
+    const int E = c->E, k = c->k;
+    float* score = (float*)malloc(sizeof(float) * E);
+    if (!score) return -1;
+    int rc = 0;
+    for (int t = 0; t < T && rc == 0; ++t) {
+        const float* l = logits + (size_t)t * E;
+        orc_scores(l, E, c->scoring, score);
+        int32_t* ch = ids_log + (size_t)t * k;
+        if (c->use_hash) {
+            int64_t v = input_ids[t];
+            if (v < 0 || v >= V) { rc = -2; break; }
+            for (int j = 0; j < k; ++j) {
+                int32_t e = tid2eid[v * k + j];
+                if (e < 0 || e >= E) { rc = -3; break; }
+                ch[j] = e;
+            }
+            if (rc) break;
+        } else {
+            if (orc_select(c, score, corr_bias, ch)) { rc = -1; break; }
+        }
+        float* w = weights + (size_t)t * k;
+        if (c->renormalize) {
+            float sum = 0.0f;
+            for (int j = 0; j < k; ++j) sum = sum + score[ch[j]];
+            for (int j = 0; j < k; ++j) w[j] = (score[ch[j]] / sum) * c->routed_scaling;
+        } else {
+            for (int j = 0; j < k; ++j) w[j] = score[ch[j]] * c->routed_scaling;
+        }
+        for (int j = 0; j < k; ++j) {
+            int32_t e = ch[j], p = e;
+            if (log2phy) {
+                int32_t n = replica_cnt[e];
+                if (n < 1 || n > R) { rc = -4; break; }
+                p = log2phy[(size_t)e * R + (t % n)];
+                if (p < 0 || p >= c->P) { rc = -4; break; }
+            }
+            ids_phys[(size_t)t * k + j] = p;
+        }
+    }
+    free(score);
+    return rc;
+}
+
+/* -------------------------------------------------- counts, permutation */
+void oracle_expert_counts(const int32_t* ids_phys, int T, int k, int P, int32_t* counts,
+                          int accumulate) {
+    if (!accumulate)
+        for (int p = 0; p < P; ++p) counts[p] = 0;
+    for (int64_t f = 0; f < (int64_t)T * k; ++f) counts[ids_phys[f]] += 1;
+}
+
+/* R9: stable counting sort; offsets has P+1 entries. */
+void oracle_permute(const int32_t* ids_phys, int T, int k, int P, int32_t* counts,
+                    int32_t* offsets, int32_t* row_to_token, int32_t* flat_to_row) {
+    const int64_t N = (int64_t)T * k;
+    oracle_expert_counts(ids_phys, T, k, P, counts, 0);
+    offsets[0] = 0;
+    for (int p = 0; p < P; ++p) offsets[p + 1] = offsets[p] + counts[p];
+    int32_t* cursor = (int32_t*)malloc(sizeof(int32_t) * (P > 0 ? P : 1));
+    for (int p = 0; p < P; ++p) cursor[p] = offsets[p];
+    for (int64_t f = 0; f < N; ++f) {
+        int32_t r = cursor[ids_phys[f]]++;
+        row_to_token[r] = (int32_t)(f / k);
+        flat_to_row[f] = r;
+    }
+    free(cursor);
+}
+
+/* ----------------------------------------------------------- expert MLP */
+/* One row through one SwiGLU expert (R10).
+ * wg, wu: [I, H]; wd: [H, I]; act_out [I] and y_out [H] as bf16 bits. */
+void orc_ffn_row(const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
+                 const uint16_t* wd, int H, int I, uint16_t* act_out, uint16_t* y_out) {
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        const uint16_t* rg = wg + (size_t)i * H;
+        const uint16_t* ru = wu + (size_t)i * H;
+        for (int h = 0; h < H; ++h) {
+            double xv = bf16_to_f32(x[h]);
+            g += xv * bf16_to_f32(rg[h]);
+            u += xv * bf16_to_f32(ru[h]);
+        }
+        double gf = (float)g, uf = (float)u;
+        double silu = gf / (1.0 + exp(-gf));
+        act_out[i] = f32_to_bf16((float)(silu * uf));
+    }
+    for (int h = 0; h < H; ++h) {
+        double acc = 0.0;
+        const uint16_t* rd = wd + (size_t)h * I;
+        for (int i = 0; i < I; ++i) acc += (double)bf16_to_f32(act_out[i]) * bf16_to_f32(rd[i]);
+        y_out[h] = f32_to_bf16((float)acc);
+    }
+}
+
+/* a tiny static-striped parallel-for */
+typedef struct {
+    void (*fn)(void*, int64_t);
+    void* ctx;
+    int64_t n;
+    int tid, nth;
+} orc_job;
+
+static void* orc_job_run(void* a) {
+    orc_job* j = (orc_job*)a;
+    for (int64_t i = j->tid; i < j->n; i += j->nth) j->fn(j->ctx, i);
+    return NULL;
+}
+
+static void orc_parallel_for(int64_t n, int nthreads, void (*fn)(void*, int64_t), void* ctx) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads == 1 || n < 2) {
+        for (int64_t i = 0; i < n; ++i) fn(ctx, i);
+        return;
+    }
+    pthread_t th[256];
+    orc_job jobs[256];
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = (orc_job){fn, ctx, n, t, nthreads};
+        pthread_create(&th[t], NULL, orc_job_run, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+}
+
+typedef struct {
+    const uint16_t *x, *wg, *wu, *wd;
+    const int32_t *row_to_token, *row_expert;
+    int H, I;
+    uint16_t *act, *y;
+} orc_ffn_ctx;
+
+static void orc_ffn_task(void* c_, int64_t r) {
+    orc_ffn_ctx* c = (orc_ffn_ctx*)c_;
+    int64_t t = c->row_to_token ? c->row_to_token[r] : r;
+    int64_t p = c->row_expert ? c->row_expert[r] : 0;
+    const size_t HI = (size_t)c->H * c->I;
+    orc_ffn_row(c->x + (size_t)t * c->H, c->wg + p * HI, c->wu + p * HI, c->wd + p * HI, c->H,
+                c->I, c->act + (size_t)r * c->I, c->y + (size_t)r * c->H);
+}
+
+/* Rows of n inputs through one expert: act [n, I], y [n, H]. */
+void oracle_expert_ffn_rows(const uint16_t* x, int64_t n, int H, int I, const uint16_t* wg,
+                            const uint16_t* wu, const uint16_t* wd, uint16_t* act,
+                            uint16_t* y, int nthreads) {
+    orc_ffn_ctx c = {x, wg, wu, wd, NULL, NULL, H, I, act, y};
+    orc_parallel_for(n, nthreads, orc_ffn_task, &c);
+}
+
+/* Grouped MLP over the permuted rows: row r belongs to the expert p with
+ * offsets[p] <= r < offsets[p+1] and carries token row_to_token[r].
+ * wg/wu [P, I, H], wd [P, H, I]; act [N, I], y [N, H]. */
+void oracle_ffn_grouped(const uint16_t* x, const int32_t* row_to_token, const int32_t* offsets,
+                        int P, int H, int I, const uint16_t* wg, const uint16_t* wu,
+                        const uint16_t* wd, uint16_t* act, uint16_t* y, int nthreads) {
+    int64_t N = offsets[P];
+    int32_t* row_expert = (int32_t*)malloc(sizeof(int32_t) * (N > 0 ? N : 1));
+    for (int p = 0; p < P; ++p)
+        for (int32_t r = offsets[p]; r < offsets[p + 1]; ++r) row_expert[r] = p;
+    orc_ffn_ctx c = {x, wg, wu, wd, row_to_token, row_expert, H, I, act, y};
+    orc_parallel_for(N, nthreads, orc_ffn_task, &c);
+    free(row_expert);
+}
+
+/* Restore token order and apply the routing weights (R10):
+ * out[t,h] = bf16(sum_j w[t,j] * y[flat_to_row[t*k+j], h] + ys[t,h]). */
+void oracle_combine(const uint16_t* y, const int32_t* flat_to_row, const float* weights,
+                    const uint16_t* ys, int T, int k, int H, uint16_t* out) {
+    for (int t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int64_t r = flat_to_row[(int64_t)t * k + j];
+                acc += (double)weights[(int64_t)t * k + j] * bf16_to_f32(y[r * H + h]);
+            }
+            if (ys) acc += bf16_to_f32(ys[(size_t)t * H + h]);
+            out[(size_t)t * H + h] = f32_to_bf16((float)acc);
+        }
+}
+
+/*
+ * The whole layer, stage by stage.  Weights are physical-slot stacks
+ * (wg/wu [P, I, H], wd [P, H, I]); shared-expert weights may be NULL.
+ * logits [T, E] are computed here when w_router is given, else taken as input.
+ * Scratch outputs: offsets [P+1], row_to_token / flat_to_row [T*k],
+ * act [T*k, I], y [T*k, H]; ys [T, H] when a shared expert is present.
+ */
+int oracle_moe_forward(const orc_route_cfg* c, const uint16_t* x, int T, int H, int I,
+                       const float* w_router, const float* router_bias, float* logits,
+                       const float* corr_bias, const int32_t* input_ids,
+                       const int32_t* tid2eid, int64_t V, const int32_t* log2phy,
+                       const int32_t* replica_cnt, int R, const uint16_t* wg,
+                       const uint16_t* wu, const uint16_t* wd, int I_shared,
+                       const uint16_t* wg_s, const uint16_t* wu_s, const uint16_t* wd_s,
+                       int32_t* ids_log, int32_t* ids_phys, float* weights, int32_t* counts,
+                       int32_t* offsets, int32_t* row_to_token, int32_t* flat_to_row,
+                       uint16_t* act, uint16_t* y, uint16_t* act_s, uint16_t* ys,
+                       uint16_t* out, int nthreads) {
+    if (w_router) oracle_router_logits(x, T, H, w_router, c->E, router_bias, logits);
+    int rc = oracle_route(c, logits, T, corr_bias, input_ids, tid2eid, V, log2phy, replica_cnt,
+                          R, ids_log, ids_phys, weights);
+    if (rc) return rc;
+    oracle_permute(ids_phys, T, c->k, c->P, counts, offsets, row_to_token, flat_to_row);
+    oracle_ffn_grouped(x, row_to_token, offsets, c->P, H, I, wg, wu, wd, act, y, nthreads);
+    const uint16_t* ysp = NULL;
+    if (wg_s) {
+        oracle_expert_ffn_rows(x, T, H, I_shared, wg_s, wu_s, wd_s, act_s, ys, nthreads);
+        ysp = ys;
+    }
+    oracle_combine(y, flat_to_row, weights, ysp, T, c->k, H, out);
+    return 0;
+}
