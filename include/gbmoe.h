@@ -1,0 +1,264 @@
+/*
+ * gbmoe — routed mixture-of-experts layer forward for GB300 (sm_103a).
+ *
+ * C ABI of libgbmoe.so.  The operations follow the routed-MoE forward traced
+ * on the vLLM-Ascend "Kimi K3 MoE Forward Insight" page: expert selection
+ * (section "Stage 2: Select Experts", with the routing settings listed under
+ * "Runner Initialization"), logical-to-physical mapping and token dispatch
+ * (section "Stage 4: Dispatch, MLP, Combine", AllGather row of its table),
+ * the grouped gate/up -> activation -> down expert MLP (same section), the
+ * combine that restores token order and applies the routing probabilities
+ * (same table), and per-expert token counts for load tracking (section
+ * "Stage 6: Dynamic EPLB").  On one GPU the dispatch is a local permutation:
+ * no expert parallelism and no collectives.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller (except where a
+ *    name ends in _host), row-major and contiguous with the stated shapes.
+ *    bf16 tensors are passed as uint16_t* (raw bf16 bits).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and performs no host synchronisation.  It returns
+ *    a gbmoe_status.  Argument errors are detected on the host before any
+ *    work is enqueued and leave all outputs untouched.  Errors that only the
+ *    device can see (an out-of-range id in a caller table, a pipeline wait
+ *    that gave up) are recorded in a per-device status word and reported by
+ *    gbmoe_check_device_status(); the affected outputs are then unspecified.
+ *  - T = 0 is valid and enqueues nothing (outputs of size 0).
+ *  - No exception crosses the ABI.  The library keeps one lazily created
+ *    context per device (its status word and SM count); it is thread-safe.
+ */
+#ifndef GBMOE_H
+#define GBMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gbmoe_stream_t; /* == cudaStream_t */
+
+enum gbmoe_status {
+    GBMOE_OK = 0,
+    GBMOE_ERR_INVALID_ARG = 1, /* bad shape, pointer or configuration */
+    GBMOE_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle */
+    GBMOE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    GBMOE_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+    GBMOE_ERR_DEVICE = 5,      /* a device-side check tripped (bad table entry / id) */
+    GBMOE_ERR_TIMEOUT = 6      /* a GEMM pipeline wait gave up (bounded wait) */
+};
+
+/* scoring function ("Stage 2: Select Experts": softmax, sigmoid, sqrtsoftplus) */
+enum { GBMOE_SCORE_SOFTMAX = 0, GBMOE_SCORE_SIGMOID = 1, GBMOE_SCORE_SQRTSOFTPLUS = 2 };
+/* group score used by grouped top-k */
+enum { GBMOE_GROUP_MAX = 0, GBMOE_GROUP_TOP2SUM = 1 };
+/* activation of the gate/up GEMM epilogue */
+enum { GBMOE_ACT_SWIGLU = 0 };
+
+/*
+ * Routing settings ("Runner Initialization": grouped top-k settings,
+ * renormalisation, scoring function, correction bias, routed scaling; "Entry
+ * Point": tid2eid for hash routing).
+ *   E_log       logical experts (1..1024)
+ *   E_phys      physical slots (E_log..1024); E_phys == E_log without log2phy
+ *   top_k       experts per token (1..min(E_log, 32))
+ *   n_group     expert groups for grouped top-k (1 = flat); divides E_log
+ *   topk_group  groups kept (1..n_group); topk_group * E_log/n_group >= top_k
+ *   scoring     GBMOE_SCORE_*
+ *   group_score GBMOE_GROUP_*
+ *   renormalize 1: w_j = s_j / sum_j s_j * routed_scaling; 0: s_j * routed_scaling
+ *   use_hash    1: ids come from tid2eid[input_ids[t]] (requires n_group == 1
+ *               and no correction bias)
+ * Scores s are the unbiased scoring-function values; a correction bias, when
+ * given, enters the selection only.
+ */
+typedef struct gbmoe_route_cfg {
+    int E_log;
+    int E_phys;
+    int top_k;
+    int n_group;
+    int topk_group;
+    int scoring;
+    int group_score;
+    int renormalize;
+    float routed_scaling;
+    int use_hash;
+} gbmoe_route_cfg;
+
+/* One layer: routing settings, sizes and (device) weights. */
+typedef struct gbmoe_layer {
+    gbmoe_route_cfg route;
+    int H;                        /* hidden size, multiple of 128 */
+    int I;                        /* expert intermediate size, multiple of 128 */
+    int I_shared;                 /* shared-expert intermediate (0: none), multiple of 128 */
+    const float* w_router;        /* [E_log, H] fp32 router weight */
+    const float* router_bias;     /* [E_log] fp32 added to the logits, or NULL */
+    const float* corr_bias;       /* [E_log] fp32 selection-only bias, or NULL */
+    const int32_t* tid2eid;       /* [tid2eid_rows, top_k] (use_hash) */
+    int64_t tid2eid_rows;
+    const int32_t* log2phy;       /* [E_log, R_max] physical slot of each replica, or NULL */
+    const int32_t* replica_cnt;   /* [E_log] replicas per logical expert (1..R_max) */
+    int R_max;
+    const uint16_t* w_gate;       /* [E_phys, I, H] bf16 */
+    const uint16_t* w_up;         /* [E_phys, I, H] bf16 */
+    const uint16_t* w_down;       /* [E_phys, H, I] bf16 */
+    const uint16_t* w_gate_shared;/* [I_shared, H] bf16 or NULL */
+    const uint16_t* w_up_shared;  /* [I_shared, H] bf16 or NULL */
+    const uint16_t* w_down_shared;/* [H, I_shared] bf16 or NULL */
+} gbmoe_layer;
+
+/* Text for a status code (static storage). */
+const char* gbmoe_status_string(int status);
+
+/* Host-side check of a routing configuration (GBMOE_OK or INVALID_ARG). */
+int gbmoe_validate_route_cfg(const gbmoe_route_cfg* cfg);
+
+/*
+ * Host-side check of a placement table ("Stage 6: Dynamic EPLB": every
+ * logical expert stays placed; no physical slot is shared by two logical
+ * experts).  log2phy_host [E_log, R_max], replica_cnt_host [E_log] in host
+ * memory.  Returns GBMOE_OK or GBMOE_ERR_INVALID_ARG.
+ */
+int gbmoe_validate_log2phy(const int32_t* log2phy_host, const int32_t* replica_cnt_host,
+                           int E_log, int R_max, int E_phys);
+
+/*
+ * Synchronises `stream`, then reads and clears this device's status word.
+ * *status receives GBMOE_OK or the first device-side error recorded since
+ * the last check (GBMOE_ERR_DEVICE / GBMOE_ERR_TIMEOUT).  Not for hot loops.
+ */
+int gbmoe_check_device_status(gbmoe_stream_t stream, int* status);
+
+/*
+ * moe_route — router scoring and expert selection ("Stage 2: Select
+ * Experts"), then the logical -> physical mapping ("Stage 4", step 2: map
+ * logical topk_ids through log2phy).
+ *   x            [T, H] bf16 hidden states (read when w_router != NULL)
+ *   w_router     [E_log, H] fp32, or NULL when the caller supplies logits
+ *   logits       [T, E_log] fp32: OUTPUT (router logits) when w_router is
+ *                given, INPUT otherwise; always required
+ *   router_bias  [E_log] fp32 added to computed logits, or NULL
+ *   corr_bias    [E_log] fp32 selection-only bias, or NULL
+ *   input_ids    [T] token ids (use_hash), tid2eid [tid2eid_rows, top_k]
+ *   log2phy      [E_log, R_max] + replica_cnt [E_log], or NULL (identity);
+ *                token t uses replica (t mod replica_cnt[e])
+ *   ids_log      [T, top_k] int32 logical expert ids in user token order
+ *                (the routed-expert capture of "Stage 5")
+ *   ids_phys     [T, top_k] int32 physical slots
+ *   weights      [T, top_k] fp32 routing weights
+ *   counts       [E_phys] int32 tokens per physical slot (overwritten), or NULL
+ * Selection order: slots hold experts in descending selection score, ties
+ * to the lower expert id.  Logits use a fixed fp32 summation order, so ids
+ * and weights are reproducible bit for bit.
+ */
+int moe_route(const gbmoe_route_cfg* cfg, const uint16_t* x, int T, int H,
+              const float* w_router, float* logits, const float* router_bias,
+              const float* corr_bias, const int32_t* input_ids, const int32_t* tid2eid,
+              int64_t tid2eid_rows, const int32_t* log2phy, const int32_t* replica_cnt,
+              int R_max, int32_t* ids_log, int32_t* ids_phys, float* weights, int32_t* counts,
+              gbmoe_stream_t stream);
+
+/*
+ * moe_expert_counts — tokens per physical expert ("Stage 6": expert_tokens
+ * converted to per-expert counts and added into moe_load).
+ *   ids_phys [T, k] int32; counts [E_phys] int32, overwritten (accumulate=0)
+ *   or incremented (accumulate=1).  Integer counts: deterministic.
+ */
+int moe_expert_counts(const int32_t* ids_phys, int T, int k, int E_phys, int32_t* counts,
+                      int accumulate, gbmoe_stream_t stream);
+
+/* Scratch bytes moe_permute needs for T tokens, k slots, E_phys experts. */
+size_t gbmoe_permute_workspace_size(int T, int k, int E_phys);
+
+/*
+ * moe_permute — dispatch as a local permutation ("Stage 4" table, AllGather
+ * row: sort tokens by expert and return expert token counts).
+ * Stable: row r = offsets[p] + (rank of flat index t*k+j among the pairs
+ * routed to p), so rows of one expert keep token order.  Bit-exact and
+ * deterministic (no atomics decide an order).
+ *   ids_phys     [T, k] int32 in [0, E_phys)
+ *   x            [T, H] bf16 (read only when x_perm != NULL)
+ *   counts       [E_phys] int32 out
+ *   offsets      [E_phys + 1] int32 out (exclusive scan; offsets[E_phys] = T*k)
+ *   row_to_token [T*k] int32 out; flat_to_row [T*k] int32 out
+ *   x_perm       [T*k, H] bf16 out (x_perm[r] = x[row_to_token[r]]), or NULL
+ *   ws           device scratch of ws_bytes >= gbmoe_permute_workspace_size()
+ * An id outside [0, E_phys) sets GBMOE_ERR_DEVICE and is skipped.
+ */
+int moe_permute(const int32_t* ids_phys, int T, int k, int E_phys, const uint16_t* x, int H,
+                int32_t* counts, int32_t* offsets, int32_t* row_to_token, int32_t* flat_to_row,
+                uint16_t* x_perm, void* ws, size_t ws_bytes, gbmoe_stream_t stream);
+
+/*
+ * moe_gemm_gateup_act — grouped gate/up GEMM with the activation fused into
+ * its epilogue ("Stage 4": grouped matmul gate/up -> activation; SwiGLU).
+ * For each expert p and each row r in [offsets[p], offsets[p+1]):
+ *   g = x_perm[r] . w_gate[p]^T,  u = x_perm[r] . w_up[p]^T   (fp32 accumulate)
+ *   act[r, i] = bf16(silu(g_i) * u_i),  silu(g) = g / (1 + e^-g)
+ *   x_perm [N, H] bf16; offsets [E_phys + 1] int32 on the device, or NULL for a
+ *   single group of N rows (E_phys must then be 1); w_gate, w_up [E_phys, I, H]
+ *   bf16; act [N, I] bf16 out.  H, I multiples of 128; 16-byte aligned pointers.
+ * Runs on tcgen05 tensor cores (TMEM accumulators, TMA-fed shared memory).
+ */
+int moe_gemm_gateup_act(const uint16_t* x_perm, const int32_t* offsets, int E_phys, int N, int H,
+                        int I, const uint16_t* w_gate, const uint16_t* w_up, int activation,
+                        uint16_t* act, gbmoe_stream_t stream);
+
+/*
+ * moe_gemm_down — grouped down GEMM ("Stage 4": grouped matmul down).
+ *   y[r] = bf16(act[r] . w_down[p]^T) for r in expert p's rows.
+ *   act [N, I] bf16; w_down [E_phys, H, I] bf16; y [N, H] bf16 out;
+ *   offsets as for moe_gemm_gateup_act.
+ */
+int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N, int H, int I,
+                  const uint16_t* w_down, uint16_t* y, gbmoe_stream_t stream);
+
+/*
+ * moe_combine — restore token order and apply the routing probabilities
+ * ("Stage 4" table, AllGather combine), plus the shared expert's output
+ * ("Forward Skeleton": shared experts).
+ *   out[t] = bf16( sum_{j=0..k-1} weights[t,j] * y[flat_to_row[t*k+j]] + shared_y[t] )
+ * in fp32, summed in the fixed order j = 0..k-1, then the shared term.
+ *   y [T*k, H] bf16; flat_to_row [T*k]; weights [T, k] fp32;
+ *   shared_y [T, H] bf16 or NULL; out [T, H] bf16.  H multiple of 8.
+ */
+int moe_combine(const uint16_t* y, const int32_t* flat_to_row, const float* weights,
+                const uint16_t* shared_y, int T, int k, int H, uint16_t* out,
+                gbmoe_stream_t stream);
+
+/* Scratch bytes moe_forward needs for any T <= T_max (sized from capacity,
+ * not from the runtime token count). */
+size_t gbmoe_forward_workspace_size(const gbmoe_layer* L, int T_max);
+
+/*
+ * moe_forward — the whole routed layer: route -> permute -> gate/up GEMM +
+ * SwiGLU -> down GEMM -> (shared expert) -> combine, all on `stream`.
+ *   x [T, H] bf16; input_ids [T] (hash routing) or NULL; out [T, H] bf16.
+ *   ids_log, ids_phys [T, top_k] int32, weights [T, top_k] fp32 and
+ *   counts [E_phys] int32 are optional outputs (NULL: kept in the workspace).
+ *   ws: device scratch of ws_bytes >= gbmoe_forward_workspace_size(L, T).
+ */
+int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* input_ids,
+                uint16_t* out, int32_t* ids_log, int32_t* ids_phys, float* weights,
+                int32_t* counts, void* ws, size_t ws_bytes, gbmoe_stream_t stream);
+
+/* Scratch bytes moe_forward_host needs (moe_forward's plus staging). */
+size_t gbmoe_forward_host_workspace_size(const gbmoe_layer* L, int T_max);
+
+/*
+ * moe_forward_host — moe_forward with HOST activations: copies x_host [T, H]
+ * bf16 (and input_ids_host [T], when hash routing) to the device, runs the
+ * layer, and copies out_host [T, H] (and ids_log_host [T, top_k] when not
+ * NULL) back, all enqueued on `stream`.  Host buffers should be pinned
+ * (cudaHostAlloc) for the copies to overlap; the caller synchronises
+ * `stream` before reading the outputs.  Weights stay in device memory.
+ */
+int moe_forward_host(const gbmoe_layer* L, const uint16_t* x_host, int T,
+                     const int32_t* input_ids_host, uint16_t* out_host, int32_t* ids_log_host,
+                     void* ws, size_t ws_bytes, gbmoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GBMOE_H */

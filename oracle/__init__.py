@@ -93,7 +93,7 @@ def _L():
             lib.orc_f32_to_bf16.restype = ctypes.c_uint16
             lib.orc_router_logit.argtypes = [vp, vp, i]
             lib.orc_router_logit.restype = f
-            lib.oracle_router_logits.argtypes = [vp, i, i, vp, i, vp, vp]
+            lib.oracle_router_logits.argtypes = [vp, i, i, vp, i, vp, vp, i]
             lib.oracle_router_logits.restype = None
             lib.orc_scores.argtypes = [vp, i, i, vp]
             lib.orc_scores.restype = None
@@ -152,7 +152,7 @@ def f32_to_bf16(x: float) -> int:
 
 
 # --- routing (Runner Initialization + Stage 2: Select Experts) ---
-def router_logits(x_bits, w_router, router_bias=None) -> np.ndarray:
+def router_logits(x_bits, w_router, router_bias=None, nthreads=None) -> np.ndarray:
     """fp32 logits [T, E] in the pinned summation order (reading R1)."""
     x_bits = _c(x_bits, np.uint16)
     w_router = _c(w_router, np.float32)
@@ -160,7 +160,8 @@ def router_logits(x_bits, w_router, router_bias=None) -> np.ndarray:
     E = w_router.shape[0]
     out = np.empty((T, E), dtype=np.float32)
     rb = _c(router_bias, np.float32)
-    _L().oracle_router_logits(_p(x_bits), T, H, _p(w_router), E, _p(rb), _p(out))
+    _L().oracle_router_logits(_p(x_bits), T, H, _p(w_router), E, _p(rb), _p(out),
+                              nthreads or default_threads())
     return out
 
 

@@ -174,15 +174,58 @@ float orc_router_logit(const uint16_t* x, const float* w, int H) {
     return p[0];
 }
 
-/* logits [T, E]; router_bias may be NULL */
+/* a tiny static-striped parallel-for */
+typedef struct {
+    void (*fn)(void*, int64_t);
+    void* ctx;
+    int64_t n;
+    int tid, nth;
+} orc_job;
+
+static void* orc_job_run(void* a) {
+    orc_job* j = (orc_job*)a;
+    for (int64_t i = j->tid; i < j->n; i += j->nth) j->fn(j->ctx, i);
+    return NULL;
+}
+
+static void orc_parallel_for(int64_t n, int nthreads, void (*fn)(void*, int64_t), void* ctx) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads == 1 || n < 2) {
+        for (int64_t i = 0; i < n; ++i) fn(ctx, i);
+        return;
+    }
+    pthread_t th[256];
+    orc_job jobs[256];
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = (orc_job){fn, ctx, n, t, nthreads};
+        pthread_create(&th[t], NULL, orc_job_run, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+}
+
+typedef struct {
+    const uint16_t* x;
+    const float *w, *bias;
+    int H, E;
+    float* logits;
+} orc_logit_ctx;
+
+static void orc_logit_task(void* c_, int64_t t) {
+    orc_logit_ctx* c = (orc_logit_ctx*)c_;
+    for (int e = 0; e < c->E; ++e) {
+        float l = orc_router_logit(c->x + (size_t)t * c->H, c->w + (size_t)e * c->H, c->H);
+        if (c->bias) l = l + c->bias[e];
+        c->logits[(size_t)t * c->E + e] = l;
+    }
+}
+
+/* logits [T, E]; router_bias may be NULL; tokens are independent (threads
+ * split them; each logit keeps the R1 order). */
 void oracle_router_logits(const uint16_t* x, int T, int H, const float* w_router, int E,
-                          const float* router_bias, float* logits) {
-    for (int t = 0; t < T; ++t)
-        for (int e = 0; e < E; ++e) {
-            float l = orc_router_logit(x + (size_t)t * H, w_router + (size_t)e * H, H);
-            if (router_bias) l = l + router_bias[e];
-            logits[(size_t)t * E + e] = l;
-        }
+                          const float* router_bias, float* logits, int nthreads) {
+    orc_logit_ctx c = {x, w_router, router_bias, H, E, logits};
+    orc_parallel_for(T, nthreads, orc_logit_task, &c);
 }
 
 /* R2: scores of all E experts of one token. */
@@ -356,36 +399,6 @@ void orc_ffn_row(const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
     }
 }
 
-/* a tiny static-striped parallel-for */
-typedef struct {
-    void (*fn)(void*, int64_t);
-    void* ctx;
-    int64_t n;
-    int tid, nth;
-} orc_job;
-
-static void* orc_job_run(void* a) {
-    orc_job* j = (orc_job*)a;
-    for (int64_t i = j->tid; i < j->n; i += j->nth) j->fn(j->ctx, i);
-    return NULL;
-}
-
-static void orc_parallel_for(int64_t n, int nthreads, void (*fn)(void*, int64_t), void* ctx) {
-    if (nthreads < 1) nthreads = 1;
-    if (nthreads > 256) nthreads = 256;
-    if (nthreads == 1 || n < 2) {
-        for (int64_t i = 0; i < n; ++i) fn(ctx, i);
-        return;
-    }
-    pthread_t th[256];
-    orc_job jobs[256];
-    for (int t = 0; t < nthreads; ++t) {
-        jobs[t] = (orc_job){fn, ctx, n, t, nthreads};
-        pthread_create(&th[t], NULL, orc_job_run, &jobs[t]);
-    }
-    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
-}
-
 typedef struct {
     const uint16_t *x, *wg, *wu, *wd;
     const int32_t *row_to_token, *row_expert;
@@ -459,7 +472,7 @@ int oracle_moe_forward(const orc_route_cfg* c, const uint16_t* x, int T, int H, 
                        int32_t* offsets, int32_t* row_to_token, int32_t* flat_to_row,
                        uint16_t* act, uint16_t* y, uint16_t* act_s, uint16_t* ys,
                        uint16_t* out, int nthreads) {
-    if (w_router) oracle_router_logits(x, T, H, w_router, c->E, router_bias, logits);
+    if (w_router) oracle_router_logits(x, T, H, w_router, c->E, router_bias, logits, nthreads);
     int rc = oracle_route(c, logits, T, corr_bias, input_ids, tid2eid, V, log2phy, replica_cnt,
                           R, ids_log, ids_phys, weights);
     if (rc) return rc;

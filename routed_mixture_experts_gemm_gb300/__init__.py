@@ -1,0 +1,243 @@
+"""Routed mixture-of-experts layer forward on GB300 (sm_103a).
+
+Thin Python binding over libgbmoe.so (C ABI: include/gbmoe.h).  Every step
+of the layer runs in the library's CUDA kernels; this module only marshals
+arguments (torch tensors for device memory and streams) and raises on a
+non-zero status.  There is no CPU or Python fallback: without the built
+library every call raises.
+
+Functions carry the C names: moe_route, moe_permute, moe_gemm_gateup_act,
+moe_gemm_down, moe_combine, moe_expert_counts, moe_forward, moe_forward_host.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
+
+__all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_permute",
+           "moe_gemm_gateup_act", "moe_gemm_down", "moe_combine", "MoELayer", "moe_forward",
+           "moe_forward_host", "check_device_status", "library"]
+
+
+class GbmoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _lib.load().gbmoe_status_string(status).decode()
+        super().__init__(f"{what}: {_lib.STATUS_NAMES.get(status, status)} ({msg})")
+
+
+def library():
+    return _lib.load()
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise GbmoeError(st, what)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def route_cfg(E_log: int, top_k: int, scoring="softmax", E_phys: Optional[int] = None,
+              n_group: int = 1, topk_group: int = 1, group_score="max", renormalize=True,
+              routed_scaling: float = 1.0, use_hash=False) -> RouteCfg:
+    return RouteCfg(E_log, E_log if E_phys is None else E_phys, top_k, n_group, topk_group,
+                    SCORE[scoring] if isinstance(scoring, str) else scoring,
+                    GROUP[group_score] if isinstance(group_score, str) else group_score,
+                    int(bool(renormalize)), float(routed_scaling), int(bool(use_hash)))
+
+
+def moe_route(cfg: RouteCfg, x=None, w_router=None, logits=None, router_bias=None,
+              corr_bias=None, input_ids=None, tid2eid=None, log2phy=None, replica_cnt=None,
+              with_counts=True, stream=None) -> dict:
+    """Router scoring + selection + log2phy.  Give w_router (and x) to compute
+    the logits, or logits [T, E_log] to score caller-provided logits."""
+    lib = _lib.load()
+    if w_router is not None:
+        T, H = x.shape
+        dev = x.device
+        logits = torch.empty((T, cfg.E_log), dtype=torch.float32, device=dev)
+    else:
+        T, H = logits.shape[0], 0
+        dev = logits.device
+    k = cfg.top_k
+    out = {
+        "logits": logits,
+        "ids_log": torch.empty((T, k), dtype=torch.int32, device=dev),
+        "ids_phys": torch.empty((T, k), dtype=torch.int32, device=dev),
+        "weights": torch.empty((T, k), dtype=torch.float32, device=dev),
+        "counts": torch.empty(cfg.E_phys, dtype=torch.int32, device=dev) if with_counts else None,
+    }
+    R = 1 if log2phy is None else log2phy.shape[1]
+    rows = 0 if tid2eid is None else tid2eid.shape[0]
+    st = lib.moe_route(ctypes.byref(cfg), _ptr(x) if w_router is not None else None, T, H,
+                       _ptr(w_router), _ptr(logits), _ptr(router_bias), _ptr(corr_bias),
+                       _ptr(input_ids), _ptr(tid2eid), rows, _ptr(log2phy), _ptr(replica_cnt), R,
+                       _ptr(out["ids_log"]), _ptr(out["ids_phys"]), _ptr(out["weights"]),
+                       _ptr(out["counts"]), _stream(stream))
+    _check(st, "moe_route")
+    return out
+
+
+def moe_expert_counts(ids_phys, E_phys: int, counts=None, accumulate=False, stream=None):
+    lib = _lib.load()
+    T, k = ids_phys.shape
+    if counts is None:
+        counts = torch.empty(E_phys, dtype=torch.int32, device=ids_phys.device)
+        accumulate = False
+    _check(lib.moe_expert_counts(_ptr(ids_phys), T, k, E_phys, _ptr(counts), int(accumulate),
+                                 _stream(stream)), "moe_expert_counts")
+    return counts
+
+
+def moe_permute(ids_phys, E_phys: int, x=None, ws=None, stream=None) -> dict:
+    lib = _lib.load()
+    T, k = ids_phys.shape
+    dev = ids_phys.device
+    N = T * k
+    o = {
+        "counts": torch.empty(E_phys, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E_phys + 1, dtype=torch.int32, device=dev),
+        "row_to_token": torch.empty(N, dtype=torch.int32, device=dev),
+        "flat_to_row": torch.empty(N, dtype=torch.int32, device=dev),
+        "x_perm": None if x is None else torch.empty((N, x.shape[1]), dtype=x.dtype, device=dev),
+    }
+    need = lib.gbmoe_permute_workspace_size(T, k, E_phys)
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(lib.moe_permute(_ptr(ids_phys), T, k, E_phys, _ptr(x), 0 if x is None else x.shape[1],
+                           _ptr(o["counts"]), _ptr(o["offsets"]), _ptr(o["row_to_token"]),
+                           _ptr(o["flat_to_row"]), _ptr(o["x_perm"]), _ptr(ws), ws.numel(),
+                           _stream(stream)), "moe_permute")
+    return o
+
+
+def moe_gemm_gateup_act(x_perm, offsets, w_gate, w_up, act=None, stream=None):
+    """act = bf16(silu(x W_gate^T) * (x W_up^T)) per expert group; offsets None = one group."""
+    lib = _lib.load()
+    N, H = x_perm.shape
+    P, I, _ = w_gate.shape
+    if act is None:
+        act = torch.empty((N, I), dtype=torch.bfloat16, device=x_perm.device)
+    _check(lib.moe_gemm_gateup_act(_ptr(x_perm), _ptr(offsets), P, N, H, I, _ptr(w_gate),
+                                   _ptr(w_up), ACT_SWIGLU, _ptr(act), _stream(stream)),
+           "moe_gemm_gateup_act")
+    return act
+
+
+def moe_gemm_down(act, offsets, w_down, y=None, stream=None):
+    lib = _lib.load()
+    N, I = act.shape
+    P, H, _ = w_down.shape
+    if y is None:
+        y = torch.empty((N, H), dtype=torch.bfloat16, device=act.device)
+    _check(lib.moe_gemm_down(_ptr(act), _ptr(offsets), P, N, H, I, _ptr(w_down), _ptr(y),
+                             _stream(stream)), "moe_gemm_down")
+    return y
+
+
+def moe_combine(y, flat_to_row, weights, shared_y=None, out=None, stream=None):
+    lib = _lib.load()
+    T, k = weights.shape
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
+    _check(lib.moe_combine(_ptr(y), _ptr(flat_to_row), _ptr(weights), _ptr(shared_y), T, k, H,
+                           _ptr(out), _stream(stream)), "moe_combine")
+    return out
+
+
+class MoELayer:
+    """A layer's routing settings and device weights, as the C struct moe_forward takes.
+
+    Weights are torch tensors on the device: w_router fp32 [E_log, H];
+    w_gate / w_up bf16 [E_phys, I, H]; w_down bf16 [E_phys, H, I]; optional
+    router_bias / corr_bias fp32 [E_log], tid2eid int32 [V, top_k],
+    log2phy int32 [E_log, R_max] + replica_cnt int32 [E_log], shared expert
+    (w_gate_shared, w_up_shared [I_s, H], w_down_shared [H, I_s]).
+    """
+
+    def __init__(self, cfg: RouteCfg, w_router, w_gate, w_up, w_down, router_bias=None,
+                 corr_bias=None, tid2eid=None, log2phy=None, replica_cnt=None, shared=None):
+        self.cfg = cfg
+        self._keep = [w_router, w_gate, w_up, w_down, router_bias, corr_bias, tid2eid, log2phy,
+                      replica_cnt] + list(shared or [])
+        P, I, H = w_gate.shape
+        Is = 0 if shared is None else shared[0].shape[0]
+        self.H, self.I, self.I_shared = H, I, Is
+        self.device = w_gate.device
+        s = shared or (None, None, None)
+        self.c = Layer(cfg, H, I, Is, _ptr(w_router), _ptr(router_bias), _ptr(corr_bias),
+                       _ptr(tid2eid), 0 if tid2eid is None else tid2eid.shape[0], _ptr(log2phy),
+                       _ptr(replica_cnt), 1 if log2phy is None else log2phy.shape[1],
+                       _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s[0]), _ptr(s[1]),
+                       _ptr(s[2]))
+        self._ws = None
+
+    def workspace_size(self, T_max: int, host: bool = False) -> int:
+        lib = _lib.load()
+        fn = lib.gbmoe_forward_host_workspace_size if host else lib.gbmoe_forward_workspace_size
+        n = fn(ctypes.byref(self.c), T_max)
+        if n == 0 and T_max > 0:
+            raise GbmoeError(1, "gbmoe_forward_workspace_size")
+        return n
+
+    def workspace(self, T_max: int, host: bool = False):
+        need = self.workspace_size(T_max, host)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 1), dtype=torch.uint8, device=self.device)
+        return self._ws
+
+
+def moe_forward(layer: MoELayer, x, input_ids=None, out=None, ids_log=None, ids_phys=None,
+                weights=None, counts=None, ws=None, stream=None):
+    lib = _lib.load()
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty((T, layer.H), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = layer.workspace(T)
+    _check(lib.moe_forward(ctypes.byref(layer.c), _ptr(x), T, _ptr(input_ids), _ptr(out),
+                           _ptr(ids_log), _ptr(ids_phys), _ptr(weights), _ptr(counts), _ptr(ws),
+                           ws.numel(), _stream(stream)), "moe_forward")
+    return out
+
+
+def moe_forward_host(layer: MoELayer, x_host, input_ids_host=None, out_host=None,
+                     ids_log_host=None, ws=None, stream=None):
+    """Host (ideally pinned) x in, host out; copies are enqueued on the stream.
+    Synchronise the stream before reading out_host."""
+    lib = _lib.load()
+    T = x_host.shape[0]
+    if out_host is None:
+        out_host = torch.empty((T, layer.H), dtype=torch.bfloat16, pin_memory=True)
+    if ws is None:
+        ws = layer.workspace(T, host=True)
+    _check(lib.moe_forward_host(ctypes.byref(layer.c), _ptr(x_host), T, _ptr(input_ids_host),
+                                _ptr(out_host), _ptr(ids_log_host), _ptr(ws), ws.numel(),
+                                _stream(stream)), "moe_forward_host")
+    return out_host
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronise and return (then clear) the device-side error status."""
+    lib = _lib.load()
+    st = ctypes.c_int(0)
+    _check(lib.gbmoe_check_device_status(_stream(stream), ctypes.byref(st)),
+           "gbmoe_check_device_status")
+    return st.value

@@ -1,0 +1,74 @@
+"""ctypes declarations of libgbmoe.so (the C ABI in include/gbmoe.h)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgbmoe.so")
+
+GBMOE_OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA",
+                5: "DEVICE", 6: "TIMEOUT"}
+SCORE = {"softmax": 0, "sigmoid": 1, "sqrtsoftplus": 2}
+GROUP = {"max": 0, "top2sum": 1}
+ACT_SWIGLU = 0
+
+# every function the header declares, with (restype, argtypes)
+_vp, _i, _i64, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+
+class RouteCfg(ctypes.Structure):
+    _fields_ = [("E_log", _i), ("E_phys", _i), ("top_k", _i), ("n_group", _i),
+                ("topk_group", _i), ("scoring", _i), ("group_score", _i), ("renormalize", _i),
+                ("routed_scaling", _f), ("use_hash", _i)]
+
+
+class Layer(ctypes.Structure):
+    _fields_ = [("route", RouteCfg), ("H", _i), ("I", _i), ("I_shared", _i),
+                ("w_router", _vp), ("router_bias", _vp), ("corr_bias", _vp),
+                ("tid2eid", _vp), ("tid2eid_rows", _i64), ("log2phy", _vp),
+                ("replica_cnt", _vp), ("R_max", _i), ("w_gate", _vp), ("w_up", _vp),
+                ("w_down", _vp), ("w_gate_shared", _vp), ("w_up_shared", _vp),
+                ("w_down_shared", _vp)]
+
+
+_P = ctypes.POINTER
+SIGNATURES = {
+    "gbmoe_status_string": (ctypes.c_char_p, [_i]),
+    "gbmoe_validate_route_cfg": (_i, [_P(RouteCfg)]),
+    "gbmoe_validate_log2phy": (_i, [_vp, _vp, _i, _i, _i]),
+    "gbmoe_check_device_status": (_i, [_vp, _P(_i)]),
+    "moe_route": (_i, [_P(RouteCfg), _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp,
+                       _i, _vp, _vp, _vp, _vp, _vp]),
+    "moe_expert_counts": (_i, [_vp, _i, _i, _i, _vp, _i, _vp]),
+    "gbmoe_permute_workspace_size": (_sz, [_i, _i, _i]),
+    "moe_permute": (_i, [_vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_gemm_gateup_act": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp]),
+    "moe_gemm_down": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
+    "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "gbmoe_forward_workspace_size": (_sz, [_P(Layer), _i]),
+    "moe_forward": (_i, [_P(Layer), _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "gbmoe_forward_host_workspace_size": (_sz, [_P(Layer), _i]),
+    "moe_forward_host": (_i, [_P(Layer), _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libgbmoe.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m routed_mixture_experts_gemm_gb300.build` "
+            "(there is no CPU or Python fallback for the routed-MoE kernels)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib

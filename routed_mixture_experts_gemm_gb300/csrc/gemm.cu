@@ -1,0 +1,475 @@
+// Grouped expert GEMMs on 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Follows the vLLM-Ascend "Kimi K3 MoE Forward Insight" page, section
+// "Stage 4: Dispatch, MLP, Combine": expert input -> grouped matmul gate/up
+// -> activation (SwiGLU) -> grouped matmul down, over per-expert token groups.
+//
+// Orientation ("weights as M"): every tile is D[128 weight rows x n tokens] =
+// W[128 x K] . X[n x K]^T, with the expert weight rows as the MMA's M = 128
+// operand and the expert's tokens as its N operand (N = 16..BN, a multiple of
+// 16, chosen per tile from the expert's row count).  Decode-sized groups (a
+// handful of rows per expert) then waste no tensor-core rows on padding and
+// every CTA streams distinct weight tiles; prefill-sized groups use N = BN.
+//
+// Gate/up: two A operands (W_gate and W_up rows of the same intermediate
+// block) feed two TMEM accumulators, so each thread of the epilogue holds g
+// and u of the same output and applies act = bf16(silu(g) * u) in registers.
+// Down: one A operand (W_down rows), y = bf16(acc).
+//
+// One persistent CTA per SM; warp 0 issues TMA loads (128B-swizzled K-major
+// tiles), warp 1 issues tcgen05.mma and owns TMEM (2 accumulator buffers so
+// the epilogue of tile i overlaps the main loop of tile i+1), warps 2-5 drain
+// TMEM with tcgen05.ld, stage the output tile in shared memory and write
+// coalesced 256-byte rows.  Tiles are ordered (expert, weight block, token
+// block) so CTAs working on the token blocks of one expert read the same
+// weight tile at the same time (one HBM read, L2 hits after).  The tile table
+// is built on the device from the group offsets: no host synchronisation.
+//
+// Every pipeline wait is bounded (wall-clock limit); a wait that gives up
+// raises an abort flag seen by all roles, records GBMOE_ERR_TIMEOUT, lets
+// in-flight copies and MMAs finish, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbmoe {
+namespace {
+
+constexpr int BM = 128;          // weight rows per tile (MMA M)
+constexpr int BK = 64;           // K elements per pipeline stage: one 128-byte swizzle row
+constexpr int UMMA_K = 16;       // K per tcgen05.mma kind::f16
+constexpr int BOX_ROWS = 16;     // token rows per TMA box
+constexpr int EPI_COLS = 32;     // tokens per epilogue pass
+constexpr int MAX_GROUPS = 1024;
+constexpr int NUM_THREADS = 192; // warp 0 TMA, warp 1 MMA/TMEM, warps 2..5 epilogue
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+template <int NUM_A, int BN, int STAGES>
+struct Layout {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
+    static constexpr int ACC_COLS = NUM_A * BN;
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;
+    static constexpr int OUT_BYTES = EPI_COLS * BM * 2;
+    static constexpr int TABLE_INTS = MAX_GROUPS + 4;
+    static constexpr int OFF_OUT = STAGES * STAGE_BYTES;
+    static constexpr int OFF_TILE = OFF_OUT + OUT_BYTES;
+    static constexpr int OFF_GSTART = OFF_TILE + TABLE_INTS * 4;
+    static constexpr int OFF_GCNT = OFF_GSTART + TABLE_INTS * 4;
+    static constexpr int OFF_SCAN = OFF_GCNT + TABLE_INTS * 4;
+    static constexpr int OFF_BARS = OFF_SCAN + NUM_THREADS * 4 + 16;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+    static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+    static constexpr int END = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of 2");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(BN % BOX_ROWS == 0 && BN % EPI_COLS == 0 && BN <= 256, "tile width");
+};
+
+struct GemmArgs {
+    const int32_t* offsets;  // [groups + 1] or null: one group of n_rows
+    int groups;
+    int n_rows;              // rows of the token operand
+    int R;                   // weight rows per group (I for gate/up, H for down)
+    int K;                   // reduction length
+    uint16_t* out;           // [n_rows, R] bf16
+    int* status;
+};
+
+struct Tile {
+    int p, rblk, row0, n_valid;
+};
+
+__device__ __forceinline__ Tile decode_tile(int tau, const int* tile_start, const int* gstart,
+                                            const int* gcnt, int P, int rblocks, int BN) {
+    int lo = 0, hi = P;  // largest p with tile_start[p] <= tau
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tile_start[mid] <= tau) lo = mid; else hi = mid;
+    }
+    const int p = lo;
+    const int cnt = gcnt[p];
+    const int tb = (cnt + BN - 1) / BN;
+    const int local = tau - tile_start[p];
+    Tile t;
+    t.p = p;
+    t.rblk = local / tb;
+    const int tblk = local - t.rblk * tb;
+    t.row0 = gstart[p] + tblk * BN;
+    t.n_valid = min(BN, cnt - tblk * BN);
+    return t;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier over the 128 epilogue threads that also ANDs a flag across them, so
+// the four epilogue warps take the same branch after a bounded wait.
+__device__ __forceinline__ bool epi_bar_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, __expf(-g))), u);
+}
+
+template <int NUM_A, int BN, int STAGES, bool SWIGLU>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
+                    const __grid_constant__ CUtensorMap tmA1,
+                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+    using L = Layout<NUM_A, BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint16_t* out_s = reinterpret_cast<uint16_t*>(smem + L::OFF_OUT);
+    int* tile_start = reinterpret_cast<int*>(smem + L::OFF_TILE);
+    int* gstart = reinterpret_cast<int*>(smem + L::OFF_GSTART);
+    int* gcnt = reinterpret_cast<int*>(smem + L::OFF_GCNT);
+    int* scan = reinterpret_cast<int*>(smem + L::OFF_SCAN);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BARS);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = bars + 2 * STAGES + 2;
+    uint64_t* drain = bars + 2 * STAGES + 4;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = args.groups;
+    const int rblocks = args.R / BM;
+    const int KB = args.K / BK;
+
+    // ---- set-up: barriers, TMEM, tile table
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull + b, 1);
+            mbar_init(tempty + b, 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA0);
+        if (NUM_A == 2) tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_base_s, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    {
+        // tile table: tile_start[p] = number of tiles of groups < p
+        const int seg = (P + NUM_THREADS - 1) / NUM_THREADS;
+        const int s0 = min(P, tid * seg), s1 = min(P, s0 + seg);
+        int local = 0;
+        for (int p = s0; p < s1; ++p) {
+            int off = 0, cnt = args.n_rows;
+            if (args.offsets) {
+                off = args.offsets[p];
+                cnt = args.offsets[p + 1] - off;
+                if (cnt < 0 || off < 0 || off + cnt > args.n_rows) {
+                    record_error(args.status, GBMOE_ERR_DEVICE);
+                    off = 0;
+                    cnt = 0;
+                }
+            }
+            gstart[p] = off;
+            gcnt[p] = cnt;
+            local += (cnt + BN - 1) / BN * rblocks;
+        }
+        scan[tid] = local;
+        __syncthreads();
+        if (tid == 0) {
+            int run = 0;
+            for (int i = 0; i < NUM_THREADS; ++i) {
+                const int v = scan[i];
+                scan[i] = run;
+                run += v;
+            }
+            scan[NUM_THREADS] = run;
+        }
+        __syncthreads();
+        int run = scan[tid];
+        for (int p = s0; p < s1; ++p) {
+            tile_start[p] = run;
+            run += (gcnt[p] + BN - 1) / BN * rblocks;
+        }
+        if (tid == 0) tile_start[P] = scan[NUM_THREADS];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_base_s;
+    const int total = tile_start[P];
+
+    // ---------------------------------------------------------- roles
+    if (warp == 0 && lane == 0) {
+        // TMA producer
+        const uint64_t pol_w = l2_policy_evict_first();
+        const uint64_t pol_x = l2_policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t armed = 0;          // bit s: stage s has been armed at least once
+        uint32_t armed_phase = 0;    // bit s: parity of its last armed phase
+        for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
+            const Tile tl = decode_tile(tau, tile_start, gstart, gcnt, P, rblocks, BN);
+            const int nbox = (tl.n_valid + BOX_ROWS - 1) / BOX_ROWS;
+            const uint32_t bytes = NUM_A * L::A_BYTES + nbox * BOX_ROWS * BK * 2;
+            const int a_row = tl.p * args.R + tl.rblk * BM;
+            bool ok = true;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, args.status,
+                                       kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(full + stage, bytes);
+                uint8_t* sA = smem + stage * L::STAGE_BYTES;
+                tma_load_2d(sA, &tmA0, full + stage, kb * BK, a_row, pol_w);
+                if (NUM_A == 2) tma_load_2d(sA + L::A_BYTES, &tmA1, full + stage, kb * BK, a_row, pol_w);
+                uint8_t* sB = sA + NUM_A * L::A_BYTES;
+                for (int b = 0; b < nbox; ++b)
+                    tma_load_2d(sB + b * BOX_ROWS * BK * 2, &tmB, full + stage, kb * BK,
+                                tl.row0 + b * BOX_ROWS, pol_x);
+                armed |= 1u << stage;
+                armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+        if (*abort_flag) {  // let every copy this thread issued land before exit
+            for (int s = 0; s < STAGES; ++s)
+                if ((armed >> s) & 1u)
+                    mbar_wait_timeout(full + s, (armed_phase >> s) & 1u, kDrainLimitNs);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool issued = false;
+        for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
+            const Tile tl = decode_tile(tau, tile_start, gstart, gcnt, P, rblocks, BN);
+            const int n_mma = ((tl.n_valid + 15) / 16) * 16;
+            const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
+            if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, args.status,
+                                   kWaitLimitNs))
+                break;
+            tc_fence_after();
+            const uint32_t d0 = tmem_base + acc * L::ACC_COLS;
+            bool ok = true;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait_bounded(full + stage, phase, abort_flag, args.status,
+                                       kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sA = smem_u32(smem + stage * L::STAGE_BYTES);
+                const uint32_t sB = sA + NUM_A * L::A_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < BK / UMMA_K; ++ks) {
+                    const uint64_t bdesc = smem_desc_sw128(sB + ks * UMMA_K * 2);
+#pragma unroll
+                    for (int a = 0; a < NUM_A; ++a) {
+                        const uint64_t adesc = smem_desc_sw128(sA + a * L::A_BYTES + ks * UMMA_K * 2);
+                        umma_bf16(d0 + a * BN, adesc, bdesc, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
+                issued = true;
+                umma_commit(empty + stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(tfull + acc);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (*abort_flag && issued) {  // wait for the MMAs in flight before TMEM is freed
+            umma_commit(drain);
+            mbar_wait_timeout(drain, 0u, kDrainLimitNs);
+        }
+    } else if (warp >= 2) {
+        // epilogue: TMEM -> registers -> (activation) -> bf16 -> smem -> global
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;      // weight row within the tile
+        const int etid = tid - 64;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tau = blockIdx.x; tau < total; tau += gridDim.x) {
+            const Tile tl = decode_tile(tau, tile_start, gstart, gcnt, P, rblocks, BN);
+            const bool got = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, args.status,
+                                               kWaitLimitNs);
+            if (!epi_bar_all(got)) break;
+            tc_fence_after();
+            const uint32_t tb = tmem_base + acc * L::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
+            for (int c0 = 0; c0 < tl.n_valid; c0 += EPI_COLS) {
+                uint32_t g[32];
+                tmem_ld_32x32b_x16(tb + c0, *reinterpret_cast<uint32_t(*)[16]>(g));
+                tmem_ld_32x32b_x16(tb + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(g + 16));
+                float v[32];
+                if constexpr (SWIGLU) {
+                    uint32_t u[32];
+                    tmem_ld_32x32b_x16(tb + BN + c0, *reinterpret_cast<uint32_t(*)[16]>(u));
+                    tmem_ld_32x32b_x16(tb + BN + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[c] = silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c]));
+                } else {
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(g[c]);
+                }
+                epi_bar();  // the previous pass has finished reading out_s
+#pragma unroll
+                for (int c = 0; c < 32; ++c) out_s[c * BM + r] = f32_to_bf16_bits(v[c]);
+                epi_bar();
+                const int nr = min(EPI_COLS, tl.n_valid - c0);
+                for (int i = etid; i < nr * (BM / 8); i += 128) {
+                    const int row = i / (BM / 8), vq = i % (BM / 8);
+                    const int grow = tl.row0 + c0 + row;
+                    if (grow < args.n_rows) {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            args.out + static_cast<size_t>(grow) * args.R + tl.rblk * BM + vq * 8);
+                        *dst = *reinterpret_cast<const uint4*>(out_s + row * BM + vq * 8);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty + acc);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    // ---- teardown
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------- host
+using Gemm1Layout = Layout<2, 128, 4>;
+using Gemm2Layout = Layout<1, 128, 6>;
+#define GEMM1_KERNEL grouped_gemm_kernel<2, 128, 4, true>
+#define GEMM2_KERNEL grouped_gemm_kernel<1, 128, 6, false>
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over [rows, K] (K contiguous), box = {64, box_rows}, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+std::mutex g_attr_mu;
+bool g_attr_done[64];
+
+cudaError_t ensure_attrs(int device) {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (device >= 0 && device < 64 && g_attr_done[device]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(GEMM1_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Gemm1Layout::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(GEMM2_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Gemm2Layout::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (device >= 0 && device < 64) g_attr_done[device] = true;
+    return cudaSuccess;
+}
+
+int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
+    const long bound = static_cast<long>(R / BM) * ((n_rows + BN - 1) / BN + groups);
+    return static_cast<int>(std::max<long>(1, std::min<long>(bound, num_sms)));
+}
+
+}  // namespace
+
+int gemm_max_groups() { return MAX_GROUPS; }
+
+int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int groups, int n_rows,
+                       int H, int I, const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
+                       const DevCtx& ctx, cudaStream_t s) {
+    if (n_rows == 0) return GBMOE_OK;
+    CUtensorMap ma0, ma1, mb;
+    if (!make_map(&ma0, w_gate, static_cast<uint64_t>(groups) * I, H, BM) ||
+        !make_map(&ma1, w_up, static_cast<uint64_t>(groups) * I, H, BM) ||
+        !make_map(&mb, x_rows, n_rows, H, BOX_ROWS))
+        return GBMOE_ERR_CUDA;
+    if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
+    GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
+    const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
+    GEMM1_KERNEL<<<grid, NUM_THREADS, Gemm1Layout::SMEM_BYTES, s>>>(ma0, ma1, mb, a);
+    return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
+}
+
+int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, int n_rows, int H,
+                     int I, const uint16_t* w_down, uint16_t* y, const DevCtx& ctx,
+                     cudaStream_t s) {
+    if (n_rows == 0) return GBMOE_OK;
+    CUtensorMap ma0, mb;
+    if (!make_map(&ma0, w_down, static_cast<uint64_t>(groups) * H, I, BM) ||
+        !make_map(&mb, act, n_rows, I, BOX_ROWS))
+        return GBMOE_ERR_CUDA;
+    if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
+    GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status};
+    const int grid = grid_for(groups, n_rows, H, 128, ctx.num_sms);
+    GEMM2_KERNEL<<<grid, NUM_THREADS, Gemm2Layout::SMEM_BYTES, s>>>(ma0, ma0, mb, a);
+    return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
+}
+
+}  // namespace gbmoe

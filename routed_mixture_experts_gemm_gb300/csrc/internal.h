@@ -1,0 +1,69 @@
+// Host-side launchers shared between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gbmoe.h"
+
+namespace gbmoe {
+
+struct DevCtx {
+    int device;
+    int num_sms;
+    int* status;  // device address of this device's status word
+};
+
+// Lazily created per-device context for the current device (nullptr on failure).
+const DevCtx* device_ctx();
+
+// --- routing (route.cu) ---
+struct RouteArgs {
+    gbmoe_route_cfg cfg;
+    int T, H;
+    const uint16_t* x;
+    const float* w_router;
+    float* logits;
+    const float* router_bias;
+    const float* corr_bias;
+    const int32_t* input_ids;
+    const int32_t* tid2eid;
+    int64_t tid2eid_rows;
+    const int32_t* log2phy;
+    const int32_t* replica_cnt;
+    int R_max;
+    int32_t* ids_log;
+    int32_t* ids_phys;
+    float* weights;
+    int32_t* counts;  // may be null; zeroed by the caller beforehand
+};
+cudaError_t launch_route(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s);
+cudaError_t launch_expert_counts(const int32_t* ids, int64_t n, int E_phys, int32_t* counts,
+                                 const DevCtx& ctx, cudaStream_t s);
+
+// --- permutation (permute.cu) ---
+constexpr int kPermChunk = 256;  // flat (token, slot) pairs per scatter worker
+size_t permute_ws_bytes(int64_t N, int E_phys);
+cudaError_t launch_permute(const int32_t* ids_phys, int64_t N, int k, int E_phys,
+                           const uint16_t* x, int H, int32_t* counts, int32_t* offsets,
+                           int32_t* row_to_token, int32_t* flat_to_row, uint16_t* x_perm,
+                           void* ws, const DevCtx& ctx, cudaStream_t s);
+
+// --- grouped GEMMs (gemm.cu) ---
+// Returns GBMOE_OK or an error status (tensor-map encode or launch failure).
+int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int groups, int n_rows,
+                       int H, int I, const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
+                       const DevCtx& ctx, cudaStream_t s);
+int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, int n_rows, int H,
+                     int I, const uint16_t* w_down, uint16_t* y, const DevCtx& ctx,
+                     cudaStream_t s);
+int gemm_max_groups();
+
+// --- combine (combine.cu) ---
+cudaError_t launch_combine(const uint16_t* y, const int32_t* flat_to_row, const float* weights,
+                           const uint16_t* shared_y, int T, int k, int H, uint16_t* out,
+                           const DevCtx& ctx, cudaStream_t s);
+
+}  // namespace gbmoe
