@@ -219,12 +219,12 @@ def permute(ids_phys, P):
 
 # --- expert MLP (Stage 4: grouped gate/up -> activation -> grouped down) ---
 def expert_ffn_rows(x_rows, wg, wu, wd, nthreads=None):
-    """act [n, I], y [n, H] of rows through one SwiGLU expert (bf16 bits)."""
+    """act [n, I] (bf16 bits) and y [n, H] (fp32) of rows through one SwiGLU expert."""
     x_rows = _c(x_rows, np.uint16)
     n, H = x_rows.shape
     I = wg.shape[0]
     act = np.empty((n, I), dtype=np.uint16)
-    y = np.empty((n, H), dtype=np.uint16)
+    y = np.empty((n, H), dtype=np.float32)
     _L().oracle_expert_ffn_rows(_p(x_rows), n, H, I, _p(_c(wg, np.uint16)), _p(_c(wu, np.uint16)),
                                 _p(_c(wd, np.uint16)), _p(act), _p(y),
                                 nthreads or default_threads())
@@ -236,7 +236,7 @@ def ffn_grouped(x, row_to_token, offsets, wg, wu, wd, nthreads=None):
     P, I, H = wg.shape
     N = int(offsets[P])
     act = np.empty((N, I), dtype=np.uint16)
-    y = np.empty((N, H), dtype=np.uint16)
+    y = np.empty((N, H), dtype=np.float32)
     _L().oracle_ffn_grouped(_p(x), _p(_c(row_to_token, np.int32)), _p(_c(offsets, np.int32)), P, H,
                             I, _p(_c(wg, np.uint16)), _p(_c(wu, np.uint16)),
                             _p(_c(wd, np.uint16)), _p(act), _p(y), nthreads or default_threads())
@@ -244,13 +244,14 @@ def ffn_grouped(x, row_to_token, offsets, wg, wu, wd, nthreads=None):
 
 
 def combine(y, flat_to_row, weights, ys=None):
-    """out [T, H] bf16 bits (Stage 4 AllGather combine: restore order x probabilities)."""
-    y = _c(y, np.uint16)
+    """out [T, H] bf16 bits from fp32 y [T*k, H] (and fp32 ys [T, H])
+    (Stage 4 AllGather combine: restore token order, apply the probabilities)."""
+    y = _c(y, np.float32)
     w = _c(weights, np.float32)
     T, k = w.shape
     H = y.shape[1]
     out = np.empty((T, H), dtype=np.uint16)
-    _L().oracle_combine(_p(y), _p(_c(flat_to_row, np.int32)), _p(w), _p(_c(ys, np.uint16)), T, k,
+    _L().oracle_combine(_p(y), _p(_c(flat_to_row, np.int32)), _p(w), _p(_c(ys, np.float32)), T, k,
                         H, _p(out))
     return out
 
@@ -270,7 +271,7 @@ def moe_forward(cfg: RouteCfg, x, H, I, w_router=None, logits=None, router_bias=
         "weights": np.empty((T, k), np.float32), "counts": np.empty(P, np.int32),
         "offsets": np.empty(P + 1, np.int32), "row_to_token": np.empty(N, np.int32),
         "flat_to_row": np.empty(N, np.int32), "act": np.empty((N, I), np.uint16),
-        "y": np.empty((N, H), np.uint16), "out": np.empty((T, H), np.uint16),
+        "y": np.empty((N, H), np.float32), "out": np.empty((T, H), np.uint16),
     }
     Is = 0
     sg = su = sd = None
@@ -278,7 +279,7 @@ def moe_forward(cfg: RouteCfg, x, H, I, w_router=None, logits=None, router_bias=
         sg, su, sd = (_c(a, np.uint16) for a in shared)
         Is = sg.shape[0]
         o["act_s"] = np.empty((T, Is), np.uint16)
-        o["ys"] = np.empty((T, H), np.uint16)
+        o["ys"] = np.empty((T, H), np.float32)
     tt = _c(tid2eid, np.int32)
     lp = _c(log2phy, np.int32)
     rc = _L().oracle_moe_forward(

@@ -47,9 +47,11 @@
  *   R8 replica of logical e for token t: log2phy[e][t mod replica_cnt[e]].
  *   R9 permutation: stable counting sort of the flat index f = t*k + j by
  *      physical expert; row r = offsets[p] + rank of f among equal p.
- *   R10 rounding points: act = bf16(silu(g) * u) with g, u held in fp32;
- *      y = bf16(act . Wd); shared ys = bf16(...); out = bf16(sum_j w_j y_j + ys).
- *      Dot products of the expert MLP accumulate in double (exact products).
+ *   R10 rounding points: only the activation is rounded to bf16 inside the
+ *      layer (it is the input of the down matmul): act = bf16(silu(g) * u)
+ *      with g, u held in fp32; the expert outputs y = act . Wd and the shared
+ *      expert's ys stay fp32; out = bf16(sum_j w_j y_j + ys).  Dot products
+ *      of the expert MLP accumulate in double (exact products).
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared -pthread
  * (-ffp-contract=off keeps every a*b+c below as two rounded operations unless
@@ -375,9 +377,9 @@ void oracle_permute(const int32_t* ids_phys, int T, int k, int P, int32_t* count
 
 /* ----------------------------------------------------------- expert MLP */
 /* One row through one SwiGLU expert (R10).
- * wg, wu: [I, H]; wd: [H, I]; act_out [I] and y_out [H] as bf16 bits. */
+ * wg, wu: [I, H]; wd: [H, I]; act_out [I] as bf16 bits, y_out [H] fp32. */
 void orc_ffn_row(const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
-                 const uint16_t* wd, int H, int I, uint16_t* act_out, uint16_t* y_out) {
+                 const uint16_t* wd, int H, int I, uint16_t* act_out, float* y_out) {
     for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         const uint16_t* rg = wg + (size_t)i * H;
@@ -395,7 +397,7 @@ void orc_ffn_row(const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
         double acc = 0.0;
         const uint16_t* rd = wd + (size_t)h * I;
         for (int i = 0; i < I; ++i) acc += (double)bf16_to_f32(act_out[i]) * bf16_to_f32(rd[i]);
-        y_out[h] = f32_to_bf16((float)acc);
+        y_out[h] = (float)acc;
     }
 }
 
@@ -403,7 +405,8 @@ typedef struct {
     const uint16_t *x, *wg, *wu, *wd;
     const int32_t *row_to_token, *row_expert;
     int H, I;
-    uint16_t *act, *y;
+    uint16_t* act;
+    float* y;
 } orc_ffn_ctx;
 
 static void orc_ffn_task(void* c_, int64_t r) {
@@ -415,20 +418,20 @@ static void orc_ffn_task(void* c_, int64_t r) {
                 c->I, c->act + (size_t)r * c->I, c->y + (size_t)r * c->H);
 }
 
-/* Rows of n inputs through one expert: act [n, I], y [n, H]. */
+/* Rows of n inputs through one expert: act [n, I] bf16, y [n, H] fp32. */
 void oracle_expert_ffn_rows(const uint16_t* x, int64_t n, int H, int I, const uint16_t* wg,
                             const uint16_t* wu, const uint16_t* wd, uint16_t* act,
-                            uint16_t* y, int nthreads) {
+                            float* y, int nthreads) {
     orc_ffn_ctx c = {x, wg, wu, wd, NULL, NULL, H, I, act, y};
     orc_parallel_for(n, nthreads, orc_ffn_task, &c);
 }
 
 /* Grouped MLP over the permuted rows: row r belongs to the expert p with
  * offsets[p] <= r < offsets[p+1] and carries token row_to_token[r].
- * wg/wu [P, I, H], wd [P, H, I]; act [N, I], y [N, H]. */
+ * wg/wu [P, I, H], wd [P, H, I]; act [N, I] bf16, y [N, H] fp32. */
 void oracle_ffn_grouped(const uint16_t* x, const int32_t* row_to_token, const int32_t* offsets,
                         int P, int H, int I, const uint16_t* wg, const uint16_t* wu,
-                        const uint16_t* wd, uint16_t* act, uint16_t* y, int nthreads) {
+                        const uint16_t* wd, uint16_t* act, float* y, int nthreads) {
     int64_t N = offsets[P];
     int32_t* row_expert = (int32_t*)malloc(sizeof(int32_t) * (N > 0 ? N : 1));
     for (int p = 0; p < P; ++p)
@@ -439,17 +442,17 @@ void oracle_ffn_grouped(const uint16_t* x, const int32_t* row_to_token, const in
 }
 
 /* Restore token order and apply the routing weights (R10):
- * out[t,h] = bf16(sum_j w[t,j] * y[flat_to_row[t*k+j], h] + ys[t,h]). */
-void oracle_combine(const uint16_t* y, const int32_t* flat_to_row, const float* weights,
-                    const uint16_t* ys, int T, int k, int H, uint16_t* out) {
+ * out[t,h] = bf16(sum_j w[t,j] * y[flat_to_row[t*k+j], h] + ys[t,h]); y, ys fp32. */
+void oracle_combine(const float* y, const int32_t* flat_to_row, const float* weights,
+                    const float* ys, int T, int k, int H, uint16_t* out) {
     for (int t = 0; t < T; ++t)
         for (int h = 0; h < H; ++h) {
             double acc = 0.0;
             for (int j = 0; j < k; ++j) {
                 int64_t r = flat_to_row[(int64_t)t * k + j];
-                acc += (double)weights[(int64_t)t * k + j] * bf16_to_f32(y[r * H + h]);
+                acc += (double)weights[(int64_t)t * k + j] * (double)y[r * H + h];
             }
-            if (ys) acc += bf16_to_f32(ys[(size_t)t * H + h]);
+            if (ys) acc += (double)ys[(size_t)t * H + h];
             out[(size_t)t * H + h] = f32_to_bf16((float)acc);
         }
 }
@@ -459,7 +462,8 @@ void oracle_combine(const uint16_t* y, const int32_t* flat_to_row, const float* 
  * (wg/wu [P, I, H], wd [P, H, I]); shared-expert weights may be NULL.
  * logits [T, E] are computed here when w_router is given, else taken as input.
  * Scratch outputs: offsets [P+1], row_to_token / flat_to_row [T*k],
- * act [T*k, I], y [T*k, H]; ys [T, H] when a shared expert is present.
+ * act [T*k, I] bf16, y [T*k, H] fp32; ys [T, H] fp32 when a shared expert is
+ * present.
  */
 int oracle_moe_forward(const orc_route_cfg* c, const uint16_t* x, int T, int H, int I,
                        const float* w_router, const float* router_bias, float* logits,
@@ -470,7 +474,7 @@ int oracle_moe_forward(const orc_route_cfg* c, const uint16_t* x, int T, int H, 
                        const uint16_t* wg_s, const uint16_t* wu_s, const uint16_t* wd_s,
                        int32_t* ids_log, int32_t* ids_phys, float* weights, int32_t* counts,
                        int32_t* offsets, int32_t* row_to_token, int32_t* flat_to_row,
-                       uint16_t* act, uint16_t* y, uint16_t* act_s, uint16_t* ys,
+                       uint16_t* act, float* y, uint16_t* act_s, float* ys,
                        uint16_t* out, int nthreads) {
     if (w_router) oracle_router_logits(x, T, H, w_router, c->E, router_bias, logits, nthreads);
     int rc = oracle_route(c, logits, T, corr_bias, input_ids, tid2eid, V, log2phy, replica_cnt,
@@ -478,7 +482,7 @@ int oracle_moe_forward(const orc_route_cfg* c, const uint16_t* x, int T, int H, 
     if (rc) return rc;
     oracle_permute(ids_phys, T, c->k, c->P, counts, offsets, row_to_token, flat_to_row);
     oracle_ffn_grouped(x, row_to_token, offsets, c->P, H, I, wg, wu, wd, act, y, nthreads);
-    const uint16_t* ysp = NULL;
+    const float* ysp = NULL;
     if (wg_s) {
         oracle_expert_ffn_rows(x, T, H, I_shared, wg_s, wu_s, wd_s, act_s, ys, nthreads);
         ysp = ys;

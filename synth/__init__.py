@@ -169,7 +169,7 @@ def _fmix32_t(h):
 
 
 def _draw_t(k: int, i):
-    return _fmix32_t(((i + 0x61C88647) & _M32) ^ k)
+    return _fmix32_t(_fmix32_t((i + 0x61C88647) & _M32) ^ k)
 
 
 def normal_bf16_device(seed: int, tag: int, slab: int, n: int, sigma: float, device,

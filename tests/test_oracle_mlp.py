@@ -27,13 +27,21 @@ def _f(bits):
 
 
 def _ffn_dense(x_bits, wg, wu, wd):
-    """SwiGLU expert by library matmuls: act = bf16(silu(g) u), y = bf16(act Wd^T)."""
+    """SwiGLU expert by library matmuls: act = bf16(silu(g) u), y = fp32(act Wd^T)."""
     x = _f(x_bits)
     g = (x @ _f(wg).T).astype(np.float32).astype(np.float64)
     u = (x @ _f(wu).T).astype(np.float32).astype(np.float64)
     act = _bf16_bits(g / (1 + np.exp(-g)) * u)
-    y = _bf16_bits(_f(act) @ _f(wd).T)
+    y = (_f(act) @ _f(wd).T).astype(np.float32)
     return act, y
+
+
+def _close_f32(a, b, ulps=2):
+    """fp32 arrays equal to within a couple of ulps (double sums in other orders)."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    sp = np.spacing(np.abs(b).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(a - b) <= ulps * sp + 1e-30)
 
 
 def _close_bf16(a_bits, b_bits, max_ulps=1, frac=0.999):
@@ -53,7 +61,7 @@ def test_expert_rows_match_library_matmul(rng):
     act, y = oracle.expert_ffn_rows(d["x"][:40], wg, wu, wd, nthreads=4)
     act_r, y_r = _ffn_dense(d["x"][:40], wg, wu, wd)
     _close_bf16(act, act_r)
-    _close_bf16(y, y_r)
+    _close_f32(y, y_r)
 
 
 @pytest.mark.parametrize("name", ["tiny", "mini_decode", "mini_hash", "mini_skew"])
@@ -71,10 +79,10 @@ def test_routed_output_matches_dense_brute_force(name):
             mask[t, o["ids_phys"][t, j]] += o["weights"][t, j]
     for p in range(cfg.P):
         _, y = _ffn_dense(d["x"], W[0][p], W[1][p], W[2][p])
-        dense += mask[:, p:p + 1] * _f(y)
+        dense += mask[:, p:p + 1] * y.astype(np.float64)
     sw = synth.shared_weights_host(cfg)
     if sw is not None:
-        dense += _f(_ffn_dense(d["x"], *sw)[1])
+        dense += _ffn_dense(d["x"], *sw)[1].astype(np.float64)
     _close_bf16(o["out"], _bf16_bits(dense), frac=0.995)
     # stage outputs are consistent with the permutation
     assert np.array_equal(o["counts"], np.bincount(o["ids_phys"].ravel(),
@@ -91,7 +99,7 @@ def test_single_expert_is_plain_swiglu_mlp(rng):
                            wg=wg[None], wu=wu[None], wd=wd[None], nthreads=2)
     assert np.all(o["weights"] == 1.0)
     _, y = _ffn_dense(x, wg, wu, wd)
-    _close_bf16(o["out"], y)
+    _close_bf16(o["out"], _bf16_bits(y))
 
 
 def test_all_experts_softmax_is_dense_softmax_mixture(rng):
@@ -105,7 +113,7 @@ def test_all_experts_softmax_is_dense_softmax_mixture(rng):
                            wg=wg, wu=wu, wd=wd, nthreads=2)
     p = np.exp(l - l.max(1, keepdims=True))
     p /= p.sum(1, keepdims=True)
-    dense = sum(p[:, e:e + 1] * _f(_ffn_dense(x, wg[e], wu[e], wd[e])[1]) for e in range(E))
+    dense = sum(p[:, e:e + 1] * _ffn_dense(x, wg[e], wu[e], wd[e])[1] for e in range(E))
     _close_bf16(o["out"], _bf16_bits(dense), frac=0.99)
 
 
@@ -133,14 +141,14 @@ def test_replicated_placement_equals_identity_placement():
 def test_combine_restores_token_order(rng):
     T, k, H = 7, 3, 16
     N = T * k
-    y = _bf16_bits(rng.standard_normal((N, H)))
+    y = rng.standard_normal((N, H)).astype(np.float32)
     f2r = rng.permutation(N).astype(np.int32)
     w = rng.random((T, k)).astype(np.float32)
-    ys = _bf16_bits(rng.standard_normal((T, H)))
+    ys = rng.standard_normal((T, H)).astype(np.float32)
     out = oracle.combine(y, f2r, w, ys)
     ref = np.zeros((T, H))
     for t in range(T):
         for j in range(k):
-            ref[t] += float(w[t, j]) * _f(y[f2r[t * k + j]])
-    ref += _f(ys)
+            ref[t] += float(w[t, j]) * y[f2r[t * k + j]].astype(np.float64)
+    ref += ys
     _close_bf16(out, _bf16_bits(ref), frac=1.0)

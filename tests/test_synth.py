@@ -38,3 +38,11 @@ def test_uniform_ids_and_rows():
     assert all(len(set(r)) == 8 for r in rows)
     counts = np.bincount(rows.ravel(), minlength=384)
     assert counts.min() > 0.8 * counts.mean()
+
+
+def test_torch_restatement_matches_c_generator():
+    import torch
+    n = 3 * 4096 + 17
+    d = synth.normal_bf16_device(5, synth.TAG_WU, 9, n, 0.02, "cpu")
+    h = synth.normal_bf16(5, synth.TAG_WU, 9, n, 0.02)
+    assert np.array_equal(d.view(torch.int16).numpy().view(np.uint16), h)
