@@ -1,0 +1,529 @@
+"""Benchmark of the routed-MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+                    [--impl reference]
+
+One step = one moe_forward over one batch of the workload (router scoring and
+grouped top-k, permutation, grouped gate/up GEMM + SwiGLU, grouped down GEMM,
+combine; shared expert where the workload has one), inputs and weights
+resident in HBM.  Prints ONE JSON line (rank 0):
+
+  value     tokens/s of the headline workload (decode shape, T=128), device
+            time by CUDA events on the launching stream, max over ranks
+  e2e       the same metric through moe_forward_host with pinned host
+            buffers: host->device copy of x and device->host copy of out
+            inside the timed region
+  prefill   the same measurement at T=8192 (the metric's second batch size)
+  roofline  the dominant kernel (the gate/up grouped GEMM) against the
+            measured peak: HBM bytes of the touched experts for decode,
+            tensor FLOPs for prefill
+  cpu_baseline  the CPU oracle timed on this host on a bounded token sample
+
+--impl reference times the CPU oracle itself (the only reference there is:
+the pages publish no implementation), on the same workload and metric.
+
+Multi-GPU (torchrun, N > 1): every rank runs an independent replica of the
+workload (weak scaling, no collective on the data path); value = tokens all
+ranks processed / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at T=128 and T=8192; % of HBM / bf16 TC roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_SOURCES = ["routed_mixture_experts_gemm_gb300/csrc/gemm.cu",
+                "routed_mixture_experts_gemm_gb300/csrc/common.cuh"]
+
+# small twins of the decode / prefill shapes for ncu captures (weights > L2,
+# a few GB on the device): same H, I, k and rows-per-expert character
+PROFILE_WORKLOADS = {
+    "decode_e16": synth.MoEConfig("decode_e16", 21, T=8, H=7168, I=2048, E=16, k=8,
+                                  scoring="sigmoid", n_group=8, topk_group=4,
+                                  routed_scaling=2.5, corr_bias_sigma=0.1),
+    "prefill_e16": synth.MoEConfig("prefill_e16", 22, T=512, H=7168, I=2048, E=16, k=8,
+                                   scoring="sigmoid", n_group=8, topk_group=4,
+                                   routed_scaling=2.5, corr_bias_sigma=0.1, router_sigma=None),
+}
+
+
+def workload(name):
+    if name in synth.CONFIGS:
+        return synth.CONFIGS[name]
+    return PROFILE_WORKLOADS[name]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, wl: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}/{wl}")
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- GPU path
+class Workload:
+    """Device inputs, weights and preallocated buffers of one workload."""
+
+    def __init__(self, cfg, device):
+        import torch
+        from synth.device import device_case
+        import routed_mixture_experts_gemm_gb300 as gb
+        self.cfg = cfg
+        self.gb = gb
+        self.lib = gb.library()
+        self.case = device_case(cfg, device, host_weights=False)
+        T, k, P = cfg.T, cfg.k, cfg.P
+        self.torch = torch
+        self.out = torch.empty((T, cfg.H), dtype=torch.bfloat16, device=device)
+        self.ids = torch.empty((T, k), dtype=torch.int32, device=device)
+        self.idp = torch.empty((T, k), dtype=torch.int32, device=device)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=device)
+        self.counts = torch.empty(P, dtype=torch.int32, device=device)
+        self.ws = self.case.layer.workspace(T)
+        # staged buffers (same kernels as moe_forward, one call per stage)
+        N = T * k
+        e = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device=device)  # noqa: E731
+        self.logits = e(T, cfg.E, dt=torch.float32)
+        self.offsets = e(P + 1, dt=torch.int32)
+        self.r2t = e(N, dt=torch.int32)
+        self.f2r = e(N, dt=torch.int32)
+        self.x_perm = e(N, cfg.H)
+        self.act = e(N, cfg.I)
+        self.y = e(N, cfg.H, dt=torch.float32)
+        if cfg.shared_I:
+            self.act_s = e(T, cfg.shared_I)
+            self.ys = e(T, cfg.H, dt=torch.float32)
+        self.pws = e(max(1, self.lib.gbmoe_permute_workspace_size(T, k, P)), dt=torch.uint8)
+        self.stream = torch.cuda.current_stream()
+
+    def forward(self):
+        c = self.case
+        self.gb.moe_forward(c.layer, c.x, input_ids=c.input_ids, out=self.out, ids_log=self.ids,
+                            ids_phys=self.idp, weights=self.w, counts=self.counts, ws=self.ws,
+                            stream=self.stream)
+
+    def staged(self, ev):
+        """The forward as separate C-ABI calls with an event after each stage."""
+        L, cfg, c, s = self.lib, self.cfg, self.case, self.stream.cuda_stream
+        d = c.dev
+        p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        R = 1 if d["log2phy"] is None else d["log2phy"].shape[1]
+        rows = 0 if d["tid2eid"] is None else d["tid2eid"].shape[0]
+        T, k, P, H, I = cfg.T, cfg.k, cfg.P, cfg.H, cfg.I
+        N = T * k
+        ev[0].record(self.stream)
+        st = L.moe_route(ctypes.byref(c.layer.cfg), p(c.x), T, H, p(d["w_router"]), p(self.logits),
+                         p(d["router_bias"]), p(d["corr_bias"]), p(c.input_ids), p(d["tid2eid"]),
+                         rows, p(d["log2phy"]), p(d["replica_cnt"]), R, p(self.ids), p(self.idp),
+                         p(self.w), None, s)
+        ev[1].record(self.stream)
+        st |= L.moe_permute(p(self.idp), T, k, P, p(c.x), H, p(self.counts), p(self.offsets),
+                            p(self.r2t), p(self.f2r), p(self.x_perm), p(self.pws),
+                            self.pws.numel(), s)
+        ev[2].record(self.stream)
+        st |= L.moe_gemm_gateup_act(p(self.x_perm), p(self.offsets), P, N, H, I, p(d["w_gate"]),
+                                    p(d["w_up"]), 0, p(self.act), s)
+        ev[3].record(self.stream)
+        st |= L.moe_gemm_down(p(self.act), p(self.offsets), P, N, H, I, p(d["w_down"]), p(self.y),
+                              s)
+        ev[4].record(self.stream)
+        ys = None
+        if cfg.shared_I:
+            sg, su, sd = d["shared"]
+            st |= L.moe_gemm_gateup_act(p(c.x), None, 1, T, H, cfg.shared_I, p(sg), p(su), 0,
+                                        p(self.act_s), s)
+            st |= L.moe_gemm_down(p(self.act_s), None, 1, T, H, cfg.shared_I, p(sd), p(self.ys), s)
+            ys = self.ys
+        ev[5].record(self.stream)
+        st |= L.moe_combine(p(self.y), p(self.f2r), p(self.w), p(ys), T, k, H, p(self.out), s)
+        ev[6].record(self.stream)
+        if st:
+            raise RuntimeError(f"staged forward failed (status bits {st})")
+
+    def launches_per_step(self):
+        cfg = self.cfg
+        # route: logits + select; permute: hist, column scan, scatter, gather;
+        # gate/up GEMM, down GEMM (+2 for the shared expert); combine
+        return 2 + 4 + 2 + (2 if cfg.shared_I else 0) + 1
+
+
+def time_device(fn, steps, warmup, torch, barrier=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1) / 1000.0
+
+
+def stage_times(wl, steps, torch):
+    names = ["route", "permute", "gemm_gateup", "gemm_down", "shared_expert", "combine"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for _ in range(3):
+        wl.staged(evs[0])
+    torch.cuda.synchronize()
+    for i in range(steps):
+        wl.staged(evs[i])
+    torch.cuda.synchronize()
+    out = {}
+    for j, n in enumerate(names):
+        out[n] = sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
+    return out  # ms per step
+
+
+def touched_bytes(cfg, counts):
+    """Algorithmic bytes of the gate/up GEMM: weights of experts with rows,
+    the permuted activations read and the SwiGLU output written."""
+    touched = int((counts > 0).sum())
+    w = touched * 2 * cfg.I * cfg.H * 2
+    xa = cfg.N * cfg.H * 2 + cfg.N * cfg.I * 2
+    return w + xa, touched
+
+
+def e2e_time(wl, steps, warmup, torch):
+    import routed_mixture_experts_gemm_gb300 as gb
+    c = wl.case
+    cfg = wl.cfg
+    x_h = c.x.cpu().pin_memory()
+    ids_h = c.input_ids.cpu().pin_memory() if c.input_ids is not None else None
+    out_h = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    ws = c.layer.workspace(cfg.T, host=True)
+    fn = lambda: gb.moe_forward_host(c.layer, x_h, input_ids_host=ids_h, out_host=out_h,  # noqa
+                                     ws=ws, stream=wl.stream)
+    t = time_device(fn, steps, warmup, torch)
+    h2d = cfg.T * cfg.H * 2 + (cfg.T * 4 if ids_h is not None else 0)
+    d2h = cfg.T * cfg.H * 2
+    return t, h2d, d2h
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_step(cfg, d, tokens, cache, nthreads):
+    """The CPU oracle over a sample of tokens: routing, permutation, every
+    touched expert's SwiGLU on its rows, combine.  Returns seconds of oracle
+    time (expert weights are generated beforehand, outside the timing)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    pl = d["placement"]
+    x = np.ascontiguousarray(d["x"][tokens])
+    ids_in = d["input_ids"][tokens] if d["input_ids"] is not None else None
+    t0 = time.perf_counter()
+    lg = oracle.router_logits(x, d["w_router"], d["router_bias"], nthreads=nthreads)
+    t_route = time.perf_counter() - t0
+    # replica choice uses the token's batch position: route the sample with
+    # its own positions (the sample is a prefix of the batch)
+    ids, idp, w = oracle.route(oracle.cfg_from(cfg), lg, corr_bias=d["corr_bias"],
+                               input_ids=ids_in, tid2eid=d["tid2eid"], log2phy=pl.log2phy,
+                               replica_cnt=pl.replica_cnt)
+    counts, offs, r2t, f2r = oracle.permute(idp, cfg.P)
+    t_route = time.perf_counter() - t0
+    need = [p for p in range(cfg.P) if counts[p] > 0]
+    for p in need:
+        e = int(pl.phys_to_log[p])
+        if e not in cache:
+            cache[e] = synth.expert_weights_host(cfg, e)
+    y = np.empty((len(tokens) * cfg.k, cfg.H), np.uint16)
+
+    def one(p):
+        e = int(pl.phys_to_log[p])
+        rows = np.arange(offs[p], offs[p + 1])
+        a0 = time.perf_counter()
+        _, yp = oracle.expert_ffn_rows(x[r2t[rows]], *cache[e], nthreads=1)
+        y[rows] = yp
+        return time.perf_counter() - a0
+
+    t1 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=nthreads) as ex:
+        list(ex.map(one, need))
+    ys = None
+    if cfg.shared_I:
+        if "shared" not in cache:
+            cache["shared"] = synth.shared_weights_host(cfg)
+        _, ys = oracle.expert_ffn_rows(x, *cache["shared"], nthreads=nthreads)
+    oracle.combine(y, f2r, w, ys)
+    return t_route + (time.perf_counter() - t1)
+
+
+def cpu_baseline(cfg, n_tokens, nthreads, reps=1, cache=None):
+    d = synth.make_inputs(cfg)
+    cache = {} if cache is None else cache
+    tokens = np.arange(min(n_tokens, cfg.T))
+    oracle_step(cfg, d, tokens, cache, nthreads)  # generates and caches weights, warms up
+    secs = [oracle_step(cfg, d, tokens, cache, nthreads) for _ in range(reps)]
+    sec = float(np.mean(secs))
+    return {"value": len(tokens) / sec, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"first {len(tokens)} of the {cfg.T} tokens of the {cfg.name} workload "
+                      f"(routing, permutation, every touched expert's SwiGLU, combine); "
+                      f"tokens/s = sample tokens / oracle seconds, mean of {reps}",
+            "seconds": sec}
+
+
+# ------------------------------------------------------------ aggregation
+def aggregate(times, tokens_per_rank, steps):
+    """Whole-job throughput from per-rank elapsed seconds (max over ranks)."""
+    t = max(times)
+    return {"value": len(times) * tokens_per_rank * steps / t, "seconds": t,
+            "ms_per_step": 1000.0 * t / steps}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--secondary", default="prefill",
+                    help="second workload reported in the same line ('' to skip)")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+    cfg = workload(args.workload)
+    nthreads = os.cpu_count() or 1
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        cache = {}
+        d = synth.make_inputs(cfg)
+        n = max(1, min(cfg.T, 4))
+        tokens = np.arange(n)
+        for _ in range(max(args.warmup, 1)):
+            oracle_step(cfg, d, tokens, cache, nthreads)
+        secs = sum(oracle_step(cfg, d, tokens, cache, nthreads) for _ in range(args.steps))
+        value = n * args.steps / secs
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64 (CPU oracle)",
+                "data": "synthetic (seeded generator)",
+                "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E,
+                           "I": cfg.I, "k": cfg.k},
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads,
+                                 "kind": "oracle",
+                                 "sample": f"first {n} tokens of the {cfg.name} batch per step"},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        barrier = dist.barrier
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if barrier:
+        barrier()
+    __graft_entry__.build()
+
+    wl = Workload(cfg, dev)
+    wl.forward()
+    torch.cuda.synchronize()
+    import routed_mixture_experts_gemm_gb300 as gb
+    st = gb.check_device_status()
+    if st:
+        raise RuntimeError(f"device status {st} after the first forward")
+
+    with ClockSampler(local) as clk:
+        secs = time_device(wl.forward, args.steps, args.warmup, torch, barrier)
+    clocks = clk.summary()
+    times = [secs]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([secs], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        times = [float(t.item())] * world
+    agg = aggregate(times, cfg.T, args.steps)
+
+    stages = stage_times(wl, min(args.steps, 20), torch)
+    counts = wl.counts.cpu().numpy()
+    peaks, peak_src = load_peaks()
+    alg_bytes, touched = touched_bytes(cfg, counts)
+    g1 = stages["gemm_gateup"] / 1000.0
+    hbm = peaks["hbm_gbs"]
+    roof = {"kernel": "grouped_gemm gate/up + SwiGLU (tcgen05)", "bound": "hbm",
+            "achieved": alg_bytes / g1 / 1e9, "peak": hbm, "unit": "GB/s",
+            "frac": alg_bytes / g1 / 1e9 / hbm,
+            "traffic": profiled_traffic("gemm_gateup", cfg.name),
+            "algorithmic_bytes": alg_bytes, "touched_experts": touched,
+            "peak_source": f"{peak_src} hbm_gbs"}
+    t_e2e, h2d, d2h = e2e_time(wl, args.steps, args.warmup, torch)
+    e2e = {"value": world * cfg.T * args.steps / t_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    line = {
+        "metric": METRIC, "value": agg["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": agg["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator; random-init expert weights)",
+        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "P": cfg.P,
+                   "I": cfg.I, "k": cfg.k, "scoring": cfg.scoring, "n_group": cfg.n_group,
+                   "topk_group": cfg.topk_group, "seed": cfg.seed,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (the step streams the touched experts' weights, "
+                         f"{touched * 3 * cfg.I * cfg.H * 2 / 1e9:.1f} GB); no flush"},
+        "roofline": roof, "stages_ms": stages, "e2e": e2e,
+        "gpu_launches": wl.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    del wl
+    torch.cuda.empty_cache()
+
+    if args.secondary:
+        c2 = workload(args.secondary)
+        w2 = Workload(c2, dev)
+        w2.forward()
+        s2 = time_device(w2.forward, max(3, args.steps // 2), args.warmup, torch, barrier)
+        stg2 = stage_times(w2, min(args.steps, 10), torch)
+        steps2 = max(3, args.steps // 2)
+        flops = 2.0 * c2.N * 2 * c2.H * c2.I
+        g1b = stg2["gemm_gateup"] / 1000.0
+        peak_t = peaks["bf16_tflops_sustained"]
+        line["prefill" if args.secondary == "prefill" else args.secondary] = {
+            "workload": c2.name, "T": c2.T,
+            "value": world * c2.T * steps2 / s2, "unit": UNIT,
+            "ms_per_step": 1000.0 * s2 / steps2, "stages_ms": stg2,
+            "layer_tflops": 2.0 * c2.N * 3 * c2.H * c2.I / (s2 / steps2) / 1e12,
+            "roofline": {"kernel": "grouped_gemm gate/up + SwiGLU (tcgen05)", "bound": "tensor",
+                         "achieved": flops / g1b / 1e12, "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": flops / g1b / 1e12 / peak_t,
+                         "traffic": profiled_traffic("gemm_gateup", c2.name),
+                         "peak_source": f"{peak_src} bf16_tflops_sustained"},
+        }
+        line["gpu_launches"] += w2.launches_per_step() * steps2
+        del w2
+        torch.cuda.empty_cache()
+
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_tokens, nthreads)
+        line["cpu_baseline"].pop("seconds", None)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

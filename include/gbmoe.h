@@ -207,12 +207,13 @@ int moe_gemm_gateup_act(const uint16_t* x_perm, const int32_t* offsets, int E_ph
 
 /*
  * moe_gemm_down — grouped down GEMM ("Stage 4": grouped matmul down).
- *   y[r] = bf16(act[r] . w_down[p]^T) for r in expert p's rows.
- *   act [N, I] bf16; w_down [E_phys, H, I] bf16; y [N, H] bf16 out;
+ *   y[r] = act[r] . w_down[p]^T for r in expert p's rows, fp32 accumulate,
+ *   written in fp32 (inside the layer only the activation is rounded to bf16).
+ *   act [N, I] bf16; w_down [E_phys, H, I] bf16; y [N, H] fp32 out;
  *   offsets as for moe_gemm_gateup_act.
  */
 int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N, int H, int I,
-                  const uint16_t* w_down, uint16_t* y, gbmoe_stream_t stream);
+                  const uint16_t* w_down, float* y, gbmoe_stream_t stream);
 
 /*
  * moe_combine — restore token order and apply the routing probabilities
@@ -220,11 +221,11 @@ int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N
  * ("Forward Skeleton": shared experts).
  *   out[t] = bf16( sum_{j=0..k-1} weights[t,j] * y[flat_to_row[t*k+j]] + shared_y[t] )
  * in fp32, summed in the fixed order j = 0..k-1, then the shared term.
- *   y [T*k, H] bf16; flat_to_row [T*k]; weights [T, k] fp32;
- *   shared_y [T, H] bf16 or NULL; out [T, H] bf16.  H multiple of 8.
+ *   y [T*k, H] fp32; flat_to_row [T*k]; weights [T, k] fp32;
+ *   shared_y [T, H] fp32 or NULL; out [T, H] bf16.  H multiple of 8.
  */
-int moe_combine(const uint16_t* y, const int32_t* flat_to_row, const float* weights,
-                const uint16_t* shared_y, int T, int k, int H, uint16_t* out,
+int moe_combine(const float* y, const int32_t* flat_to_row, const float* weights,
+                const float* shared_y, int T, int k, int H, uint16_t* out,
                 gbmoe_stream_t stream);
 
 /* Scratch bytes moe_forward needs for any T <= T_max (sized from capacity,

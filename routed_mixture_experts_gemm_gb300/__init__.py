@@ -141,17 +141,19 @@ def moe_gemm_gateup_act(x_perm, offsets, w_gate, w_up, act=None, stream=None):
 
 
 def moe_gemm_down(act, offsets, w_down, y=None, stream=None):
+    """y = act W_down^T per expert group, fp32 output [N, H]."""
     lib = _lib.load()
     N, I = act.shape
     P, H, _ = w_down.shape
     if y is None:
-        y = torch.empty((N, H), dtype=torch.bfloat16, device=act.device)
+        y = torch.empty((N, H), dtype=torch.float32, device=act.device)
     _check(lib.moe_gemm_down(_ptr(act), _ptr(offsets), P, N, H, I, _ptr(w_down), _ptr(y),
                              _stream(stream)), "moe_gemm_down")
     return y
 
 
 def moe_combine(y, flat_to_row, weights, shared_y=None, out=None, stream=None):
+    """out = bf16(sum_j w_j y[flat_to_row] + shared_y); y, shared_y fp32."""
     lib = _lib.load()
     T, k = weights.shape
     H = y.shape[1]

@@ -67,7 +67,8 @@ struct FwdWs {
     int32_t *ids_log, *ids_phys, *counts, *offsets, *row_to_token, *flat_to_row;
     float* weights;
     void* perm;
-    uint16_t *x_perm, *act, *y, *act_s, *ys;
+    uint16_t *x_perm, *act, *act_s;
+    float *y, *ys;
     size_t bytes;
 };
 
@@ -87,9 +88,9 @@ FwdWs layout_fwd(const gbmoe_layer* L, int T, void* ws) {
     f.perm = w.take<char>(permute_ws_bytes(static_cast<int64_t>(N), c.E_phys));
     f.x_perm = w.take<uint16_t>(N * L->H);
     f.act = w.take<uint16_t>(N * L->I);
-    f.y = w.take<uint16_t>(N * L->H);
+    f.y = w.take<float>(N * L->H);
     f.act_s = w.take<uint16_t>(static_cast<size_t>(T) * L->I_shared);
-    f.ys = w.take<uint16_t>(L->I_shared ? static_cast<size_t>(T) * L->H : 0);
+    f.ys = w.take<float>(L->I_shared ? static_cast<size_t>(T) * L->H : 0);
     f.bytes = w.off;
     return f;
 }
@@ -274,7 +275,7 @@ int moe_gemm_gateup_act(const uint16_t* x_perm, const int32_t* offsets, int E_ph
 }
 
 int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N, int H, int I,
-                  const uint16_t* w_down, uint16_t* y, gbmoe_stream_t stream) {
+                  const uint16_t* w_down, float* y, gbmoe_stream_t stream) {
     if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
     if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
     if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
@@ -288,8 +289,8 @@ int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
-int moe_combine(const uint16_t* y, const int32_t* flat_to_row, const float* weights,
-                const uint16_t* shared_y, int T, int k, int H, uint16_t* out,
+int moe_combine(const float* y, const int32_t* flat_to_row, const float* weights,
+                const float* shared_y, int T, int k, int H, uint16_t* out,
                 gbmoe_stream_t stream) {
     if (T < 0 || k < 1 || k > kMaxTopK || H <= 0 || H % 8) return GBMOE_ERR_INVALID_ARG;
     if (T == 0) return GBMOE_OK;
@@ -348,7 +349,7 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
     st = launch_gemm_down(f.act, f.offsets, c.E_phys, N, L->H, L->I, L->w_down, f.y, *ctx, s);
     if (st) return st;
     // 5. shared expert over all tokens in order (one group)
-    const uint16_t* ys = nullptr;
+    const float* ys = nullptr;
     if (L->I_shared) {
         st = launch_gemm_gateup(x, nullptr, 1, T, L->H, L->I_shared, L->w_gate_shared,
                                 L->w_up_shared, f.act_s, *ctx, s);

@@ -14,7 +14,8 @@
 // Gate/up: two A operands (W_gate and W_up rows of the same intermediate
 // block) feed two TMEM accumulators, so each thread of the epilogue holds g
 // and u of the same output and applies act = bf16(silu(g) * u) in registers.
-// Down: one A operand (W_down rows), y = bf16(acc).
+// Down: one A operand (W_down rows), y = acc kept in fp32 (only the
+// activation is rounded to bf16 inside the layer).
 //
 // One persistent CTA per SM; warp 0 issues TMA loads (128B-swizzled K-major
 // tiles), warp 1 issues tcgen05.mma and owns TMEM (2 accumulator buffers so
@@ -50,14 +51,14 @@ constexpr int NUM_THREADS = 192; // warp 0 TMA, warp 1 MMA/TMEM, warps 2..5 epil
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-template <int NUM_A, int BN, int STAGES>
+template <int NUM_A, int BN, int STAGES, int OUT_ELEM>
 struct Layout {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
-    static constexpr int OUT_BYTES = EPI_COLS * BM * 2;
+    static constexpr int OUT_BYTES = EPI_COLS * BM * OUT_ELEM;
     static constexpr int TABLE_INTS = MAX_GROUPS + 4;
     static constexpr int OFF_OUT = STAGES * STAGE_BYTES;
     static constexpr int OFF_TILE = OFF_OUT + OUT_BYTES;
@@ -81,7 +82,7 @@ struct GemmArgs {
     int n_rows;              // rows of the token operand
     int R;                   // weight rows per group (I for gate/up, H for down)
     int K;                   // reduction length
-    uint16_t* out;           // [n_rows, R] bf16
+    void* out;               // [n_rows, R]: bf16 (gate/up + SwiGLU) or fp32 (down)
     int* status;
 };
 
@@ -134,11 +135,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-    using L = Layout<NUM_A, BN, STAGES>;
+    constexpr int OUT_ELEM = SWIGLU ? 2 : 4;
+    using L = Layout<NUM_A, BN, STAGES, OUT_ELEM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint16_t* out_s = reinterpret_cast<uint16_t*>(smem + L::OFF_OUT);
+    uint8_t* out_s = smem + L::OFF_OUT;
     int* tile_start = reinterpret_cast<int*>(smem + L::OFF_TILE);
     int* gstart = reinterpret_cast<int*>(smem + L::OFF_GSTART);
     int* gcnt = reinterpret_cast<int*>(smem + L::OFF_GCNT);
@@ -349,17 +351,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(g[c]);
                 }
                 epi_bar();  // the previous pass has finished reading out_s
+                if constexpr (SWIGLU) {
+                    uint16_t* o16 = reinterpret_cast<uint16_t*>(out_s);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) out_s[c * BM + r] = f32_to_bf16_bits(v[c]);
+                    for (int c = 0; c < 32; ++c) o16[c * BM + r] = f32_to_bf16_bits(v[c]);
+                } else {
+                    float* o32 = reinterpret_cast<float*>(out_s);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o32[c * BM + r] = v[c];
+                }
                 epi_bar();
+                // rows of BM outputs, 16-byte vectors
+                constexpr int VPR = BM * OUT_ELEM / 16;
                 const int nr = min(EPI_COLS, tl.n_valid - c0);
-                for (int i = etid; i < nr * (BM / 8); i += 128) {
-                    const int row = i / (BM / 8), vq = i % (BM / 8);
+                for (int i = etid; i < nr * VPR; i += 128) {
+                    const int row = i / VPR, vq = i % VPR;
                     const int grow = tl.row0 + c0 + row;
                     if (grow < args.n_rows) {
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            args.out + static_cast<size_t>(grow) * args.R + tl.rblk * BM + vq * 8);
-                        *dst = *reinterpret_cast<const uint4*>(out_s + row * BM + vq * 8);
+                        uint8_t* dst = static_cast<uint8_t*>(args.out) +
+                                       (static_cast<size_t>(grow) * args.R + tl.rblk * BM) * OUT_ELEM +
+                                       vq * 16;
+                        *reinterpret_cast<uint4*>(dst) =
+                            *reinterpret_cast<const uint4*>(out_s + (row * BM) * OUT_ELEM + vq * 16);
                     }
                 }
             }
@@ -383,8 +396,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
 }
 
 // ----------------------------------------------------------------- host
-using Gemm1Layout = Layout<2, 128, 4>;
-using Gemm2Layout = Layout<1, 128, 6>;
+using Gemm1Layout = Layout<2, 128, 4, 2>;
+using Gemm2Layout = Layout<1, 128, 6, 4>;
 #define GEMM1_KERNEL grouped_gemm_kernel<2, 128, 4, true>
 #define GEMM2_KERNEL grouped_gemm_kernel<1, 128, 6, false>
 
@@ -458,7 +471,7 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int group
 }
 
 int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, int n_rows, int H,
-                     int I, const uint16_t* w_down, uint16_t* y, const DevCtx& ctx,
+                     int I, const uint16_t* w_down, float* y, const DevCtx& ctx,
                      cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
     CUtensorMap ma0, mb;

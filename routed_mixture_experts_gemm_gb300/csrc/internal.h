@@ -57,13 +57,13 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int group
                        int H, int I, const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
                        const DevCtx& ctx, cudaStream_t s);
 int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, int n_rows, int H,
-                     int I, const uint16_t* w_down, uint16_t* y, const DevCtx& ctx,
+                     int I, const uint16_t* w_down, float* y, const DevCtx& ctx,
                      cudaStream_t s);
 int gemm_max_groups();
 
 // --- combine (combine.cu) ---
-cudaError_t launch_combine(const uint16_t* y, const int32_t* flat_to_row, const float* weights,
-                           const uint16_t* shared_y, int T, int k, int H, uint16_t* out,
+cudaError_t launch_combine(const float* y, const int32_t* flat_to_row, const float* weights,
+                           const float* shared_y, int T, int k, int H, uint16_t* out,
                            const DevCtx& ctx, cudaStream_t s);
 
 }  // namespace gbmoe
