@@ -191,6 +191,30 @@ int moe_permute(const int32_t* ids_phys, int T, int k, int E_phys, const uint16_
                 uint16_t* x_perm, void* ws, size_t ws_bytes, gbmoe_stream_t stream);
 
 /*
+ * moe_permute_static — the same permutation as moe_permute, for callers that
+ * cannot allocate device memory (cudaMalloc/cudaFree can synchronise the
+ * device and stall every stream, and a process whose GPU memory belongs to
+ * another framework's pool must not allocate behind it).  The pages have no
+ * counterpart to this entry point; it is an addition of this library.
+ *
+ * Arguments, outputs and results are those of moe_permute, without the
+ * workspace: the scratch lives in a 1 MiB array inside the library, one per
+ * device, held until the process exits.  The library allocates nothing.
+ *   Limit: ceil(T*k/256) * E_phys * 4 + 256 bytes must fit in 1 MiB
+ *   (e.g. E_phys = 256 allows T*k up to 261,888); larger requests return
+ *   GBMOE_ERR_WORKSPACE and enqueue nothing.
+ *   The first call on each device resolves the array's device address
+ *   (cudaGetSymbolAddress with that device current); make it before any
+ *   stream capture.
+ *   All calls share the array and it keeps the last call's contents; calls
+ *   that overlap on the GPU (several streams or threads) race on it, so the
+ *   caller must serialise them.
+ */
+int moe_permute_static(const int32_t* ids_phys, int T, int k, int E_phys, const uint16_t* x,
+                       int H, int32_t* counts, int32_t* offsets, int32_t* row_to_token,
+                       int32_t* flat_to_row, uint16_t* x_perm, gbmoe_stream_t stream);
+
+/*
  * moe_gemm_gateup_act — grouped gate/up GEMM with the activation fused into
  * its epilogue ("Stage 4": grouped matmul gate/up -> activation; SwiGLU).
  * For each expert p and each row r in [offsets[p], offsets[p+1]):

@@ -44,6 +44,7 @@ SIGNATURES = {
     "moe_expert_counts": (_i, [_vp, _i, _i, _i, _vp, _i, _vp]),
     "gbmoe_permute_workspace_size": (_sz, [_i, _i, _i]),
     "moe_permute": (_i, [_vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_permute_static": (_i, [_vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_gemm_gateup_act": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp]),
     "moe_gemm_down": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
