@@ -44,7 +44,7 @@ namespace {
 constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BK = 64;           // K elements per pipeline stage: one 128-byte swizzle row
 constexpr int UMMA_K = 16;       // K per tcgen05.mma kind::f16
-constexpr int BOX_ROWS = 16;     // token rows per TMA box
+constexpr int BOX_ROWS = 16;     // granularity of the token dimension (MMA N step, smallest box)
 constexpr int EPI_COLS = 32;     // tokens per epilogue pass
 constexpr int MAX_GROUPS = 1024;
 constexpr int NUM_THREADS = 192; // warp 0 TMA, warp 1 MMA/TMEM, warps 2..5 epilogue
@@ -134,7 +134,10 @@ template <int NUM_A, int BN, int STAGES, bool SWIGLU>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
-                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmB16,
+                    const __grid_constant__ CUtensorMap tmB32,
+                    const __grid_constant__ CUtensorMap tmB64,
+                    const __grid_constant__ CUtensorMap tmB128, const GemmArgs args) {
     constexpr int OUT_ELEM = SWIGLU ? 2 : 4;
     using L = Layout<NUM_A, BN, STAGES, OUT_ELEM>;
     extern __shared__ uint8_t smem_raw[];
@@ -174,7 +177,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         fence_barrier_init();
         tma_prefetch_desc(&tmA0);
         if (NUM_A == 2) tma_prefetch_desc(&tmA1);
-        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmB16);
+        tma_prefetch_desc(&tmB32);
+        tma_prefetch_desc(&tmB64);
+        tma_prefetch_desc(&tmB128);
     }
     if (warp == 1) {
         tmem_alloc(tmem_base_s, L::TMEM_COLS);
@@ -236,8 +242,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         uint32_t armed_phase = 0;    // bit s: parity of its last armed phase
         for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
             const Tile tl = decode_tile(tau, tile_start, gstart, gcnt, P, rblocks, BN);
-            const int nbox = (tl.n_valid + BOX_ROWS - 1) / BOX_ROWS;
-            const uint32_t bytes = NUM_A * L::A_BYTES + nbox * BOX_ROWS * BK * 2;
+            const int n_load = (tl.n_valid + BOX_ROWS - 1) / BOX_ROWS * BOX_ROWS;
+            const uint32_t bytes = NUM_A * L::A_BYTES + n_load * BK * 2;
             const int a_row = tl.p * args.R + tl.rblk * BM;
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
@@ -250,10 +256,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                 uint8_t* sA = smem + stage * L::STAGE_BYTES;
                 tma_load_2d(sA, &tmA0, full + stage, kb * BK, a_row, pol_w);
                 if (NUM_A == 2) tma_load_2d(sA + L::A_BYTES, &tmA1, full + stage, kb * BK, a_row, pol_w);
+                // token rows in as few boxes as possible (128/64/32/16 rows)
                 uint8_t* sB = sA + NUM_A * L::A_BYTES;
-                for (int b = 0; b < nbox; ++b)
-                    tma_load_2d(sB + b * BOX_ROWS * BK * 2, &tmB, full + stage, kb * BK,
-                                tl.row0 + b * BOX_ROWS, pol_x);
+                for (int off = 0; off < n_load;) {
+                    const int rem = n_load - off;
+                    const int box = rem >= 128 ? 128 : rem >= 64 ? 64 : rem >= 32 ? 32 : 16;
+                    const CUtensorMap* m = box == 128 ? &tmB128 : box == 64 ? &tmB64
+                                         : box == 32 ? &tmB32 : &tmB16;
+                    tma_load_2d(sB + off * BK * 2, m, full + stage, kb * BK, tl.row0 + off, pol_x);
+                    off += box;
+                }
                 armed |= 1u << stage;
                 armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) {
@@ -450,6 +462,14 @@ int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
     return static_cast<int>(std::max<long>(1, std::min<long>(bound, num_sms)));
 }
 
+struct TokenMaps {
+    CUtensorMap b16, b32, b64, b128;
+};
+bool make_token_maps(TokenMaps* t, const void* ptr, uint64_t rows, uint64_t K) {
+    return make_map(&t->b16, ptr, rows, K, 16) && make_map(&t->b32, ptr, rows, K, 32) &&
+           make_map(&t->b64, ptr, rows, K, 64) && make_map(&t->b128, ptr, rows, K, 128);
+}
+
 }  // namespace
 
 int gemm_max_groups() { return MAX_GROUPS; }
@@ -458,15 +478,17 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int group
                        int H, int I, const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
                        const DevCtx& ctx, cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
-    CUtensorMap ma0, ma1, mb;
+    CUtensorMap ma0, ma1;
+    TokenMaps mb;
     if (!make_map(&ma0, w_gate, static_cast<uint64_t>(groups) * I, H, BM) ||
         !make_map(&ma1, w_up, static_cast<uint64_t>(groups) * I, H, BM) ||
-        !make_map(&mb, x_rows, n_rows, H, BOX_ROWS))
+        !make_token_maps(&mb, x_rows, n_rows, H))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
     const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
-    GEMM1_KERNEL<<<grid, NUM_THREADS, Gemm1Layout::SMEM_BYTES, s>>>(ma0, ma1, mb, a);
+    GEMM1_KERNEL<<<grid, NUM_THREADS, Gemm1Layout::SMEM_BYTES, s>>>(ma0, ma1, mb.b16, mb.b32,
+                                                                    mb.b64, mb.b128, a);
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 
@@ -474,14 +496,16 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
                      int I, const uint16_t* w_down, float* y, const DevCtx& ctx,
                      cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
-    CUtensorMap ma0, mb;
+    CUtensorMap ma0;
+    TokenMaps mb;
     if (!make_map(&ma0, w_down, static_cast<uint64_t>(groups) * H, I, BM) ||
-        !make_map(&mb, act, n_rows, I, BOX_ROWS))
+        !make_token_maps(&mb, act, n_rows, I))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status};
     const int grid = grid_for(groups, n_rows, H, 128, ctx.num_sms);
-    GEMM2_KERNEL<<<grid, NUM_THREADS, Gemm2Layout::SMEM_BYTES, s>>>(ma0, ma0, mb, a);
+    GEMM2_KERNEL<<<grid, NUM_THREADS, Gemm2Layout::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
+                                                                    mb.b64, mb.b128, a);
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 

@@ -17,6 +17,7 @@
 // weights are bit-for-bit reproducible by any implementation of the same
 // definitions.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -124,6 +125,143 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
             const float v = warp_sum_tree(acc[i][j]);
             const int t = t0 + i, e = e0 + j;
             if (lane == ((i * WE + j) & 31) && t < T && e < E)
+                logits[static_cast<size_t>(t) * E + e] = bias ? __fadd_rn(v, __ldg(bias + e)) : v;
+        }
+}
+
+// Shared-memory tiled variant (H % 32 == 0, 16-byte aligned x and w).  A
+// block of 8 warps covers BT = 8*WT tokens x BE = 8*WE experts; H is walked
+// in chunks of 256 (eight h-steps of 32 lanes), double-buffered: router
+// weight rows arrive by cp.async in their natural layout (lane j reads
+// w[e][h0 + 32 i + j], consecutive words), token rows are transposed on the
+// way in so lane j finds its eight values x[t][h0 + j + 32 i], i = 0..7, in
+// one 16-byte word.  Lane j still accumulates h = j, j+32, ... ascending, so
+// the result is the same pinned sum as router_logits_kernel.
+constexpr int kChunk = 256;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+template <int WT, int WE>
+__global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
+    int T, int E, int H, float* __restrict__ logits) {
+    constexpr int TT = 8, TE = 8;
+    constexpr int BT = TT * WT, BE = TE * WE;
+    constexpr int XV = BT * (kChunk / 8);  // 16-byte token vectors per chunk
+    constexpr int WV = BE * (kChunk / 4);  // 16-byte weight vectors per chunk
+    constexpr int XR = (XV + 255) / 256;   // per thread
+    static_assert(WT * WE == 8, "8 warps per block");
+    extern __shared__ __align__(16) uint8_t route_smem[];
+    // xs[2][BT][32][8] bf16 (transposed token chunk), ws[2][BE][kChunk] fp32
+    auto xs = reinterpret_cast<uint16_t(*)[BT][32][8]>(route_smem);
+    auto ws = reinterpret_cast<float(*)[BE][kChunk]>(route_smem + 2 * BT * 32 * 8 * 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wt = warp / WE, we = warp % WE;
+    const int t0 = blockIdx.x * BT, e0 = blockIdx.y * BE;
+    const int nc = (H + kChunk - 1) / kChunk;
+
+    uint4 xr[XR];
+    auto load_x = [&](int c) {
+        const int h0 = c * kChunk;
+#pragma unroll
+        for (int r = 0; r < XR; ++r) {
+            const int idx = tid + r * 256;
+            xr[r] = make_uint4(0, 0, 0, 0);
+            if (idx < XV) {
+                const int row = idx / (kChunk / 8), q = idx % (kChunk / 8);
+                const int t = t0 + row, h = h0 + 8 * q;
+                if (t < T && h < H)
+                    xr[r] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + h));
+            }
+        }
+    };
+    auto store_x = [&](int buf) {
+#pragma unroll
+        for (int r = 0; r < XR; ++r) {
+            const int idx = tid + r * 256;
+            if (idx < XV) {
+                const int row = idx / (kChunk / 8), q = idx % (kChunk / 8);
+                const int i = q >> 2, j0 = (q & 3) * 8;
+                const uint32_t v[4] = {xr[r].x, xr[r].y, xr[r].z, xr[r].w};
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    xs[buf][row][j0 + jj][i] =
+                        static_cast<uint16_t>((jj & 1) ? (v[jj >> 1] >> 16) : (v[jj >> 1] & 0xffffu));
+            }
+        }
+    };
+    auto load_w = [&](int c, int buf) {
+        const int h0 = c * kChunk;
+        for (int idx = tid; idx < WV; idx += 256) {
+            const int row = idx / (kChunk / 4), q = idx % (kChunk / 4);
+            const int e = e0 + row, h = h0 + 4 * q;
+            if (e < E && h < H) cp_async16(&ws[buf][row][4 * q], w + static_cast<size_t>(e) * H + h);
+        }
+        cp_async_commit();
+    };
+
+    float acc[TT][TE];
+#pragma unroll
+    for (int a = 0; a < TT; ++a)
+#pragma unroll
+        for (int b = 0; b < TE; ++b) acc[a][b] = 0.0f;
+
+    load_w(0, 0);
+    load_x(0);
+    store_x(0);
+    cp_async_wait_all();
+    __syncthreads();
+    for (int c = 0; c < nc; ++c) {
+        const int buf = c & 1;
+        if (c + 1 < nc) {
+            load_w(c + 1, buf ^ 1);
+            load_x(c + 1);
+        }
+        const int n_i = min(8, (H - c * kChunk) / 32);
+        uint32_t xp[TT][4];
+#pragma unroll
+        for (int a = 0; a < TT; ++a) {
+            const uint4 v = *reinterpret_cast<const uint4*>(&xs[buf][wt * TT + a][lane][0]);
+            xp[a][0] = v.x;
+            xp[a][1] = v.y;
+            xp[a][2] = v.z;
+            xp[a][3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < n_i) {
+                float wv[TE];
+#pragma unroll
+                for (int b = 0; b < TE; ++b) wv[b] = ws[buf][we * TE + b][32 * i + lane];
+#pragma unroll
+                for (int a = 0; a < TT; ++a) {
+                    const uint32_t pk = xp[a][i >> 1];
+                    const float xv = __uint_as_float((i & 1) ? (pk & 0xffff0000u) : (pk << 16));
+#pragma unroll
+                    for (int b = 0; b < TE; ++b) acc[a][b] = __fmaf_rn(xv, wv[b], acc[a][b]);
+                }
+            }
+        }
+        if (c + 1 < nc) store_x(buf ^ 1);
+        cp_async_wait_all();
+        __syncthreads();
+    }
+#pragma unroll
+    for (int a = 0; a < TT; ++a)
+#pragma unroll
+        for (int b = 0; b < TE; ++b) {
+            const float v = warp_sum_tree(acc[a][b]);
+            const int t = t0 + wt * TT + a, e = e0 + we * TE + b;
+            if (lane == ((a * TE + b) & 31) && t < T && e < E)
                 logits[static_cast<size_t>(t) * E + e] = bias ? __fadd_rn(v, __ldg(bias + e)) : v;
         }
 }
@@ -336,6 +474,31 @@ __global__ void expert_counts_kernel(const int32_t* __restrict__ ids, int64_t n,
     }
 }
 
+template <int WT, int WE>
+constexpr int tiled_smem_bytes() {
+    return 2 * (8 * WT) * 32 * 8 * 2 + 2 * (8 * WE) * kChunk * 4;
+}
+
+template <int WT, int WE>
+cudaError_t launch_tiled(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s) {
+    static bool attr_done[64];
+    static std::mutex mu;
+    constexpr int smem = tiled_smem_bytes<WT, WE>();
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (ctx.device < 0 || ctx.device >= 64 || !attr_done[ctx.device]) {
+            cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel<WT, WE>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            if (ctx.device >= 0 && ctx.device < 64) attr_done[ctx.device] = true;
+        }
+    }
+    dim3 grid((a.T + 8 * WT - 1) / (8 * WT), (a.cfg.E_log + 8 * WE - 1) / (8 * WE));
+    router_logits_tiled_kernel<WT, WE><<<grid, 256, smem, s>>>(a.x, a.w_router, a.router_bias, a.T,
+                                                               a.cfg.E_log, a.H, a.logits);
+    return cudaGetLastError();
+}
+
 template <int EPL>
 cudaError_t launch_select(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s) {
     const int warps_per_block = 8;
@@ -349,7 +512,18 @@ cudaError_t launch_select(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s)
 cudaError_t launch_route(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
     const int E = a.cfg.E_log;
-    if (a.w_router) {
+    const bool tiled = a.w_router && a.H % 32 == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.w_router) & 15u) == 0;
+    if (tiled) {
+        // few tokens: one token tile of 8, 64 experts per block; many tokens:
+        // 16 x 32 tiles (more blocks, router weight re-read less often)
+        const cudaError_t err =
+            static_cast<long>((a.T + 15) / 16) * ((E + 31) / 32) >= 4L * ctx.num_sms
+                ? launch_tiled<2, 4>(a, ctx, s)
+                : launch_tiled<1, 8>(a, ctx, s);
+        if (err != cudaSuccess) return err;
+    } else if (a.w_router) {
         // small batches: thin token tiles so the grid still covers the GPU
         const long big_blocks = ((a.T + 31) / 32) * static_cast<long>((E + 31) / 32);
         if (big_blocks >= 2L * ctx.num_sms) {
