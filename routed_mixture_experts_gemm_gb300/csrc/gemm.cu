@@ -19,7 +19,8 @@
 //
 // One persistent CTA per SM; warp 0 issues TMA loads (128B-swizzled K-major
 // tiles), warp 1 issues tcgen05.mma and owns TMEM (2 accumulator buffers so
-// the epilogue of tile i overlaps the main loop of tile i+1), warps 2-5 drain
+// the epilogue of tile i overlaps the main loop of tile i+1, except for the
+// 256-token gate/up tiles whose two accumulators fill TMEM), warps 2-5 drain
 // TMEM with tcgen05.ld, stage the output tile in shared memory and write
 // coalesced 256-byte rows.  Tiles are ordered (expert, weight block, token
 // block) so CTAs working on the token blocks of one expert read the same
@@ -51,13 +52,13 @@ constexpr int NUM_THREADS = 192; // warp 0 TMA, warp 1 MMA/TMEM, warps 2..5 epil
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-template <int NUM_A, int BN, int STAGES, int OUT_ELEM>
+template <int NUM_A, int BN, int STAGES, int OUT_ELEM, int ACC_BUFS>
 struct Layout {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
-    static constexpr int TMEM_COLS = 2 * ACC_COLS;
+    static constexpr int TMEM_COLS = ACC_BUFS * ACC_COLS;
     static constexpr int OUT_BYTES = EPI_COLS * BM * OUT_ELEM;
     static constexpr int TABLE_INTS = MAX_GROUPS + 4;
     static constexpr int OFF_OUT = STAGES * STAGE_BYTES;
@@ -90,6 +91,18 @@ struct Tile {
     int p, rblk, row0, n_valid;
 };
 
+// A group of cnt rows is cut into token blocks of equal size (a multiple of
+// 16, at most BN): blocks of one weight tile then take the same time and
+// the CTAs running them stay in step, sharing the weight tile through L2.
+__device__ __forceinline__ int block_rows(int cnt, int BN) {
+    const int tb = (cnt + BN - 1) / BN;
+    return tb == 0 ? BN : ((cnt + tb - 1) / tb + 15) / 16 * 16;
+}
+__device__ __forceinline__ int token_blocks(int cnt, int BN) {
+    const int rpb = block_rows(cnt, BN);
+    return (cnt + rpb - 1) / rpb;
+}
+
 __device__ __forceinline__ Tile decode_tile(int tau, const int* tile_start, const int* gstart,
                                             const int* gcnt, int P, int rblocks, int BN) {
     int lo = 0, hi = P;  // largest p with tile_start[p] <= tau
@@ -99,14 +112,15 @@ __device__ __forceinline__ Tile decode_tile(int tau, const int* tile_start, cons
     }
     const int p = lo;
     const int cnt = gcnt[p];
-    const int tb = (cnt + BN - 1) / BN;
+    const int rpb = block_rows(cnt, BN);
+    const int tb = (cnt + rpb - 1) / rpb;
     const int local = tau - tile_start[p];
     Tile t;
     t.p = p;
     t.rblk = local / tb;
     const int tblk = local - t.rblk * tb;
-    t.row0 = gstart[p] + tblk * BN;
-    t.n_valid = min(BN, cnt - tblk * BN);
+    t.row0 = gstart[p] + tblk * rpb;
+    t.n_valid = min(rpb, cnt - tblk * rpb);
     return t;
 }
 
@@ -130,7 +144,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, __expf(-g))), u);
 }
 
-template <int NUM_A, int BN, int STAGES, bool SWIGLU>
+template <int NUM_A, int BN, int STAGES, bool SWIGLU, int ACC_BUFS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -139,7 +153,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmB64,
                     const __grid_constant__ CUtensorMap tmB128, const GemmArgs args) {
     constexpr int OUT_ELEM = SWIGLU ? 2 : 4;
-    using L = Layout<NUM_A, BN, STAGES, OUT_ELEM>;
+    using L = Layout<NUM_A, BN, STAGES, OUT_ELEM, ACC_BUFS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -204,7 +218,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             }
             gstart[p] = off;
             gcnt[p] = cnt;
-            local += (cnt + BN - 1) / BN * rblocks;
+            local += token_blocks(cnt, BN) * rblocks;
         }
         scan[tid] = local;
         __syncthreads();
@@ -221,7 +235,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         int run = scan[tid];
         for (int p = s0; p < s1; ++p) {
             tile_start[p] = run;
-            run += (gcnt[p] + BN - 1) / BN * rblocks;
+            run += token_blocks(gcnt[p], BN) * rblocks;
         }
         if (tid == 0) tile_start[P] = scan[NUM_THREADS];
     }
@@ -322,7 +336,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             }
             if (!ok) break;
             umma_commit(tfull + acc);
-            if (++acc == 2) {
+            if (++acc == ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -391,7 +405,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
-            if (++acc == 2) {
+            if (++acc == ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -408,10 +422,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
 }
 
 // ----------------------------------------------------------------- host
-using Gemm1Layout = Layout<2, 128, 4, 2>;
-using Gemm2Layout = Layout<1, 128, 6, 4>;
-#define GEMM1_KERNEL grouped_gemm_kernel<2, 128, 4, true>
-#define GEMM2_KERNEL grouped_gemm_kernel<1, 128, 6, false>
+// 128-token tiles with two accumulator buffers (groups of a few to ~128 rows,
+// e.g. decode) and 256-token tiles (groups of hundreds of rows, e.g.
+// prefill: an expert's weights are then read once per ~256 rows).
+using Gemm1Small = Layout<2, 128, 4, 2, 2>;
+using Gemm1Large = Layout<2, 256, 3, 2, 1>;
+using Gemm2Small = Layout<1, 128, 6, 4, 2>;
+using Gemm2Large = Layout<1, 256, 4, 4, 2>;
+#define GEMM1_SMALL grouped_gemm_kernel<2, 128, 4, true, 2>
+#define GEMM1_LARGE grouped_gemm_kernel<2, 256, 3, true, 1>
+#define GEMM2_SMALL grouped_gemm_kernel<1, 128, 6, false, 2>
+#define GEMM2_LARGE grouped_gemm_kernel<1, 256, 4, false, 2>
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -447,11 +468,17 @@ bool g_attr_done[64];
 cudaError_t ensure_attrs(int device) {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (device >= 0 && device < 64 && g_attr_done[device]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(GEMM1_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Gemm1Layout::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(GEMM2_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Gemm2Layout::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(GEMM1_SMALL, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Gemm1Small::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(GEMM1_LARGE, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Gemm1Large::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(GEMM2_SMALL, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Gemm2Small::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(GEMM2_LARGE, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Gemm2Large::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) g_attr_done[device] = true;
     return cudaSuccess;
@@ -486,9 +513,15 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int group
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
-    const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
-    GEMM1_KERNEL<<<grid, NUM_THREADS, Gemm1Layout::SMEM_BYTES, s>>>(ma0, ma1, mb.b16, mb.b32,
-                                                                    mb.b64, mb.b128, a);
+    if (n_rows >= 128L * groups) {
+        const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
+        GEMM1_LARGE<<<grid, NUM_THREADS, Gemm1Large::SMEM_BYTES, s>>>(ma0, ma1, mb.b16, mb.b32,
+                                                                      mb.b64, mb.b128, a);
+    } else {
+        const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
+        GEMM1_SMALL<<<grid, NUM_THREADS, Gemm1Small::SMEM_BYTES, s>>>(ma0, ma1, mb.b16, mb.b32,
+                                                                      mb.b64, mb.b128, a);
+    }
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 
@@ -503,9 +536,15 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status};
-    const int grid = grid_for(groups, n_rows, H, 128, ctx.num_sms);
-    GEMM2_KERNEL<<<grid, NUM_THREADS, Gemm2Layout::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
-                                                                    mb.b64, mb.b128, a);
+    if (n_rows >= 128L * groups) {
+        const int grid = grid_for(groups, n_rows, H, 256, ctx.num_sms);
+        GEMM2_LARGE<<<grid, NUM_THREADS, Gemm2Large::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
+                                                                      mb.b64, mb.b128, a);
+    } else {
+        const int grid = grid_for(groups, n_rows, H, 128, ctx.num_sms);
+        GEMM2_SMALL<<<grid, NUM_THREADS, Gemm2Small::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
+                                                                      mb.b64, mb.b128, a);
+    }
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 
