@@ -21,8 +21,8 @@
 // tiles), warp 1 issues tcgen05.mma and owns TMEM (2 accumulator buffers so
 // the epilogue of tile i overlaps the main loop of tile i+1, except for the
 // 256-token gate/up tiles whose two accumulators fill TMEM), warps 2-5 drain
-// TMEM with tcgen05.ld, stage the output tile in shared memory and write
-// coalesced 256-byte rows.  Tiles are ordered (expert, weight block, token
+// TMEM with tcgen05.ld and write coalesced rows straight from registers.
+// Tiles are ordered (expert, weight block, token
 // block) so CTAs working on the token blocks of one expert read the same
 // weight tile at the same time (one HBM read, L2 hits after).  The tile table
 // is built on the device from the group offsets: no host synchronisation.
@@ -59,7 +59,7 @@ struct Layout {
     static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
     static constexpr int TMEM_COLS = ACC_BUFS * ACC_COLS;
-    static constexpr int OUT_BYTES = EPI_COLS * BM * OUT_ELEM;
+    static constexpr int OUT_BYTES = 0;  // the epilogue stores from registers
     static constexpr int TABLE_INTS = MAX_GROUPS + 4;
     static constexpr int OFF_OUT = STAGES * STAGE_BYTES;
     static constexpr int OFF_TILE = OFF_OUT + OUT_BYTES;
@@ -124,7 +124,6 @@ __device__ __forceinline__ Tile decode_tile(int tau, const int* tile_start, cons
     return t;
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // Barrier over the 128 epilogue threads that also ANDs a flag across them, so
 // the four epilogue warps take the same branch after a bounded wait.
 __device__ __forceinline__ bool epi_bar_all(bool v) {
@@ -140,11 +139,22 @@ __device__ __forceinline__ bool epi_bar_all(bool v) {
     return r != 0;
 }
 
+// Epilogue / operand modes of the kernel template.
+//   kSwiGLU:   A0 = W_gate rows, A1 = W_up rows of the same 128-row block;
+//              out = bf16(silu(g) * u) (the gate/up GEMM)
+//   kDown:     A0 = 128 W_down rows; out = fp32 accumulator
+//   kDownPair: A0, A1 = two consecutive 128-row blocks of W_down (256 output
+//              columns per tile sharing one token operand: twice the work per
+//              byte of token rows loaded); out = fp32 accumulators
+constexpr int kSwiGLU = 0, kDown = 1, kDownPair = 2;
+
+// silu(g) * u = g * u / (1 + e^-g); the result is rounded to bf16, so the
+// fast exponential and division (a few ulp of fp32) are far below its ulp.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, __expf(-g))), u);
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int NUM_A, int BN, int STAGES, bool SWIGLU, int ACC_BUFS>
+template <int NUM_A, int BN, int STAGES, int MODE, int ACC_BUFS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -152,12 +162,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmB32,
                     const __grid_constant__ CUtensorMap tmB64,
                     const __grid_constant__ CUtensorMap tmB128, const GemmArgs args) {
+    constexpr bool SWIGLU = MODE == kSwiGLU;
     constexpr int OUT_ELEM = SWIGLU ? 2 : 4;
+    constexpr int WROWS = MODE == kDownPair ? 2 * BM : BM;  // weight rows per tile
+    constexpr int NOUT = MODE == kDownPair ? 2 : 1;         // 128-column output blocks per tile
+    static_assert(MODE != kDown || NUM_A == 1, "down tiles have one A operand");
+    static_assert(MODE == kDown || NUM_A == 2, "gate/up and paired tiles have two");
     using L = Layout<NUM_A, BN, STAGES, OUT_ELEM, ACC_BUFS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* out_s = smem + L::OFF_OUT;
     int* tile_start = reinterpret_cast<int*>(smem + L::OFF_TILE);
     int* gstart = reinterpret_cast<int*>(smem + L::OFF_GSTART);
     int* gcnt = reinterpret_cast<int*>(smem + L::OFF_GCNT);
@@ -173,7 +187,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = args.groups;
-    const int rblocks = args.R / BM;
+    const int rblocks = args.R / WROWS;
     const int KB = args.K / BK;
 
     // ---- set-up: barriers, TMEM, tile table
@@ -258,7 +272,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             const Tile tl = decode_tile(tau, tile_start, gstart, gcnt, P, rblocks, BN);
             const int n_load = (tl.n_valid + BOX_ROWS - 1) / BOX_ROWS * BOX_ROWS;
             const uint32_t bytes = NUM_A * L::A_BYTES + n_load * BK * 2;
-            const int a_row = tl.p * args.R + tl.rblk * BM;
+            const int a_row = tl.p * args.R + tl.rblk * WROWS;
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, args.status,
@@ -269,7 +283,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                 mbar_arrive_expect_tx(full + stage, bytes);
                 uint8_t* sA = smem + stage * L::STAGE_BYTES;
                 tma_load_2d(sA, &tmA0, full + stage, kb * BK, a_row, pol_w);
-                if (NUM_A == 2) tma_load_2d(sA + L::A_BYTES, &tmA1, full + stage, kb * BK, a_row, pol_w);
+                if (MODE == kSwiGLU)
+                    tma_load_2d(sA + L::A_BYTES, &tmA1, full + stage, kb * BK, a_row, pol_w);
+                if (MODE == kDownPair)
+                    tma_load_2d(sA + L::A_BYTES, &tmA0, full + stage, kb * BK, a_row + BM, pol_w);
                 // token rows in as few boxes as possible (128/64/32/16 rows)
                 uint8_t* sB = sA + NUM_A * L::A_BYTES;
                 for (int off = 0; off < n_load;) {
@@ -349,7 +366,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         // epilogue: TMEM -> registers -> (activation) -> bf16 -> smem -> global
         const int q = warp & 3;           // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;      // weight row within the tile
-        const int etid = tid - 64;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tau = blockIdx.x; tau < total; tau += gridDim.x) {
@@ -359,10 +375,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             if (!epi_bar_all(got)) break;
             tc_fence_after();
             const uint32_t tb = tmem_base + acc * L::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-            for (int c0 = 0; c0 < tl.n_valid; c0 += EPI_COLS) {
+            for (int c0 = 0; c0 < tl.n_valid; c0 += EPI_COLS)
+#pragma unroll 1
+            for (int ob = 0; ob < NOUT; ++ob) {
                 uint32_t g[32];
-                tmem_ld_32x32b_x16(tb + c0, *reinterpret_cast<uint32_t(*)[16]>(g));
-                tmem_ld_32x32b_x16(tb + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(g + 16));
+                tmem_ld_32x32b_x16(tb + ob * BN + c0, *reinterpret_cast<uint32_t(*)[16]>(g));
+                tmem_ld_32x32b_x16(tb + ob * BN + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(g + 16));
                 float v[32];
                 if constexpr (SWIGLU) {
                     uint32_t u[32];
@@ -376,29 +394,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
 #pragma unroll
                     for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(g[c]);
                 }
-                epi_bar();  // the previous pass has finished reading out_s
-                if constexpr (SWIGLU) {
-                    uint16_t* o16 = reinterpret_cast<uint16_t*>(out_s);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) o16[c * BM + r] = f32_to_bf16_bits(v[c]);
-                } else {
-                    float* o32 = reinterpret_cast<float*>(out_s);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) o32[c * BM + r] = v[c];
-                }
-                epi_bar();
-                // rows of BM outputs, 16-byte vectors
-                constexpr int VPR = BM * OUT_ELEM / 16;
+                // Lane r of the tile holds output column r for 32 consecutive
+                // token rows, so for each row the 32 lanes of a warp write 32
+                // consecutive outputs (128 B of fp32 / 64 B of bf16): coalesced
+                // stores straight from registers, no staging or barriers.
                 const int nr = min(EPI_COLS, tl.n_valid - c0);
-                for (int i = etid; i < nr * VPR; i += 128) {
-                    const int row = i / VPR, vq = i % VPR;
-                    const int grow = tl.row0 + c0 + row;
-                    if (grow < args.n_rows) {
-                        uint8_t* dst = static_cast<uint8_t*>(args.out) +
-                                       (static_cast<size_t>(grow) * args.R + tl.rblk * BM) * OUT_ELEM +
-                                       vq * 16;
-                        *reinterpret_cast<uint4*>(dst) =
-                            *reinterpret_cast<const uint4*>(out_s + (row * BM) * OUT_ELEM + vq * 16);
+                const size_t col = static_cast<size_t>(tl.rblk) * WROWS + ob * BM + r;
+                uint8_t* base = static_cast<uint8_t*>(args.out) +
+                                (static_cast<size_t>(tl.row0 + c0) * args.R + col) * OUT_ELEM;
+                const size_t row_bytes = static_cast<size_t>(args.R) * OUT_ELEM;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    if (c < nr && tl.row0 + c0 + c < args.n_rows) {
+                        if constexpr (SWIGLU)
+                            *reinterpret_cast<uint16_t*>(base + c * row_bytes) = f32_to_bf16_bits(v[c]);
+                        else
+                            *reinterpret_cast<float*>(base + c * row_bytes) = v[c];
                     }
                 }
             }
@@ -425,14 +436,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
 // 128-token tiles with two accumulator buffers (groups of a few to ~128 rows,
 // e.g. decode) and 256-token tiles (groups of hundreds of rows, e.g.
 // prefill: an expert's weights are then read once per ~256 rows).
+// The down GEMM's large tiles pair two 128-row weight blocks when H % 256 == 0.
 using Gemm1Small = Layout<2, 128, 4, 2, 2>;
 using Gemm1Large = Layout<2, 256, 3, 2, 1>;
 using Gemm2Small = Layout<1, 128, 6, 4, 2>;
 using Gemm2Large = Layout<1, 256, 4, 4, 2>;
-#define GEMM1_SMALL grouped_gemm_kernel<2, 128, 4, true, 2>
-#define GEMM1_LARGE grouped_gemm_kernel<2, 256, 3, true, 1>
-#define GEMM2_SMALL grouped_gemm_kernel<1, 128, 6, false, 2>
-#define GEMM2_LARGE grouped_gemm_kernel<1, 256, 4, false, 2>
+using Gemm2Pair = Layout<2, 256, 3, 4, 1>;
+#define GEMM1_SMALL grouped_gemm_kernel<2, 128, 4, kSwiGLU, 2>
+#define GEMM1_LARGE grouped_gemm_kernel<2, 256, 3, kSwiGLU, 1>
+#define GEMM2_SMALL grouped_gemm_kernel<1, 128, 6, kDown, 2>
+#define GEMM2_LARGE grouped_gemm_kernel<1, 256, 4, kDown, 2>
+#define GEMM2_PAIR grouped_gemm_kernel<2, 256, 3, kDownPair, 1>
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -479,6 +493,9 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(GEMM2_LARGE, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Gemm2Large::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(GEMM2_PAIR, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Gemm2Pair::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) g_attr_done[device] = true;
     return cudaSuccess;
@@ -536,7 +553,11 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status};
-    if (n_rows >= 128L * groups) {
+    if (n_rows >= 128L * groups && H % 256 == 0) {
+        const int grid = grid_for(groups, n_rows, H / 2, 256, ctx.num_sms);
+        GEMM2_PAIR<<<grid, NUM_THREADS, Gemm2Pair::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
+                                                                    mb.b64, mb.b128, a);
+    } else if (n_rows >= 128L * groups) {
         const int grid = grid_for(groups, n_rows, H, 256, ctx.num_sms);
         GEMM2_LARGE<<<grid, NUM_THREADS, Gemm2Large::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
                                                                       mb.b64, mb.b128, a);

@@ -261,3 +261,45 @@ def test_device_generator_matches_host(built):
     d = synth.normal_bf16_device(cfg.seed, synth.TAG_WG, 3, n, cfg.w_sigma, DEV)
     h = synth.normal_bf16(cfg.seed, synth.TAG_WG, 3, n, cfg.w_sigma)
     assert np.array_equal(_np(d.view(torch.int16)).view(np.uint16), h)
+
+
+# every tile variant of the grouped GEMMs: 128-token tiles (two accumulator
+# buffers), 256-token tiles, the paired 256-row down tiles (H % 256 == 0) and
+# the unpaired ones (H % 256 != 0); empty groups, one-row groups, ragged rows
+GEMM_SHAPES = [
+    (384, 256, [150, 200, 300, 1, 0]),  # large tiles, unpaired down (384 % 256 != 0)
+    (512, 128, [40, 3, 17, 0, 90]),   # small tiles
+    (256, 384, [260, 140]),           # large tiles, paired down
+    (768, 256, [513, 129]),           # large tiles, several token blocks, paired down
+]
+
+
+@pytest.mark.parametrize("shape", GEMM_SHAPES)
+def test_gemm_tile_variants(built, shape):
+    gb = built
+    H, I, rows = shape
+    rng = np.random.default_rng(H + I)
+    P = len(rows)
+    offs = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    N = int(offs[-1])
+    x = (rng.standard_normal((N, H))).astype(np.float32)
+    from tests.test_oracle_mlp import _bf16_bits
+    xb = _bf16_bits(x)
+    W = [tuple(_bf16_bits(rng.standard_normal(s) * 0.05) for s in ((I, H), (I, H), (H, I)))
+         for _ in range(P)]
+    act_o = np.zeros((N, I), np.uint16)
+    y_o = np.zeros((N, H), np.float32)
+    for p in range(P):
+        if rows[p]:
+            a, y = oracle.expert_ffn_rows(xb[offs[p]:offs[p + 1]], *W[p])
+            act_o[offs[p]:offs[p + 1]] = a
+            y_o[offs[p]:offs[p + 1]] = y
+    dev_offs = torch.from_numpy(offs).to(DEV)
+    wg = bf16_dev(np.stack([w[0] for w in W]), DEV)
+    wu = bf16_dev(np.stack([w[1] for w in W]), DEV)
+    wd = bf16_dev(np.stack([w[2] for w in W]), DEV)
+    act = gb.moe_gemm_gateup_act(bf16_dev(xb, DEV), dev_offs, wg, wu)
+    y = gb.moe_gemm_down(bf16_dev(act_o, DEV), dev_offs, wd)
+    assert gb.check_device_status() == 0
+    assert_within_tol(_bf(act), synth.bf16_to_f32(act_o), f"act {shape}")
+    assert_within_tol(_np(y), y_o, f"y {shape}")
