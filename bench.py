@@ -61,6 +61,10 @@ PROFILE_WORKLOADS = {
     "prefill_e16": synth.MoEConfig("prefill_e16", 22, T=512, H=7168, I=2048, E=16, k=8,
                                    scoring="sigmoid", n_group=8, topk_group=4,
                                    routed_scaling=2.5, corr_bias_sigma=0.1, router_sigma=None),
+    # 256 rows per expert like prefill, 32 experts (2.8 GB of weights)
+    "prefill_e32": synth.MoEConfig("prefill_e32", 24, T=1024, H=7168, I=2048, E=32, k=8,
+                                   scoring="sigmoid", n_group=8, topk_group=4,
+                                   routed_scaling=2.5, corr_bias_sigma=0.1, router_sigma=None),
     # the prefill router / permutation / combine shapes with small experts
     "prefill_i128": synth.MoEConfig("prefill_i128", 23, T=8192, H=7168, I=128, E=256, k=8,
                                     scoring="sigmoid", n_group=8, topk_group=4,

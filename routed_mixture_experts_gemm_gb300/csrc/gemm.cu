@@ -20,8 +20,9 @@
 // One persistent CTA per SM; warp 0 issues TMA loads (128B-swizzled K-major
 // tiles), warp 1 issues tcgen05.mma and owns TMEM (2 accumulator buffers so
 // the epilogue of tile i overlaps the main loop of tile i+1, except for the
-// 256-token gate/up tiles whose two accumulators fill TMEM), warps 2-5 drain
-// TMEM with tcgen05.ld and write coalesced rows straight from registers.
+// 256-token tiles whose accumulators fill TMEM), warps 2-9 (two per TMEM
+// lane quarter) drain TMEM with tcgen05.ld and write coalesced rows straight
+// from registers.
 // Tiles are ordered (expert, weight block, token
 // block) so CTAs working on the token blocks of one expert read the same
 // weight tile at the same time (one HBM read, L2 hits after).  The tile table
@@ -46,9 +47,10 @@ constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BK = 64;           // K elements per pipeline stage: one 128-byte swizzle row
 constexpr int UMMA_K = 16;       // K per tcgen05.mma kind::f16
 constexpr int BOX_ROWS = 16;     // granularity of the token dimension (MMA N step, smallest box)
-constexpr int EPI_COLS = 32;     // tokens per epilogue pass
+constexpr int EPI_COLS = 16;     // tokens per epilogue pass (one tcgen05.ld x16)
+constexpr int EPI_WARPS = 8;     // two warps per TMEM lane quarter, alternating passes
 constexpr int MAX_GROUPS = 1024;
-constexpr int NUM_THREADS = 192; // warp 0 TMA, warp 1 MMA/TMEM, warps 2..5 epilogue
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA/TMEM, rest epilogue
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
@@ -74,7 +76,7 @@ struct Layout {
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of 2");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-    static_assert(BN % BOX_ROWS == 0 && BN % EPI_COLS == 0 && BN <= 256, "tile width");
+    static_assert(BN % BOX_ROWS == 0 && BN % (2 * EPI_COLS) == 0 && BN <= 256, "tile width");
 };
 
 struct GemmArgs {
@@ -124,17 +126,17 @@ __device__ __forceinline__ Tile decode_tile(int tau, const int* tile_start, cons
     return t;
 }
 
-// Barrier over the 128 epilogue threads that also ANDs a flag across them, so
-// the four epilogue warps take the same branch after a bounded wait.
+// Barrier over the epilogue threads that also ANDs a flag across them, so
+// all epilogue warps take the same branch after a bounded wait.
 __device__ __forceinline__ bool epi_bar_all(bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred pi, po;\n\t"
         "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.and.pred po, 1, 128, pi;\n\t"
+        "bar.red.and.pred po, 1, %2, pi;\n\t"
         "selp.u32 %0, 1, 0, po;\n\t}"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(v))
+        : "r"(static_cast<uint32_t>(v)), "n"(32 * EPI_WARPS)
         : "memory");
     return r != 0;
 }
@@ -198,7 +200,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + b, 1);
-            mbar_init(tempty + b, 4);
+            mbar_init(tempty + b, EPI_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -363,9 +365,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             mbar_wait_timeout(drain, 0u, kDrainLimitNs);
         }
     } else if (warp >= 2) {
-        // epilogue: TMEM -> registers -> (activation) -> bf16 -> smem -> global
-        const int q = warp & 3;           // TMEM lane quarter this warp may access
-        const int r = q * 32 + lane;      // weight row within the tile
+        // epilogue: TMEM -> registers -> (activation) -> global.  Warp w may
+        // only read TMEM lanes 32*(w%4)..+31; the two warps of each lane
+        // quarter take alternate 16-token passes.
+        const int q = warp & 3;                 // TMEM lane quarter
+        const int half = (warp - 2) / 4;        // which of the quarter's two warps
+        const int r = q * 32 + lane;            // weight row within the tile
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tau = blockIdx.x; tau < total; tau += gridDim.x) {
@@ -375,36 +380,34 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             if (!epi_bar_all(got)) break;
             tc_fence_after();
             const uint32_t tb = tmem_base + acc * L::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-            for (int c0 = 0; c0 < tl.n_valid; c0 += EPI_COLS)
+            const size_t row_bytes = static_cast<size_t>(args.R) * OUT_ELEM;
+            for (int c0 = half * EPI_COLS; c0 < tl.n_valid; c0 += 2 * EPI_COLS)
 #pragma unroll 1
             for (int ob = 0; ob < NOUT; ++ob) {
-                uint32_t g[32];
-                tmem_ld_32x32b_x16(tb + ob * BN + c0, *reinterpret_cast<uint32_t(*)[16]>(g));
-                tmem_ld_32x32b_x16(tb + ob * BN + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(g + 16));
-                float v[32];
+                uint32_t g[16];
+                tmem_ld_32x32b_x16(tb + ob * BN + c0, g);
+                float v[16];
                 if constexpr (SWIGLU) {
-                    uint32_t u[32];
-                    tmem_ld_32x32b_x16(tb + BN + c0, *reinterpret_cast<uint32_t(*)[16]>(u));
-                    tmem_ld_32x32b_x16(tb + BN + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(u + 16));
+                    uint32_t u[16];
+                    tmem_ld_32x32b_x16(tb + BN + c0, u);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) v[c] = silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c]));
+                    for (int c = 0; c < 16; ++c) v[c] = silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c]));
                 } else {
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(g[c]);
+                    for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(g[c]);
                 }
-                // Lane r of the tile holds output column r for 32 consecutive
-                // token rows, so for each row the 32 lanes of a warp write 32
-                // consecutive outputs (128 B of fp32 / 64 B of bf16): coalesced
-                // stores straight from registers, no staging or barriers.
+                // Lane r holds output column r for 16 consecutive token rows,
+                // so for each row the 32 lanes of a warp write 32 consecutive
+                // outputs (128 B of fp32 / 64 B of bf16): coalesced stores
+                // straight from registers.
                 const int nr = min(EPI_COLS, tl.n_valid - c0);
                 const size_t col = static_cast<size_t>(tl.rblk) * WROWS + ob * BM + r;
                 uint8_t* base = static_cast<uint8_t*>(args.out) +
                                 (static_cast<size_t>(tl.row0 + c0) * args.R + col) * OUT_ELEM;
-                const size_t row_bytes = static_cast<size_t>(args.R) * OUT_ELEM;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
+                for (int c = 0; c < 16; ++c) {
                     if (c < nr && tl.row0 + c0 + c < args.n_rows) {
                         if constexpr (SWIGLU)
                             *reinterpret_cast<uint16_t*>(base + c * row_bytes) = f32_to_bf16_bits(v[c]);

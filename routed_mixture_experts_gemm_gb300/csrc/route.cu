@@ -150,37 +150,60 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// Two fp32 fused multiply-adds in one instruction (fma.rn.f32x2): each half
+// is an ordinary round-to-nearest fma, so results are those of two fmaf.
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+
+// Block = 8 warps covering BT = 8*WT tokens x BE = 8*WE experts; each warp
+// owns 8 tokens (four pairs, one per 64-bit accumulator) x 8 experts.  Token
+// chunks are stored pair-interleaved: for token pair p, lane j and h-step i
+// one 32-bit word holds the two tokens' bf16 x[h0 + j + 32 i]; a lane's 8
+// words (32 B) are two 16-byte halves, swapped for lanes with bit 2 set so
+// that the quarter-warp reading them hits distinct banks.
 template <int WT, int WE>
 __global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
     int T, int E, int H, float* __restrict__ logits) {
-    constexpr int TT = 8, TE = 8;
-    constexpr int BT = TT * WT, BE = TE * WE;
-    constexpr int XV = BT * (kChunk / 8);  // 16-byte token vectors per chunk
-    constexpr int WV = BE * (kChunk / 4);  // 16-byte weight vectors per chunk
+    constexpr int TP = 4, TE = 8;          // token pairs and experts per warp
+    constexpr int BT = 2 * TP * WT, BE = TE * WE;
+    constexpr int BP = BT / 2;             // token pairs per block
+    constexpr int XV = BP * (kChunk / 8);  // (pair, 8-h) units per chunk
     constexpr int XR = (XV + 255) / 256;   // per thread
+    constexpr int WV = BE * (kChunk / 4);  // 16-byte weight vectors per chunk
     static_assert(WT * WE == 8, "8 warps per block");
     extern __shared__ __align__(16) uint8_t route_smem[];
-    // xs[2][BT][32][8] bf16 (transposed token chunk), ws[2][BE][kChunk] fp32
-    auto xs = reinterpret_cast<uint16_t(*)[BT][32][8]>(route_smem);
-    auto ws = reinterpret_cast<float(*)[BE][kChunk]>(route_smem + 2 * BT * 32 * 8 * 2);
+    // xs: [2][BP][32 lanes][2 halves][4 words]; ws: [2][BE][kChunk] fp32
+    uint32_t* xs = reinterpret_cast<uint32_t*>(route_smem);
+    auto ws = reinterpret_cast<float(*)[BE][kChunk]>(route_smem + 2 * BP * 32 * 8 * 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wt = warp / WE, we = warp % WE;
     const int t0 = blockIdx.x * BT, e0 = blockIdx.y * BE;
     const int nc = (H + kChunk - 1) / kChunk;
 
-    uint4 xr[XR];
+    uint4 xa[XR], xb[XR];
     auto load_x = [&](int c) {
         const int h0 = c * kChunk;
 #pragma unroll
         for (int r = 0; r < XR; ++r) {
             const int idx = tid + r * 256;
-            xr[r] = make_uint4(0, 0, 0, 0);
+            xa[r] = xb[r] = make_uint4(0, 0, 0, 0);
             if (idx < XV) {
-                const int row = idx / (kChunk / 8), q = idx % (kChunk / 8);
-                const int t = t0 + row, h = h0 + 8 * q;
-                if (t < T && h < H)
-                    xr[r] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + h));
+                const int pr = idx / (kChunk / 8), q = idx % (kChunk / 8);
+                const int t = t0 + 2 * pr, h = h0 + 8 * q;
+                if (h < H) {
+                    if (t < T)
+                        xa[r] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + h));
+                    if (t + 1 < T)
+                        xb[r] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t + 1) * H + h));
+                }
             }
         }
     };
@@ -189,13 +212,19 @@ __global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
         for (int r = 0; r < XR; ++r) {
             const int idx = tid + r * 256;
             if (idx < XV) {
-                const int row = idx / (kChunk / 8), q = idx % (kChunk / 8);
+                const int pr = idx / (kChunk / 8), q = idx % (kChunk / 8);
                 const int i = q >> 2, j0 = (q & 3) * 8;
-                const uint32_t v[4] = {xr[r].x, xr[r].y, xr[r].z, xr[r].w};
+                const uint32_t va[4] = {xa[r].x, xa[r].y, xa[r].z, xa[r].w};
+                const uint32_t vb[4] = {xb[r].x, xb[r].y, xb[r].z, xb[r].w};
+                uint32_t* dst = xs + (buf * BP + pr) * 256;
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    xs[buf][row][j0 + jj][i] =
-                        static_cast<uint16_t>((jj & 1) ? (v[jj >> 1] >> 16) : (v[jj >> 1] & 0xffffu));
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = j0 + jj;
+                    const uint32_t lo = (jj & 1) ? (va[jj >> 1] >> 16) : (va[jj >> 1] & 0xffffu);
+                    const uint32_t hi = (jj & 1) ? (vb[jj >> 1] >> 16) : (vb[jj >> 1] & 0xffffu);
+                    const int half = (i >> 2) ^ ((j >> 2) & 1);
+                    dst[j * 8 + half * 4 + (i & 3)] = lo | (hi << 16);
+                }
             }
         }
     };
@@ -209,17 +238,18 @@ __global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
         cp_async_commit();
     };
 
-    float acc[TT][TE];
+    unsigned long long acc[TP][TE];
 #pragma unroll
-    for (int a = 0; a < TT; ++a)
+    for (int a = 0; a < TP; ++a)
 #pragma unroll
-        for (int b = 0; b < TE; ++b) acc[a][b] = 0.0f;
+        for (int b = 0; b < TE; ++b) acc[a][b] = 0ull;
 
     load_w(0, 0);
     load_x(0);
     store_x(0);
     cp_async_wait_all();
     __syncthreads();
+    const int sw = (lane >> 2) & 1;
     for (int c = 0; c < nc; ++c) {
         const int buf = c & 1;
         if (c + 1 < nc) {
@@ -227,27 +257,31 @@ __global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
             load_x(c + 1);
         }
         const int n_i = min(8, (H - c * kChunk) / 32);
-        uint32_t xp[TT][4];
+        uint32_t xp[TP][8];  // word i of token pair a: (x[t][h], x[t+1][h]), h = h0 + lane + 32 i
 #pragma unroll
-        for (int a = 0; a < TT; ++a) {
-            const uint4 v = *reinterpret_cast<const uint4*>(&xs[buf][wt * TT + a][lane][0]);
-            xp[a][0] = v.x;
-            xp[a][1] = v.y;
-            xp[a][2] = v.z;
-            xp[a][3] = v.w;
+        for (int a = 0; a < TP; ++a) {
+            const uint32_t* src = xs + (buf * BP + wt * TP + a) * 256 + lane * 8;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(src + 4 * sw);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(src + 4 * (sw ^ 1));
+            xp[a][0] = v0.x; xp[a][1] = v0.y; xp[a][2] = v0.z; xp[a][3] = v0.w;
+            xp[a][4] = v1.x; xp[a][5] = v1.y; xp[a][6] = v1.z; xp[a][7] = v1.w;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (i < n_i) {
-                float wv[TE];
+                unsigned long long wd[TE];
 #pragma unroll
-                for (int b = 0; b < TE; ++b) wv[b] = ws[buf][we * TE + b][32 * i + lane];
+                for (int b = 0; b < TE; ++b) {
+                    const float wv = ws[buf][we * TE + b][32 * i + lane];
+                    wd[b] = pack2(wv, wv);
+                }
 #pragma unroll
-                for (int a = 0; a < TT; ++a) {
-                    const uint32_t pk = xp[a][i >> 1];
-                    const float xv = __uint_as_float((i & 1) ? (pk & 0xffff0000u) : (pk << 16));
+                for (int a = 0; a < TP; ++a) {
+                    const uint32_t pk = xp[a][i];
+                    const unsigned long long xv =
+                        pack2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u));
 #pragma unroll
-                    for (int b = 0; b < TE; ++b) acc[a][b] = __fmaf_rn(xv, wv[b], acc[a][b]);
+                    for (int b = 0; b < TE; ++b) acc[a][b] = fma2(xv, wd[b], acc[a][b]);
                 }
             }
         }
@@ -256,14 +290,17 @@ __global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
         __syncthreads();
     }
 #pragma unroll
-    for (int a = 0; a < TT; ++a)
+    for (int a = 0; a < TP; ++a)
 #pragma unroll
-        for (int b = 0; b < TE; ++b) {
-            const float v = warp_sum_tree(acc[a][b]);
-            const int t = t0 + wt * TT + a, e = e0 + we * TE + b;
-            if (lane == ((a * TE + b) & 31) && t < T && e < E)
-                logits[static_cast<size_t>(t) * E + e] = bias ? __fadd_rn(v, __ldg(bias + e)) : v;
-        }
+        for (int b = 0; b < TE; ++b)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float part = __uint_as_float(static_cast<uint32_t>(acc[a][b] >> (32 * u)));
+                const float v = warp_sum_tree(part);
+                const int t = t0 + wt * 2 * TP + 2 * a + u, e = e0 + we * TE + b;
+                if (lane == ((a * 2 * TE + u * TE + b) & 31) && t < T && e < E)
+                    logits[static_cast<size_t>(t) * E + e] = bias ? __fadd_rn(v, __ldg(bias + e)) : v;
+            }
 }
 
 // ----------------------------------------------------------- selection
@@ -476,7 +513,7 @@ __global__ void expert_counts_kernel(const int32_t* __restrict__ ids, int64_t n,
 
 template <int WT, int WE>
 constexpr int tiled_smem_bytes() {
-    return 2 * (8 * WT) * 32 * 8 * 2 + 2 * (8 * WE) * kChunk * 4;
+    return 2 * (4 * WT) * 32 * 8 * 4 + 2 * (8 * WE) * kChunk * 4;
 }
 
 template <int WT, int WE>
