@@ -65,6 +65,10 @@ PROFILE_WORKLOADS = {
     "prefill_e32": synth.MoEConfig("prefill_e32", 24, T=1024, H=7168, I=2048, E=32, k=8,
                                    scoring="sigmoid", n_group=8, topk_group=4,
                                    routed_scaling=2.5, corr_bias_sigma=0.1, router_sigma=None),
+    # the decode router / permutation / combine shapes with small experts
+    "decode_i128": synth.MoEConfig("decode_i128", 25, T=128, H=7168, I=128, E=256, k=8,
+                                   scoring="sigmoid", n_group=8, topk_group=4,
+                                   routed_scaling=2.5, corr_bias_sigma=0.1),
     # the prefill router / permutation / combine shapes with small experts
     "prefill_i128": synth.MoEConfig("prefill_i128", 23, T=8192, H=7168, I=128, E=256, k=8,
                                     scoring="sigmoid", n_group=8, topk_group=4,

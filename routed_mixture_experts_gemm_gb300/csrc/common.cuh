@@ -174,15 +174,21 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for a K-major bf16 tile stored as 128-byte
-// rows with the 128B swizzle (8-row atoms of 1024 B, atoms contiguous).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor for a K-major bf16 tile stored as rows of
+// BK elements with the matching swizzle: BK = 64 -> 128-byte rows, 128B
+// swizzle, 8-row atoms of 1024 B; BK = 32 -> 64-byte rows, 64B swizzle,
+// 8-row atoms of 512 B (atoms contiguous, tiles atom-aligned).
+template <int BK>
+__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr) {
+    static_assert(BK == 64 || BK == 32, "128- or 64-byte rows");
+    constexpr uint64_t atom = BK == 64 ? 1024 : 512;
+    constexpr uint64_t layout = BK == 64 ? 2 : 4;          // 128B / 64B swizzle
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
     d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused here)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: 8-row atom
+    d |= (atom >> 4) << 32;                                // stride byte offset: 8-row atom
     d |= static_cast<uint64_t>(1) << 46;                   // descriptor version (tcgen05)
-    d |= static_cast<uint64_t>(2) << 61;                   // swizzle: 128B
+    d |= layout << 61;                                     // swizzle mode
     return d;
 }
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.

@@ -44,8 +44,10 @@ namespace gbmoe {
 namespace {
 
 constexpr int BM = 128;          // weight rows per tile (MMA M)
-constexpr int BK = 64;           // K elements per pipeline stage: one 128-byte swizzle row
 constexpr int UMMA_K = 16;       // K per tcgen05.mma kind::f16
+// K elements per pipeline stage (template parameter BK): 64 = one 128-byte
+// swizzled row (128B swizzle), 32 = one 64-byte row (64B swizzle; twice as
+// many, half-size stages for more lookahead in the same shared memory).
 constexpr int BOX_ROWS = 16;     // granularity of the token dimension (MMA N step, smallest box)
 constexpr int EPI_COLS = 16;     // tokens per epilogue pass (one tcgen05.ld x16)
 constexpr int EPI_WARPS = 8;     // two warps per TMEM lane quarter, alternating passes
@@ -54,7 +56,7 @@ constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA/TMEM
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-template <int NUM_A, int BN, int STAGES, int OUT_ELEM, int ACC_BUFS>
+template <int NUM_A, int BN, int STAGES, int OUT_ELEM, int ACC_BUFS, int BK>
 struct Layout {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
@@ -75,6 +77,7 @@ struct Layout {
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of 2");
     static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+    static_assert(BK == 64 || BK == 32, "stage K is one 128- or 64-byte swizzled row");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(BN % BOX_ROWS == 0 && BN % (2 * EPI_COLS) == 0 && BN <= 256, "tile width");
 };
@@ -156,7 +159,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int NUM_A, int BN, int STAGES, int MODE, int ACC_BUFS>
+template <int NUM_A, int BN, int STAGES, int MODE, int ACC_BUFS, int BK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
@@ -170,7 +173,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
     constexpr int NOUT = MODE == kDownPair ? 2 : 1;         // 128-column output blocks per tile
     static_assert(MODE != kDown || NUM_A == 1, "down tiles have one A operand");
     static_assert(MODE == kDown || NUM_A == 2, "gate/up and paired tiles have two");
-    using L = Layout<NUM_A, BN, STAGES, OUT_ELEM, ACC_BUFS>;
+    using L = Layout<NUM_A, BN, STAGES, OUT_ELEM, ACC_BUFS, BK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -339,10 +342,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                 const uint32_t sB = sA + NUM_A * L::A_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < BK / UMMA_K; ++ks) {
-                    const uint64_t bdesc = smem_desc_sw128(sB + ks * UMMA_K * 2);
+                    const uint64_t bdesc = smem_desc_kmajor<BK>(sB + ks * UMMA_K * 2);
 #pragma unroll
                     for (int a = 0; a < NUM_A; ++a) {
-                        const uint64_t adesc = smem_desc_sw128(sA + a * L::A_BYTES + ks * UMMA_K * 2);
+                        const uint64_t adesc =
+                            smem_desc_kmajor<BK>(sA + a * L::A_BYTES + ks * UMMA_K * 2);
                         umma_bf16(d0 + a * BN, adesc, bdesc, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
                     }
                 }
@@ -439,17 +443,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
 // 128-token tiles with two accumulator buffers (groups of a few to ~128 rows,
 // e.g. decode) and 256-token tiles (groups of hundreds of rows, e.g.
 // prefill: an expert's weights are then read once per ~256 rows).
-// The down GEMM's large tiles pair two 128-row weight blocks when H % 256 == 0.
-using Gemm1Small = Layout<2, 128, 4, 2, 2>;
-using Gemm1Large = Layout<2, 256, 3, 2, 1>;
-using Gemm2Small = Layout<1, 128, 6, 4, 2>;
-using Gemm2Large = Layout<1, 256, 4, 4, 2>;
-using Gemm2Pair = Layout<2, 256, 3, 4, 1>;
-#define GEMM1_SMALL grouped_gemm_kernel<2, 128, 4, kSwiGLU, 2>
-#define GEMM1_LARGE grouped_gemm_kernel<2, 256, 3, kSwiGLU, 1>
-#define GEMM2_SMALL grouped_gemm_kernel<1, 128, 6, kDown, 2>
-#define GEMM2_LARGE grouped_gemm_kernel<1, 256, 4, kDown, 2>
-#define GEMM2_PAIR grouped_gemm_kernel<2, 256, 3, kDownPair, 1>
+// Variant choice (measured on the decode, hash, skew and prefill routings):
+// gate/up uses 256-token tiles once groups average >= 96 rows; the down GEMM
+// pairs two 128-row W_down blocks over 128-token tiles with two accumulator
+// buffers whenever H % 256 == 0 (best or equal on every workload), else 128-
+// or 256-token single-block tiles.  All variants stream K in 64-wide stages
+// (32-wide stages with the 64B swizzle were measured slower: per-stage costs
+// outweigh the extra lookahead).
+constexpr int kBK = 64;
+constexpr long kLargeGateUpRows = 96;
+using Gemm1Small = Layout<2, 128, 4, 2, 2, kBK>;
+using Gemm1Large = Layout<2, 256, 3, 2, 1, kBK>;
+using Gemm2Small = Layout<1, 128, 6, 4, 2, kBK>;
+using Gemm2Large = Layout<1, 256, 4, 4, 2, kBK>;
+using Gemm2Pair = Layout<2, 128, 4, 4, 2, kBK>;
+#define GEMM1_SMALL grouped_gemm_kernel<2, 128, 4, kSwiGLU, 2, kBK>
+#define GEMM1_LARGE grouped_gemm_kernel<2, 256, 3, kSwiGLU, 1, kBK>
+#define GEMM2_SMALL grouped_gemm_kernel<1, 128, 6, kDown, 2, kBK>
+#define GEMM2_LARGE grouped_gemm_kernel<1, 256, 4, kDown, 2, kBK>
+#define GEMM2_PAIR grouped_gemm_kernel<2, 128, 4, kDownPair, 2, kBK>
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -465,16 +477,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 map over [rows, K] (K contiguous), box = {64, box_rows}, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+// 2-D bf16 map over [rows, K] (K contiguous), box = {bk, box_rows}; bk = 64
+// uses the 128B swizzle, bk = 32 the 64B swizzle (matching smem_desc_kmajor).
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_rows,
+              int bk) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {K, rows};
     const cuuint64_t strides[1] = {K * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(bk), box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -512,9 +527,9 @@ int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
 struct TokenMaps {
     CUtensorMap b16, b32, b64, b128;
 };
-bool make_token_maps(TokenMaps* t, const void* ptr, uint64_t rows, uint64_t K) {
-    return make_map(&t->b16, ptr, rows, K, 16) && make_map(&t->b32, ptr, rows, K, 32) &&
-           make_map(&t->b64, ptr, rows, K, 64) && make_map(&t->b128, ptr, rows, K, 128);
+bool make_token_maps(TokenMaps* t, const void* ptr, uint64_t rows, uint64_t K, int bk) {
+    return make_map(&t->b16, ptr, rows, K, 16, bk) && make_map(&t->b32, ptr, rows, K, 32, bk) &&
+           make_map(&t->b64, ptr, rows, K, 64, bk) && make_map(&t->b128, ptr, rows, K, 128, bk);
 }
 
 }  // namespace
@@ -525,15 +540,17 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int group
                        int H, int I, const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
                        const DevCtx& ctx, cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
+    const bool large = n_rows >= kLargeGateUpRows * groups;
+    const int bk = kBK;
     CUtensorMap ma0, ma1;
     TokenMaps mb;
-    if (!make_map(&ma0, w_gate, static_cast<uint64_t>(groups) * I, H, BM) ||
-        !make_map(&ma1, w_up, static_cast<uint64_t>(groups) * I, H, BM) ||
-        !make_token_maps(&mb, x_rows, n_rows, H))
+    if (!make_map(&ma0, w_gate, static_cast<uint64_t>(groups) * I, H, BM, bk) ||
+        !make_map(&ma1, w_up, static_cast<uint64_t>(groups) * I, H, BM, bk) ||
+        !make_token_maps(&mb, x_rows, n_rows, H, bk))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
-    if (n_rows >= 128L * groups) {
+    if (large) {
         const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
         GEMM1_LARGE<<<grid, NUM_THREADS, Gemm1Large::SMEM_BYTES, s>>>(ma0, ma1, mb.b16, mb.b32,
                                                                       mb.b64, mb.b128, a);
@@ -549,18 +566,20 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
                      int I, const uint16_t* w_down, float* y, const DevCtx& ctx,
                      cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
+    const bool large = n_rows >= 128L * groups;
+    const int bk = kBK;
     CUtensorMap ma0;
     TokenMaps mb;
-    if (!make_map(&ma0, w_down, static_cast<uint64_t>(groups) * H, I, BM) ||
-        !make_token_maps(&mb, act, n_rows, I))
+    if (!make_map(&ma0, w_down, static_cast<uint64_t>(groups) * H, I, BM, bk) ||
+        !make_token_maps(&mb, act, n_rows, I, bk))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status};
-    if (n_rows >= 128L * groups && H % 256 == 0) {
-        const int grid = grid_for(groups, n_rows, H / 2, 256, ctx.num_sms);
+    if (H % 256 == 0) {
+        const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
         GEMM2_PAIR<<<grid, NUM_THREADS, Gemm2Pair::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
                                                                     mb.b64, mb.b128, a);
-    } else if (n_rows >= 128L * groups) {
+    } else if (large) {
         const int grid = grid_for(groups, n_rows, H, 256, ctx.num_sms);
         GEMM2_LARGE<<<grid, NUM_THREADS, Gemm2Large::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
                                                                       mb.b64, mb.b128, a);

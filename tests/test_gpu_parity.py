@@ -263,14 +263,16 @@ def test_device_generator_matches_host(built):
     assert np.array_equal(_np(d.view(torch.int16)).view(np.uint16), h)
 
 
-# every tile variant of the grouped GEMMs: 128-token tiles (two accumulator
-# buffers), 256-token tiles, the paired 256-row down tiles (H % 256 == 0) and
-# the unpaired ones (H % 256 != 0); empty groups, one-row groups, ragged rows
+# every tile variant of the grouped GEMMs: gate/up with 128-token tiles (two
+# accumulator buffers) and 256-token tiles (groups averaging >= 96 rows);
+# down with paired 256-row weight blocks (H % 256 == 0) and, for other H,
+# 128- and 256-token single-block tiles; empty, one-row and ragged groups
 GEMM_SHAPES = [
-    (384, 256, [150, 200, 300, 1, 0]),  # large tiles, unpaired down (384 % 256 != 0)
-    (512, 128, [40, 3, 17, 0, 90]),   # small tiles
-    (256, 384, [260, 140]),           # large tiles, paired down
-    (768, 256, [513, 129]),           # large tiles, several token blocks, paired down
+    (384, 256, [150, 200, 300, 1, 0]),  # 256-token gate/up; 256-token unpaired down
+    (384, 128, [40, 3, 17, 0, 90]),     # 128-token gate/up; 128-token unpaired down
+    (512, 128, [40, 3, 17, 0, 90]),     # 128-token gate/up; paired down
+    (256, 384, [260, 140]),             # 256-token gate/up; paired down
+    (768, 256, [513, 129]),             # several token blocks per group; paired down
 ]
 
 
