@@ -64,7 +64,7 @@ struct WsCursor {
 // Workspace of moe_forward for T tokens (nullptr base: sizing only).
 struct FwdWs {
     float* logits;
-    int32_t *ids_log, *ids_phys, *counts, *offsets, *row_to_token, *flat_to_row;
+    int32_t *ids_log, *ids_phys, *counts, *offsets, *row_to_token, *flat_to_row, *ready;
     float* weights;
     void* perm;
     uint16_t *x_perm, *act, *act_s;
@@ -83,6 +83,7 @@ FwdWs layout_fwd(const gbmoe_layer* L, int T, void* ws) {
     f.weights = w.take<float>(N);
     f.counts = w.take<int32_t>(c.E_phys);
     f.offsets = w.take<int32_t>(c.E_phys + 1);
+    f.ready = w.take<int32_t>(c.E_phys);
     f.row_to_token = w.take<int32_t>(N);
     f.flat_to_row = w.take<int32_t>(N);
     f.perm = w.take<char>(permute_ws_bytes(static_cast<int64_t>(N), c.E_phys));
@@ -342,12 +343,20 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
     st = status_from(launch_permute(ip, N, c.top_k, c.E_phys, x, L->H, cn, f.offsets,
                                     f.row_to_token, f.flat_to_row, f.x_perm, f.perm, *ctx, s));
     if (st) return st;
-    // 3-4. grouped gate/up + SwiGLU, grouped down ("Stage 4": unified_apply_mlp)
-    st = launch_gemm_gateup(f.x_perm, f.offsets, c.E_phys, N, L->H, L->I, L->w_gate, L->w_up,
-                            f.act, *ctx, s);
-    if (st) return st;
-    st = launch_gemm_down(f.act, f.offsets, c.E_phys, N, L->H, L->I, L->w_down, f.y, *ctx, s);
-    if (st) return st;
+    // 3-4. grouped gate/up + SwiGLU, grouped down ("Stage 4": unified_apply_mlp);
+    // one fused launch for small groups
+    if (gemm_fused_eligible(c.E_phys, N, L->H)) {
+        st = launch_gemm_mlp_fused(f.x_perm, f.offsets, c.E_phys, N, L->H, L->I, L->w_gate,
+                                   L->w_up, L->w_down, f.act, f.y, f.ready, *ctx, s);
+        if (st) return st;
+    } else {
+        st = launch_gemm_gateup(f.x_perm, f.offsets, c.E_phys, N, L->H, L->I, L->w_gate,
+                                L->w_up, f.act, *ctx, s);
+        if (st) return st;
+        st = launch_gemm_down(f.act, f.offsets, c.E_phys, N, L->H, L->I, L->w_down, f.y, *ctx,
+                              s);
+        if (st) return st;
+    }
     // 5. shared expert over all tokens in order (one group)
     const float* ys = nullptr;
     if (L->I_shared) {

@@ -14,19 +14,25 @@
 // Gate/up: two A operands (W_gate and W_up rows of the same intermediate
 // block) feed two TMEM accumulators, so each thread of the epilogue holds g
 // and u of the same output and applies act = bf16(silu(g) * u) in registers.
-// Down: one A operand (W_down rows), y = acc kept in fp32 (only the
-// activation is rounded to bf16 inside the layer).
+// Down: one A operand (W_down rows), or two consecutive 128-row blocks
+// sharing one token operand; y = acc kept in fp32 (only the activation is
+// rounded to bf16 inside the layer).
 //
 // One persistent CTA per SM; warp 0 issues TMA loads (128B-swizzled K-major
 // tiles), warp 1 issues tcgen05.mma and owns TMEM (2 accumulator buffers so
 // the epilogue of tile i overlaps the main loop of tile i+1, except for the
 // 256-token tiles whose accumulators fill TMEM), warps 2-9 (two per TMEM
 // lane quarter) drain TMEM with tcgen05.ld and write coalesced rows straight
-// from registers.
-// Tiles are ordered (expert, weight block, token
-// block) so CTAs working on the token blocks of one expert read the same
-// weight tile at the same time (one HBM read, L2 hits after).  The tile table
-// is built on the device from the group offsets: no host synchronisation.
+// from registers.  Tiles are ordered (expert, weight block, token block) so
+// CTAs working on the token blocks of one expert read the same weight tile at
+// the same time (one HBM read, L2 hits after).  The tile table is built on
+// the device from the group offsets: no host synchronisation.
+//
+// Fused mode (small groups): one cooperative launch walks every gate/up tile
+// and then every down tile; a down tile of expert p waits (bounded) until all
+// of p's gate/up tiles have published their activations, so the down GEMM
+// fills the last wave of the gate/up GEMM instead of waiting for the launch
+// boundary.
 //
 // Every pipeline wait is bounded (wall-clock limit); a wait that gives up
 // raises an abort flag seen by all roles, records GBMOE_ERR_TIMEOUT, lets
@@ -43,11 +49,10 @@
 namespace gbmoe {
 namespace {
 
-constexpr int BM = 128;          // weight rows per tile (MMA M)
+constexpr int BM = 128;          // weight rows per MMA (M)
 constexpr int UMMA_K = 16;       // K per tcgen05.mma kind::f16
 // K elements per pipeline stage (template parameter BK): 64 = one 128-byte
-// swizzled row (128B swizzle), 32 = one 64-byte row (64B swizzle; twice as
-// many, half-size stages for more lookahead in the same shared memory).
+// swizzled row (128B swizzle), 32 = one 64-byte row (64B swizzle).
 constexpr int BOX_ROWS = 16;     // granularity of the token dimension (MMA N step, smallest box)
 constexpr int EPI_COLS = 16;     // tokens per epilogue pass (one tcgen05.ld x16)
 constexpr int EPI_WARPS = 8;     // two warps per TMEM lane quarter, alternating passes
@@ -56,18 +61,25 @@ constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA/TMEM
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-template <int NUM_A, int BN, int STAGES, int OUT_ELEM, int ACC_BUFS, int BK>
+// Operand / epilogue modes of the kernel template.
+//   kSwiGLU:   A0 = W_gate rows, A1 = W_up rows of the same 128-row block;
+//              out = bf16(silu(g) * u) (the gate/up GEMM)
+//   kDown:     A0 = 128 W_down rows; out = fp32 accumulator
+//   kDownPair: A0, A1 = two consecutive 128-row blocks of W_down (256 output
+//              columns per tile sharing one token operand); out = fp32
+//   kFused:    kSwiGLU tiles, then kDownPair tiles, in one launch
+constexpr int kSwiGLU = 0, kDown = 1, kDownPair = 2, kFused = 3;
+
+template <int NUM_A, int BN, int STAGES, int ACC_BUFS, int BK>
 struct Layout {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
     static constexpr int TMEM_COLS = ACC_BUFS * ACC_COLS;
-    static constexpr int OUT_BYTES = 0;  // the epilogue stores from registers
     static constexpr int TABLE_INTS = MAX_GROUPS + 4;
-    static constexpr int OFF_OUT = STAGES * STAGE_BYTES;
-    static constexpr int OFF_TILE = OFF_OUT + OUT_BYTES;
-    static constexpr int OFF_GSTART = OFF_TILE + TABLE_INTS * 4;
+    static constexpr int OFF_TBS = STAGES * STAGE_BYTES;      // prefix of token blocks
+    static constexpr int OFF_GSTART = OFF_TBS + TABLE_INTS * 4;
     static constexpr int OFF_GCNT = OFF_GSTART + TABLE_INTS * 4;
     static constexpr int OFF_SCAN = OFF_GCNT + TABLE_INTS * 4;
     static constexpr int OFF_BARS = OFF_SCAN + NUM_THREADS * 4 + 16;
@@ -82,6 +94,12 @@ struct Layout {
     static_assert(BN % BOX_ROWS == 0 && BN % (2 * EPI_COLS) == 0 && BN <= 256, "tile width");
 };
 
+// Tensor maps of one GEMM: the weight operand (a0, a1) and the token operand
+// with 16/32/64/128-row boxes.
+struct GemmMaps {
+    CUtensorMap a0, a1, b16, b32, b64, b128;
+};
+
 struct GemmArgs {
     const int32_t* offsets;  // [groups + 1] or null: one group of n_rows
     int groups;
@@ -90,6 +108,14 @@ struct GemmArgs {
     int K;                   // reduction length
     void* out;               // [n_rows, R]: bf16 (gate/up + SwiGLU) or fp32 (down)
     int* status;
+};
+
+// The second GEMM of the fused mode (paired down tiles) and the per-group
+// count of published gate/up tiles (zeroed before the launch).
+struct FusedArgs {
+    int R, K;                // H, I
+    float* out;              // y [n_rows, H]
+    int* ready;              // [groups]
 };
 
 struct Tile {
@@ -108,18 +134,20 @@ __device__ __forceinline__ int token_blocks(int cnt, int BN) {
     return (cnt + rpb - 1) / rpb;
 }
 
-__device__ __forceinline__ Tile decode_tile(int tau, const int* tile_start, const int* gstart,
-                                            const int* gcnt, int P, int rblocks, int BN) {
-    int lo = 0, hi = P;  // largest p with tile_start[p] <= tau
+// Tile tau of a GEMM with `rb` weight blocks per group; tbs[p] is the number
+// of token blocks of groups < p, so group p owns tiles [tbs[p]*rb, tbs[p+1]*rb).
+__device__ __forceinline__ Tile decode_tile(int tau, const int* tbs, const int* gstart,
+                                            const int* gcnt, int P, int rb, int BN) {
+    int lo = 0, hi = P;  // largest p with tbs[p] * rb <= tau
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (tile_start[mid] <= tau) lo = mid; else hi = mid;
+        if (tbs[mid] * rb <= tau) lo = mid; else hi = mid;
     }
     const int p = lo;
     const int cnt = gcnt[p];
     const int rpb = block_rows(cnt, BN);
     const int tb = (cnt + rpb - 1) / rpb;
-    const int local = tau - tile_start[p];
+    const int local = tau - tbs[p] * rb;
     Tile t;
     t.p = p;
     t.rblk = local / tb;
@@ -143,15 +171,22 @@ __device__ __forceinline__ bool epi_bar_all(bool v) {
         : "memory");
     return r != 0;
 }
-
-// Epilogue / operand modes of the kernel template.
-//   kSwiGLU:   A0 = W_gate rows, A1 = W_up rows of the same 128-row block;
-//              out = bf16(silu(g) * u) (the gate/up GEMM)
-//   kDown:     A0 = 128 W_down rows; out = fp32 accumulator
-//   kDownPair: A0, A1 = two consecutive 128-row blocks of W_down (256 output
-//              columns per tile sharing one token operand: twice the work per
-//              byte of token rows loaded); out = fp32 accumulators
-constexpr int kSwiGLU = 0, kDown = 1, kDownPair = 2;
+__device__ __forceinline__ void epi_bar_sync() {
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * EPI_WARPS) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_gpu(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Order this thread's generic-proxy global accesses with its async-proxy
+// (TMA) ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // silu(g) * u = g * u / (1 + e^-g); the result is rounded to bf16, so the
 // fast exponential and division (a few ulp of fp32) are far below its ulp.
@@ -161,23 +196,17 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 template <int NUM_A, int BN, int STAGES, int MODE, int ACC_BUFS, int BK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
-                    const __grid_constant__ CUtensorMap tmA1,
-                    const __grid_constant__ CUtensorMap tmB16,
-                    const __grid_constant__ CUtensorMap tmB32,
-                    const __grid_constant__ CUtensorMap tmB64,
-                    const __grid_constant__ CUtensorMap tmB128, const GemmArgs args) {
-    constexpr bool SWIGLU = MODE == kSwiGLU;
-    constexpr int OUT_ELEM = SWIGLU ? 2 : 4;
-    constexpr int WROWS = MODE == kDownPair ? 2 * BM : BM;  // weight rows per tile
-    constexpr int NOUT = MODE == kDownPair ? 2 : 1;         // 128-column output blocks per tile
-    static_assert(MODE != kDown || NUM_A == 1, "down tiles have one A operand");
-    static_assert(MODE == kDown || NUM_A == 2, "gate/up and paired tiles have two");
-    using L = Layout<NUM_A, BN, STAGES, OUT_ELEM, ACC_BUFS, BK>;
+grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__ GemmMaps m2,
+                    const GemmArgs args, const FusedArgs fz) {
+    constexpr bool FUSED = MODE == kFused;
+    constexpr int MODE1 = FUSED ? kSwiGLU : MODE;  // mode of the first GEMM's tiles
+    static_assert(MODE1 != kDown || NUM_A == 1, "down tiles have one A operand");
+    static_assert(MODE1 == kDown || NUM_A == 2, "gate/up and paired tiles have two");
+    using L = Layout<NUM_A, BN, STAGES, ACC_BUFS, BK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    int* tile_start = reinterpret_cast<int*>(smem + L::OFF_TILE);
+    int* tbs = reinterpret_cast<int*>(smem + L::OFF_TBS);
     int* gstart = reinterpret_cast<int*>(smem + L::OFF_GSTART);
     int* gcnt = reinterpret_cast<int*>(smem + L::OFF_GCNT);
     int* scan = reinterpret_cast<int*>(smem + L::OFF_SCAN);
@@ -192,8 +221,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = args.groups;
-    const int rblocks = args.R / WROWS;
-    const int KB = args.K / BK;
+    constexpr int WROWS1 = MODE1 == kDownPair ? 2 * BM : BM;  // weight rows per first-GEMM tile
+    const int rb1 = args.R / WROWS1;
+    const int rb2 = FUSED ? fz.R / (2 * BM) : 0;
 
     // ---- set-up: barriers, TMEM, tile table
     if (tid == 0) {
@@ -208,19 +238,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
-        tma_prefetch_desc(&tmA0);
-        if (NUM_A == 2) tma_prefetch_desc(&tmA1);
-        tma_prefetch_desc(&tmB16);
-        tma_prefetch_desc(&tmB32);
-        tma_prefetch_desc(&tmB64);
-        tma_prefetch_desc(&tmB128);
+        tma_prefetch_desc(&m1.a0);
+        tma_prefetch_desc(&m1.a1);
+        tma_prefetch_desc(&m1.b16);
+        tma_prefetch_desc(&m1.b128);
+        if (FUSED) {
+            tma_prefetch_desc(&m2.a0);
+            tma_prefetch_desc(&m2.b16);
+            tma_prefetch_desc(&m2.b128);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_base_s, L::TMEM_COLS);
         tmem_relinquish();
     }
     {
-        // tile table: tile_start[p] = number of tiles of groups < p
+        // tbs[p] = token blocks of groups < p
         const int seg = (P + NUM_THREADS - 1) / NUM_THREADS;
         const int s0 = min(P, tid * seg), s1 = min(P, s0 + seg);
         int local = 0;
@@ -237,7 +270,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             }
             gstart[p] = off;
             gcnt[p] = cnt;
-            local += token_blocks(cnt, BN) * rblocks;
+            local += token_blocks(cnt, BN);
         }
         scan[tid] = local;
         __syncthreads();
@@ -253,16 +286,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         __syncthreads();
         int run = scan[tid];
         for (int p = s0; p < s1; ++p) {
-            tile_start[p] = run;
-            run += token_blocks(gcnt[p], BN) * rblocks;
+            tbs[p] = run;
+            run += token_blocks(gcnt[p], BN);
         }
-        if (tid == 0) tile_start[P] = scan[NUM_THREADS];
+        if (tid == 0) tbs[P] = scan[NUM_THREADS];
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_s;
-    const int total = tile_start[P];
+    const int T1 = tbs[P] * rb1;                    // tiles of the first GEMM
+    const int total = T1 + (FUSED ? tbs[P] * rb2 : 0);
+
+    // tile tau -> (which GEMM, tile); the second GEMM exists only when fused
+    auto job = [&](int tau, bool& second, Tile& tl) {
+        second = FUSED && tau >= T1;
+        tl = second ? decode_tile(tau - T1, tbs, gstart, gcnt, P, rb2, BN)
+                    : decode_tile(tau, tbs, gstart, gcnt, P, rb1, BN);
+    };
 
     // ---------------------------------------------------------- roles
     if (warp == 0 && lane == 0) {
@@ -274,10 +315,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         uint32_t armed = 0;          // bit s: stage s has been armed at least once
         uint32_t armed_phase = 0;    // bit s: parity of its last armed phase
         for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
-            const Tile tl = decode_tile(tau, tile_start, gstart, gcnt, P, rblocks, BN);
+            bool second;
+            Tile tl;
+            job(tau, second, tl);
+            const GemmMaps& m = second ? m2 : m1;
+            const int mode = second ? kDownPair : MODE1;
+            const int R = second ? fz.R : args.R;
+            const int KB = (second ? fz.K : args.K) / BK;
+            const int a_row = tl.p * R + tl.rblk * (mode == kDownPair ? 2 * BM : BM);
             const int n_load = (tl.n_valid + BOX_ROWS - 1) / BOX_ROWS * BOX_ROWS;
             const uint32_t bytes = NUM_A * L::A_BYTES + n_load * BK * 2;
-            const int a_row = tl.p * args.R + tl.rblk * WROWS;
+            if (FUSED && second) {
+                // all gate/up tiles of this group must have published their rows
+                const int need = rb1 * token_blocks(gcnt[tl.p], BN);
+                const uint64_t t0 = global_timer_ns();
+                bool ok = true;
+                for (uint32_t it = 0; ld_acquire_gpu(fz.ready + tl.p) < need; ++it) {
+                    if ((it & 63u) == 63u) {
+                        if (*abort_flag) { ok = false; break; }
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            record_error(args.status, GBMOE_ERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (!ok) break;
+                fence_proxy_async_global();
+            }
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, args.status,
@@ -287,19 +353,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                 }
                 mbar_arrive_expect_tx(full + stage, bytes);
                 uint8_t* sA = smem + stage * L::STAGE_BYTES;
-                tma_load_2d(sA, &tmA0, full + stage, kb * BK, a_row, pol_w);
-                if (MODE == kSwiGLU)
-                    tma_load_2d(sA + L::A_BYTES, &tmA1, full + stage, kb * BK, a_row, pol_w);
-                if (MODE == kDownPair)
-                    tma_load_2d(sA + L::A_BYTES, &tmA0, full + stage, kb * BK, a_row + BM, pol_w);
+                tma_load_2d(sA, &m.a0, full + stage, kb * BK, a_row, pol_w);
+                if (mode == kSwiGLU)
+                    tma_load_2d(sA + L::A_BYTES, &m.a1, full + stage, kb * BK, a_row, pol_w);
+                if (mode == kDownPair)
+                    tma_load_2d(sA + L::A_BYTES, &m.a0, full + stage, kb * BK, a_row + BM, pol_w);
                 // token rows in as few boxes as possible (128/64/32/16 rows)
                 uint8_t* sB = sA + NUM_A * L::A_BYTES;
                 for (int off = 0; off < n_load;) {
                     const int rem = n_load - off;
                     const int box = rem >= 128 ? 128 : rem >= 64 ? 64 : rem >= 32 ? 32 : 16;
-                    const CUtensorMap* m = box == 128 ? &tmB128 : box == 64 ? &tmB64
-                                         : box == 32 ? &tmB32 : &tmB16;
-                    tma_load_2d(sB + off * BK * 2, m, full + stage, kb * BK, tl.row0 + off, pol_x);
+                    const CUtensorMap* mb = box == 128 ? &m.b128 : box == 64 ? &m.b64
+                                          : box == 32 ? &m.b32 : &m.b16;
+                    tma_load_2d(sB + off * BK * 2, mb, full + stage, kb * BK, tl.row0 + off, pol_x);
                     off += box;
                 }
                 armed |= 1u << stage;
@@ -322,7 +388,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         uint32_t phase = 0, acc_phase = 0;
         bool issued = false;
         for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
-            const Tile tl = decode_tile(tau, tile_start, gstart, gcnt, P, rblocks, BN);
+            bool second;
+            Tile tl;
+            job(tau, second, tl);
+            const int KB = (second ? fz.K : args.K) / BK;
             const int n_mma = ((tl.n_valid + 15) / 16) * 16;
             const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
             if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, args.status,
@@ -378,20 +447,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tau = blockIdx.x; tau < total; tau += gridDim.x) {
-            const Tile tl = decode_tile(tau, tile_start, gstart, gcnt, P, rblocks, BN);
+            bool second;
+            Tile tl;
+            job(tau, second, tl);
             const bool got = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, args.status,
                                                kWaitLimitNs);
             if (!epi_bar_all(got)) break;
             tc_fence_after();
+            const int mode = second ? kDownPair : MODE1;
+            const bool swiglu = mode == kSwiGLU;
+            const int out_elem = swiglu ? 2 : 4;
+            const int R = second ? fz.R : args.R;
+            uint8_t* outp = static_cast<uint8_t*>(second ? static_cast<void*>(fz.out) : args.out);
+            const int wrows = mode == kDownPair ? 2 * BM : BM;
+            const int nout = mode == kDownPair ? 2 : 1;
             const uint32_t tb = tmem_base + acc * L::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-            const size_t row_bytes = static_cast<size_t>(args.R) * OUT_ELEM;
+            const size_t row_bytes = static_cast<size_t>(R) * out_elem;
             for (int c0 = half * EPI_COLS; c0 < tl.n_valid; c0 += 2 * EPI_COLS)
 #pragma unroll 1
-            for (int ob = 0; ob < NOUT; ++ob) {
+            for (int ob = 0; ob < nout; ++ob) {
                 uint32_t g[16];
                 tmem_ld_32x32b_x16(tb + ob * BN + c0, g);
                 float v[16];
-                if constexpr (SWIGLU) {
+                if (swiglu) {
                     uint32_t u[16];
                     tmem_ld_32x32b_x16(tb + BN + c0, u);
                     tmem_ld_wait();
@@ -407,13 +485,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
                 // outputs (128 B of fp32 / 64 B of bf16): coalesced stores
                 // straight from registers.
                 const int nr = min(EPI_COLS, tl.n_valid - c0);
-                const size_t col = static_cast<size_t>(tl.rblk) * WROWS + ob * BM + r;
-                uint8_t* base = static_cast<uint8_t*>(args.out) +
-                                (static_cast<size_t>(tl.row0 + c0) * args.R + col) * OUT_ELEM;
+                const size_t col = static_cast<size_t>(tl.rblk) * wrows + ob * BM + r;
+                uint8_t* base = outp + (static_cast<size_t>(tl.row0 + c0) * R + col) * out_elem;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     if (c < nr && tl.row0 + c0 + c < args.n_rows) {
-                        if constexpr (SWIGLU)
+                        if (swiglu)
                             *reinterpret_cast<uint16_t*>(base + c * row_bytes) = f32_to_bf16_bits(v[c]);
                         else
                             *reinterpret_cast<float*>(base + c * row_bytes) = v[c];
@@ -423,6 +500,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
+            if (FUSED && !second) {
+                // publish this gate/up tile: its activations are in global memory
+                __threadfence();
+                fence_proxy_async_global();
+                epi_bar_sync();
+                if (warp == 2 && lane == 0) red_release_add_gpu(fz.ready + tl.p, 1);
+            }
             if (++acc == ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -440,28 +524,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
 }
 
 // ----------------------------------------------------------------- host
-// 128-token tiles with two accumulator buffers (groups of a few to ~128 rows,
-// e.g. decode) and 256-token tiles (groups of hundreds of rows, e.g.
-// prefill: an expert's weights are then read once per ~256 rows).
 // Variant choice (measured on the decode, hash, skew and prefill routings):
 // gate/up uses 256-token tiles once groups average >= 96 rows; the down GEMM
 // pairs two 128-row W_down blocks over 128-token tiles with two accumulator
 // buffers whenever H % 256 == 0 (best or equal on every workload), else 128-
 // or 256-token single-block tiles.  All variants stream K in 64-wide stages
 // (32-wide stages with the 64B swizzle were measured slower: per-stage costs
-// outweigh the extra lookahead).
+// outweigh the extra lookahead).  Below 96 rows per group with H % 256 == 0
+// moe_forward runs the two GEMMs fused in one launch (their tiles share one
+// layout).
 constexpr int kBK = 64;
 constexpr long kLargeGateUpRows = 96;
-using Gemm1Small = Layout<2, 128, 4, 2, 2, kBK>;
-using Gemm1Large = Layout<2, 256, 3, 2, 1, kBK>;
-using Gemm2Small = Layout<1, 128, 6, 4, 2, kBK>;
-using Gemm2Large = Layout<1, 256, 4, 4, 2, kBK>;
-using Gemm2Pair = Layout<2, 128, 4, 4, 2, kBK>;
+using Gemm1Small = Layout<2, 128, 4, 2, kBK>;
+using Gemm1Large = Layout<2, 256, 3, 1, kBK>;
+using Gemm2Small = Layout<1, 128, 6, 2, kBK>;
+using Gemm2Large = Layout<1, 256, 4, 2, kBK>;
+using Gemm2Pair = Layout<2, 128, 4, 2, kBK>;
 #define GEMM1_SMALL grouped_gemm_kernel<2, 128, 4, kSwiGLU, 2, kBK>
 #define GEMM1_LARGE grouped_gemm_kernel<2, 256, 3, kSwiGLU, 1, kBK>
 #define GEMM2_SMALL grouped_gemm_kernel<1, 128, 6, kDown, 2, kBK>
 #define GEMM2_LARGE grouped_gemm_kernel<1, 256, 4, kDown, 2, kBK>
 #define GEMM2_PAIR grouped_gemm_kernel<2, 128, 4, kDownPair, 2, kBK>
+#define GEMM_FUSED grouped_gemm_kernel<2, 128, 4, kFused, 2, kBK>
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -494,26 +578,29 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Maps of one GEMM: weights [groups * R, K] (a1 may be null: a copy of a0)
+// and token rows [n_rows, K].
+bool make_gemm_maps(GemmMaps* g, const void* a0, const void* a1, uint64_t weight_rows,
+                    const void* b, uint64_t n_rows, uint64_t K) {
+    return make_map(&g->a0, a0, weight_rows, K, BM, kBK) &&
+           make_map(&g->a1, a1 ? a1 : a0, weight_rows, K, BM, kBK) &&
+           make_map(&g->b16, b, n_rows, K, 16, kBK) && make_map(&g->b32, b, n_rows, K, 32, kBK) &&
+           make_map(&g->b64, b, n_rows, K, 64, kBK) && make_map(&g->b128, b, n_rows, K, 128, kBK);
+}
+
 std::mutex g_attr_mu;
 bool g_attr_done[64];
 
 cudaError_t ensure_attrs(int device) {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (device >= 0 && device < 64 && g_attr_done[device]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(GEMM1_SMALL, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Gemm1Small::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(GEMM1_LARGE, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Gemm1Large::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(GEMM2_SMALL, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Gemm2Small::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(GEMM2_LARGE, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Gemm2Large::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(GEMM2_PAIR, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Gemm2Pair::SMEM_BYTES);
+    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(GEMM1_SMALL, a, Gemm1Small::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_LARGE, a, Gemm1Large::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_SMALL, a, Gemm2Small::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_LARGE, a, Gemm2Large::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_PAIR, a, Gemm2Pair::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM_FUSED, a, Gemm1Small::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) g_attr_done[device] = true;
     return cudaSuccess;
@@ -524,40 +611,30 @@ int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
     return static_cast<int>(std::max<long>(1, std::min<long>(bound, num_sms)));
 }
 
-struct TokenMaps {
-    CUtensorMap b16, b32, b64, b128;
-};
-bool make_token_maps(TokenMaps* t, const void* ptr, uint64_t rows, uint64_t K, int bk) {
-    return make_map(&t->b16, ptr, rows, K, 16, bk) && make_map(&t->b32, ptr, rows, K, 32, bk) &&
-           make_map(&t->b64, ptr, rows, K, 64, bk) && make_map(&t->b128, ptr, rows, K, 128, bk);
-}
-
 }  // namespace
 
 int gemm_max_groups() { return MAX_GROUPS; }
+
+bool gemm_fused_eligible(int groups, int n_rows, int H) {
+    return n_rows > 0 && n_rows < kLargeGateUpRows * groups && H % 256 == 0;
+}
 
 int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int groups, int n_rows,
                        int H, int I, const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
                        const DevCtx& ctx, cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
-    const bool large = n_rows >= kLargeGateUpRows * groups;
-    const int bk = kBK;
-    CUtensorMap ma0, ma1;
-    TokenMaps mb;
-    if (!make_map(&ma0, w_gate, static_cast<uint64_t>(groups) * I, H, BM, bk) ||
-        !make_map(&ma1, w_up, static_cast<uint64_t>(groups) * I, H, BM, bk) ||
-        !make_token_maps(&mb, x_rows, n_rows, H, bk))
+    GemmMaps m;
+    if (!make_gemm_maps(&m, w_gate, w_up, static_cast<uint64_t>(groups) * I, x_rows, n_rows, H))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
-    GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
-    if (large) {
+    const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
+    const FusedArgs none{0, 0, nullptr, nullptr};
+    if (n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
-        GEMM1_LARGE<<<grid, NUM_THREADS, Gemm1Large::SMEM_BYTES, s>>>(ma0, ma1, mb.b16, mb.b32,
-                                                                      mb.b64, mb.b128, a);
+        GEMM1_LARGE<<<grid, NUM_THREADS, Gemm1Large::SMEM_BYTES, s>>>(m, m, a, none);
     } else {
         const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
-        GEMM1_SMALL<<<grid, NUM_THREADS, Gemm1Small::SMEM_BYTES, s>>>(ma0, ma1, mb.b16, mb.b32,
-                                                                      mb.b64, mb.b128, a);
+        GEMM1_SMALL<<<grid, NUM_THREADS, Gemm1Small::SMEM_BYTES, s>>>(m, m, a, none);
     }
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
@@ -566,29 +643,52 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
                      int I, const uint16_t* w_down, float* y, const DevCtx& ctx,
                      cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
-    const bool large = n_rows >= 128L * groups;
-    const int bk = kBK;
-    CUtensorMap ma0;
-    TokenMaps mb;
-    if (!make_map(&ma0, w_down, static_cast<uint64_t>(groups) * H, I, BM, bk) ||
-        !make_token_maps(&mb, act, n_rows, I, bk))
+    GemmMaps m;
+    if (!make_gemm_maps(&m, w_down, nullptr, static_cast<uint64_t>(groups) * H, act, n_rows, I))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
-    GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status};
+    const GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status};
+    const FusedArgs none{0, 0, nullptr, nullptr};
     if (H % 256 == 0) {
         const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
-        GEMM2_PAIR<<<grid, NUM_THREADS, Gemm2Pair::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
-                                                                    mb.b64, mb.b128, a);
-    } else if (large) {
+        GEMM2_PAIR<<<grid, NUM_THREADS, Gemm2Pair::SMEM_BYTES, s>>>(m, m, a, none);
+    } else if (n_rows >= 128L * groups) {
         const int grid = grid_for(groups, n_rows, H, 256, ctx.num_sms);
-        GEMM2_LARGE<<<grid, NUM_THREADS, Gemm2Large::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
-                                                                      mb.b64, mb.b128, a);
+        GEMM2_LARGE<<<grid, NUM_THREADS, Gemm2Large::SMEM_BYTES, s>>>(m, m, a, none);
     } else {
         const int grid = grid_for(groups, n_rows, H, 128, ctx.num_sms);
-        GEMM2_SMALL<<<grid, NUM_THREADS, Gemm2Small::SMEM_BYTES, s>>>(ma0, ma0, mb.b16, mb.b32,
-                                                                      mb.b64, mb.b128, a);
+        GEMM2_SMALL<<<grid, NUM_THREADS, Gemm2Small::SMEM_BYTES, s>>>(m, m, a, none);
     }
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
+}
+
+int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* offsets, int groups, int n_rows,
+                          int H, int I, const uint16_t* w_gate, const uint16_t* w_up,
+                          const uint16_t* w_down, uint16_t* act, float* y, int* ready,
+                          const DevCtx& ctx, cudaStream_t s) {
+    if (n_rows == 0) return GBMOE_OK;
+    GemmMaps m1, m2;
+    if (!make_gemm_maps(&m1, w_gate, w_up, static_cast<uint64_t>(groups) * I, x_rows, n_rows, H) ||
+        !make_gemm_maps(&m2, w_down, nullptr, static_cast<uint64_t>(groups) * H, act, n_rows, I))
+        return GBMOE_ERR_CUDA;
+    if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
+    if (cudaMemsetAsync(ready, 0, sizeof(int) * groups, s) != cudaSuccess) return GBMOE_ERR_CUDA;
+    const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
+    const FusedArgs f{H, I, y, ready};
+    // every CTA must be resident (down tiles wait on gate/up tiles of other
+    // CTAs): a cooperative launch of at most one CTA per SM
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctx.num_sms);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Gemm1Small::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, GEMM_FUSED, m1, m2, a, f);
+    return e == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 
 }  // namespace gbmoe

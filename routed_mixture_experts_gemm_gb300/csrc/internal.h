@@ -60,6 +60,14 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
                      int I, const uint16_t* w_down, float* y, const DevCtx& ctx,
                      cudaStream_t s);
 int gemm_max_groups();
+// Whether moe_forward runs both GEMMs in one fused cooperative launch (small
+// groups: decode-like batches).
+bool gemm_fused_eligible(int groups, int n_rows, int H);
+// Gate/up + SwiGLU and down in one launch; `ready` is [groups] int scratch.
+int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* offsets, int groups, int n_rows,
+                          int H, int I, const uint16_t* w_gate, const uint16_t* w_up,
+                          const uint16_t* w_down, uint16_t* act, float* y, int* ready,
+                          const DevCtx& ctx, cudaStream_t s);
 
 // --- combine (combine.cu) ---
 cudaError_t launch_combine(const float* y, const int32_t* flat_to_row, const float* weights,
