@@ -24,14 +24,16 @@
  *
  * Readings where the page is silent (each also listed in the design notes):
  *   R1 router logit l[t,e] = sum_h x[t,h]*Wr[e,h] in fp32 with a pinned order:
- *      32 partial sums, partial j accumulates h = j, j+32, ... ascending with a
- *      fused multiply-add, then the pairwise tree s = 16,8,4,2,1
+ *      32 partial sums, partial j accumulates the h with floor((h mod 64)/2)
+ *      = j (h = 2j, 2j+1, 64+2j, 65+2j, ...) ascending with a fused
+ *      multiply-add, then the pairwise tree s = 16,8,4,2,1
  *      (p[i] += p[i+s], i < s); an optional router bias is added last.
  *   R2 scores use this file's own elementary functions: exp by Cody-Waite
  *      reduction (ln2 split hi/lo) and the degree-7 Taylor polynomial;
  *      log1p(y) = 2 atanh(y/(2+y)) by its odd power series; sigmoid =
  *      1/(1+exp(-l)); sqrtsoftplus = sqrt(max(l,0) + log1p(exp(-|l|)));
- *      softmax normalises by a sum taken in the R1 order over experts.
+ *      softmax normalises by a sum over experts taken as 32 partials
+ *      (partial j takes e = j, j+32, ... ascending) and the same tree.
  *      Division and sqrt are IEEE correctly rounded.
  *   R3 selection score = score + correction bias (when given); the bias never
  *      enters the routing weights.
@@ -166,11 +168,16 @@ typedef struct {
     int use_hash;
 } orc_route_cfg;
 
-/* R1: one router logit in the pinned order. */
+/* R1: one router logit in the pinned order: 32 partial sums, partial j takes
+ * the h with floor((h mod 64) / 2) = j (the pairs 2j, 2j+1 of every 64) in
+ * ascending order with fma; then the pairwise tree s = 16, 8, 4, 2, 1. */
 float orc_router_logit(const uint16_t* x, const float* w, int H) {
     float p[32];
     for (int j = 0; j < 32; ++j) p[j] = 0.0f;
-    for (int h = 0; h < H; ++h) p[h & 31] = fmaf(bf16_to_f32(x[h]), w[h], p[h & 31]);
+    for (int h = 0; h < H; ++h) {
+        const int j = (h >> 1) & 31;
+        p[j] = fmaf(bf16_to_f32(x[h]), w[h], p[j]);
+    }
     for (int s = 16; s >= 1; s >>= 1)
         for (int i = 0; i < s; ++i) p[i] = p[i] + p[i + s];
     return p[0];
