@@ -201,6 +201,9 @@ class Workload:
             self.act_s = e(T, cfg.shared_I)
             self.ys = e(T, cfg.H, dt=torch.float32)
         self.pws = e(max(1, self.lib.gbmoe_permute_workspace_size(T, k, P)), dt=torch.uint8)
+        self.ready = e(P, dt=torch.int32)
+        # moe_forward runs both expert GEMMs as one launch for small groups
+        self.fused = bool(self.lib.gbmoe_expert_mlp_fused(P, N, cfg.H))
         self.stream = torch.cuda.current_stream()
 
     def forward(self):
@@ -228,11 +231,17 @@ class Workload:
                             p(self.r2t), p(self.f2r), p(self.x_perm), p(self.pws),
                             self.pws.numel(), s)
         ev[2].record(self.stream)
-        st |= L.moe_gemm_gateup_act(p(self.x_perm), p(self.offsets), P, N, H, I, p(d["w_gate"]),
-                                    p(d["w_up"]), 0, p(self.act), s)
-        ev[3].record(self.stream)
-        st |= L.moe_gemm_down(p(self.act), p(self.offsets), P, N, H, I, p(d["w_down"]), p(self.y),
-                              s)
+        if self.fused:
+            st |= L.moe_expert_mlp(p(self.x_perm), p(self.offsets), P, N, H, I, p(d["w_gate"]),
+                                   p(d["w_up"]), p(d["w_down"]), p(self.act), p(self.y),
+                                   p(self.ready), s)
+            ev[3].record(self.stream)
+        else:
+            st |= L.moe_gemm_gateup_act(p(self.x_perm), p(self.offsets), P, N, H, I,
+                                        p(d["w_gate"]), p(d["w_up"]), 0, p(self.act), s)
+            ev[3].record(self.stream)
+            st |= L.moe_gemm_down(p(self.act), p(self.offsets), P, N, H, I, p(d["w_down"]),
+                                  p(self.y), s)
         ev[4].record(self.stream)
         ys = None
         if cfg.shared_I:
@@ -250,8 +259,9 @@ class Workload:
     def launches_per_step(self):
         cfg = self.cfg
         # route: logits + select; permute: hist, column scan, scatter, gather;
-        # gate/up GEMM, down GEMM (+2 for the shared expert); combine
-        return 2 + 4 + 2 + (2 if cfg.shared_I else 0) + 1
+        # gate/up GEMM and down GEMM, or both in one fused launch (+2 for the
+        # shared expert); combine
+        return 2 + 4 + (1 if self.fused else 2) + (2 if cfg.shared_I else 0) + 1
 
 
 def time_device(fn, steps, warmup, torch, barrier=None):
@@ -275,7 +285,8 @@ def time_device(fn, steps, warmup, torch, barrier=None):
 
 
 def stage_times(wl, steps, torch):
-    names = ["route", "permute", "gemm_gateup", "gemm_down", "shared_expert", "combine"]
+    names = ["route", "permute", "expert_mlp_fused" if wl.fused else "gemm_gateup",
+             "gemm_down", "shared_expert", "combine"]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
     for _ in range(3):
         wl.staged(evs[0])
@@ -285,16 +296,22 @@ def stage_times(wl, steps, torch):
     torch.cuda.synchronize()
     out = {}
     for j, n in enumerate(names):
+        if n == "gemm_down" and wl.fused:
+            continue
         out[n] = sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
     return out  # ms per step
 
 
-def touched_bytes(cfg, counts):
+def touched_bytes(cfg, counts, fused=False):
     """Algorithmic bytes of the gate/up GEMM: weights of experts with rows,
-    the permuted activations read and the SwiGLU output written."""
+    the permuted activations read and the SwiGLU output written.  Fused with
+    the down GEMM: all three weight matrices of the touched experts, plus the
+    activations read back and the fp32 expert outputs written."""
     touched = int((counts > 0).sum())
-    w = touched * 2 * cfg.I * cfg.H * 2
+    w = touched * (3 if fused else 2) * cfg.I * cfg.H * 2
     xa = cfg.N * cfg.H * 2 + cfg.N * cfg.I * 2
+    if fused:
+        xa += cfg.N * cfg.I * 2 + cfg.N * cfg.H * 4
     return w + xa, touched
 
 
@@ -470,13 +487,16 @@ def main(argv=None):
     stages = stage_times(wl, min(args.steps, 20), torch)
     counts = wl.counts.cpu().numpy()
     peaks, peak_src = load_peaks()
-    alg_bytes, touched = touched_bytes(cfg, counts)
-    g1 = stages["gemm_gateup"] / 1000.0
+    alg_bytes, touched = touched_bytes(cfg, counts, wl.fused)
+    g1 = stages["expert_mlp_fused" if wl.fused else "gemm_gateup"] / 1000.0
     hbm = peaks["hbm_gbs"]
-    roof = {"kernel": "grouped_gemm gate/up + SwiGLU (tcgen05)", "bound": "hbm",
+    kname = ("grouped_gemm gate/up + SwiGLU + down, one launch (tcgen05)" if wl.fused
+             else "grouped_gemm gate/up + SwiGLU (tcgen05)")
+    roof = {"kernel": kname, "bound": "hbm",
             "achieved": alg_bytes / g1 / 1e9, "peak": hbm, "unit": "GB/s",
             "frac": alg_bytes / g1 / 1e9 / hbm,
-            "traffic": profiled_traffic("gemm_gateup", cfg.name),
+            "traffic": profiled_traffic("expert_mlp_fused" if wl.fused else "gemm_gateup",
+                                        cfg.name),
             "algorithmic_bytes": alg_bytes, "touched_experts": touched,
             "peak_source": f"{peak_src} hbm_gbs"}
     t_e2e, h2d, d2h = e2e_time(wl, args.steps, args.warmup, torch)
@@ -507,8 +527,8 @@ def main(argv=None):
         s2 = time_device(w2.forward, max(3, args.steps // 2), args.warmup, torch, barrier)
         stg2 = stage_times(w2, min(args.steps, 10), torch)
         steps2 = max(3, args.steps // 2)
-        flops = 2.0 * c2.N * 2 * c2.H * c2.I
-        g1b = stg2["gemm_gateup"] / 1000.0
+        flops = 2.0 * c2.N * (3 if w2.fused else 2) * c2.H * c2.I
+        g1b = stg2["expert_mlp_fused" if w2.fused else "gemm_gateup"] / 1000.0
         peak_t = peaks["bf16_tflops_sustained"]
         line["prefill" if args.secondary == "prefill" else args.secondary] = {
             "workload": c2.name, "T": c2.T,
@@ -518,7 +538,8 @@ def main(argv=None):
             "roofline": {"kernel": "grouped_gemm gate/up + SwiGLU (tcgen05)", "bound": "tensor",
                          "achieved": flops / g1b / 1e12, "peak": peak_t, "unit": "TFLOP/s",
                          "frac": flops / g1b / 1e12 / peak_t,
-                         "traffic": profiled_traffic("gemm_gateup", c2.name),
+                         "traffic": profiled_traffic(
+                             "expert_mlp_fused" if w2.fused else "gemm_gateup", c2.name),
                          "peak_source": f"{peak_src} bf16_tflops_sustained"},
         }
         line["gpu_launches"] += w2.launches_per_step() * steps2

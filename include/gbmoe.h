@@ -240,6 +240,27 @@ int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N
                   const uint16_t* w_down, float* y, gbmoe_stream_t stream);
 
 /*
+ * moe_expert_mlp — both grouped GEMMs of the routed experts ("Stage 4":
+ * grouped matmul gate/up -> SwiGLU -> grouped matmul down), exactly the
+ * results of moe_gemm_gateup_act followed by moe_gemm_down, and the way
+ * moe_forward runs them.  When gbmoe_expert_mlp_fused(E_phys, N, H) is 1 and
+ * `ready` is non-NULL, the two run as one launch: the down tiles of an expert
+ * start as soon as all of that expert's activation tiles are written.
+ *   x_perm, offsets, w_gate, w_up, w_down, act, y as for the two calls above
+ *   (act is written and then read back: it must not alias x_perm or y);
+ *   ready: [E_phys] int32 device scratch, overwritten (NULL: two launches).
+ * Errors as for the two calls; a fused launch whose wait runs out records
+ * GBMOE_ERR_TIMEOUT in the device status (gbmoe_check_device_status).
+ */
+int moe_expert_mlp(const uint16_t* x_perm, const int32_t* offsets, int E_phys, int N, int H,
+                   int I, const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                   uint16_t* act, float* y, int32_t* ready, gbmoe_stream_t stream);
+
+/* 1 if moe_expert_mlp (and moe_forward) runs the two GEMMs as one launch for
+ * this shape (groups averaging fewer than 96 rows, H a multiple of 256). */
+int gbmoe_expert_mlp_fused(int E_phys, int N, int H);
+
+/*
  * moe_combine — restore token order and apply the routing probabilities
  * ("Stage 4" table, AllGather combine), plus the shared expert's output
  * ("Forward Skeleton": shared experts).

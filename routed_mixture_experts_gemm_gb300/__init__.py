@@ -7,7 +7,8 @@ non-zero status.  There is no CPU or Python fallback: without the built
 library every call raises.
 
 Functions carry the C names: moe_route, moe_permute, moe_gemm_gateup_act,
-moe_gemm_down, moe_combine, moe_expert_counts, moe_forward, moe_forward_host.
+moe_gemm_down, moe_expert_mlp, moe_combine, moe_expert_counts, moe_forward,
+moe_forward_host.
 """
 from __future__ import annotations
 
@@ -20,7 +21,8 @@ from . import _lib
 from ._lib import ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
 
 __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_permute",
-           "moe_gemm_gateup_act", "moe_gemm_down", "moe_combine", "MoELayer", "moe_forward",
+           "moe_gemm_gateup_act", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
+           "moe_combine", "MoELayer", "moe_forward",
            "moe_forward_host", "check_device_status", "library"]
 
 
@@ -150,6 +152,29 @@ def moe_gemm_down(act, offsets, w_down, y=None, stream=None):
     _check(lib.moe_gemm_down(_ptr(act), _ptr(offsets), P, N, H, I, _ptr(w_down), _ptr(y),
                              _stream(stream)), "moe_gemm_down")
     return y
+
+
+def moe_expert_mlp(x_perm, offsets, w_gate, w_up, w_down, act=None, y=None, ready=None,
+                   stream=None):
+    """Both grouped GEMMs (gate/up + SwiGLU, then down) as moe_forward runs them;
+    returns (act, y).  `ready` ([E_phys] int32 scratch) enables the fused launch."""
+    lib = _lib.load()
+    N, H = x_perm.shape
+    P, I, _ = w_gate.shape
+    dev = x_perm.device
+    if act is None:
+        act = torch.empty((N, I), dtype=torch.bfloat16, device=dev)
+    if y is None:
+        y = torch.empty((N, H), dtype=torch.float32, device=dev)
+    _check(lib.moe_expert_mlp(_ptr(x_perm), _ptr(offsets), P, N, H, I, _ptr(w_gate), _ptr(w_up),
+                              _ptr(w_down), _ptr(act), _ptr(y), _ptr(ready), _stream(stream)),
+           "moe_expert_mlp")
+    return act, y
+
+
+def expert_mlp_fused(E_phys: int, N: int, H: int) -> bool:
+    """Whether moe_expert_mlp / moe_forward fuse the two GEMMs for this shape."""
+    return bool(_lib.load().gbmoe_expert_mlp_fused(E_phys, N, H))
 
 
 def moe_combine(y, flat_to_row, weights, shared_y=None, out=None, stream=None):

@@ -290,6 +290,33 @@ int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
+int gbmoe_expert_mlp_fused(int E_phys, int N, int H) {
+    return gemm_fused_eligible(E_phys, N, H) ? 1 : 0;
+}
+
+int moe_expert_mlp(const uint16_t* x_perm, const int32_t* offsets, int E_phys, int N, int H,
+                   int I, const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                   uint16_t* act, float* y, int32_t* ready, gbmoe_stream_t stream) {
+    if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
+    if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
+    if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
+    if (H % 128 || I % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (N == 0) return GBMOE_OK;
+    if (!x_perm || !w_gate || !w_up || !w_down || !act || !y) return GBMOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(act) || !aligned16(y))
+        return GBMOE_ERR_INVALID_ARG;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (ready && gemm_fused_eligible(E_phys, N, H))
+        return launch_gemm_mlp_fused(x_perm, offsets, E_phys, N, H, I, w_gate, w_up, w_down, act,
+                                     y, ready, *ctx, s);
+    int st = launch_gemm_gateup(x_perm, offsets, E_phys, N, H, I, w_gate, w_up, act, *ctx, s);
+    if (st) return st;
+    return launch_gemm_down(act, offsets, E_phys, N, H, I, w_down, y, *ctx, s);
+}
+
 int moe_combine(const float* y, const int32_t* flat_to_row, const float* weights,
                 const float* shared_y, int T, int k, int H, uint16_t* out,
                 gbmoe_stream_t stream) {

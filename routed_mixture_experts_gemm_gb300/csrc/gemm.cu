@@ -565,17 +565,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // uses the 128B swizzle, bk = 32 the 64B swizzle (matching smem_desc_kmajor).
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_rows,
               int bk) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {K, rows};
-    const cuuint64_t strides[1] = {K * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(bk), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, K, rows, K * 2,
+                         static_cast<uint32_t>(bk), box_rows,
+                         bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Maps of one GEMM: weights [groups * R, K] (a1 may be null: a copy of a0)
@@ -612,6 +604,20 @@ int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
 }
 
 }  // namespace
+
+bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+                   uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int gemm_max_groups() { return MAX_GROUPS; }
 

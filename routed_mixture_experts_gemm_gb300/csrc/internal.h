@@ -2,6 +2,7 @@
 // translation units.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -18,6 +19,13 @@ struct DevCtx {
 
 // Lazily created per-device context for the current device (nullptr on failure).
 const DevCtx* device_ctx();
+
+// 2-D TMA tensor map over a row-major [rows, inner] array whose rows are
+// row_bytes apart; box {box_inner, box_rows}.  False if the driver entry point
+// is unavailable or the encode rejects the arguments (gemm.cu).
+bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+                   uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle);
 
 // --- routing (route.cu) ---
 struct RouteArgs {

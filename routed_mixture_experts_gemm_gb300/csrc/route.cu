@@ -8,9 +8,10 @@
 // (logical topk_ids mapped through log2phy).
 //
 // Reproducibility: the router logit of (t, e) is accumulated in a fixed fp32
-// order -- 32 partial sums, partial j takes h = j, j+32, ... ascending with a
-// fused multiply-add, then the pairwise tree over the 32 partials (a warp
-// xor-butterfly computes exactly that tree) -- and the scoring functions are
+// order -- 32 partial sums, partial j takes h = 2j, 2j+1, 64+2j, 65+2j, ...
+// ascending with a fused multiply-add, then the pairwise tree over the 32
+// partials (a warp xor-butterfly computes exactly that tree) -- and the
+// scoring functions are
 // this library's own (exp by Cody-Waite reduction plus the degree-7 Taylor
 // polynomial; log1p by the atanh series; IEEE division and sqrt).  With every
 // step written with explicitly rounded intrinsics, expert ids and routing
@@ -87,8 +88,9 @@ __device__ __forceinline__ float warp_sum_tree(float v) {
 }
 
 // ------------------------------------------------------ router logits
-// Block = 16 warps arranged 4 (tokens) x 4 (experts); warp tile WT x WE;
-// lane j owns h = j, j+32, ... for every (t, e) of its warp tile.
+// Generic path (any H, any alignment).  Block = 16 warps arranged 4 (tokens)
+// x 4 (experts); warp tile WT x WE; lane j owns partial j of every (t, e) of
+// its warp tile: h = 2j, 2j+1, 64+2j, 65+2j, ... ascending.
 template <int WT, int WE>
 __global__ void __launch_bounds__(512) router_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
@@ -107,16 +109,22 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
     for (int i = 0; i < WT; ++i)
 #pragma unroll
         for (int j = 0; j < WE; ++j) acc[i][j] = 0.0f;
-    for (int h = lane; h < H; h += 32) {
-        float xv[WT], wv[WE];
+    for (int h0 = 2 * lane; h0 < H; h0 += 64) {
 #pragma unroll
-        for (int i = 0; i < WT; ++i) xv[i] = bf16_bits_to_f32(__ldg(x + xo[i] + h));
+        for (int m = 0; m < 2; ++m) {
+            const int h = h0 + m;
+            if (h < H) {
+                float xv[WT], wv[WE];
 #pragma unroll
-        for (int j = 0; j < WE; ++j) wv[j] = __ldg(w + wo[j] + h);
+                for (int i = 0; i < WT; ++i) xv[i] = bf16_bits_to_f32(__ldg(x + xo[i] + h));
 #pragma unroll
-        for (int i = 0; i < WT; ++i)
+                for (int j = 0; j < WE; ++j) wv[j] = __ldg(w + wo[j] + h);
 #pragma unroll
-            for (int j = 0; j < WE; ++j) acc[i][j] = __fmaf_rn(xv[i], wv[j], acc[i][j]);
+                for (int i = 0; i < WT; ++i)
+#pragma unroll
+                    for (int j = 0; j < WE; ++j) acc[i][j] = __fmaf_rn(xv[i], wv[j], acc[i][j]);
+            }
+        }
     }
 #pragma unroll
     for (int i = 0; i < WT; ++i)
@@ -129,27 +137,6 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
         }
 }
 
-// Shared-memory tiled variant (H % 32 == 0, 16-byte aligned x and w).  A
-// block of 8 warps covers BT = 8*WT tokens x BE = 8*WE experts; H is walked
-// in chunks of 256 (eight h-steps of 32 lanes), double-buffered: router
-// weight rows arrive by cp.async in their natural layout (lane j reads
-// w[e][h0 + 32 i + j], consecutive words), token rows are transposed on the
-// way in so lane j finds its eight values x[t][h0 + j + 32 i], i = 0..7, in
-// one 16-byte word.  Lane j still accumulates h = j, j+32, ... ascending, so
-// the result is the same pinned sum as router_logits_kernel.
-constexpr int kChunk = 256;
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
 // Two fp32 fused multiply-adds in one instruction (fma.rn.f32x2): each half
 // is an ordinary round-to-nearest fma, so results are those of two fmaf.
 __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
@@ -158,170 +145,223 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
-__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
-    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+__device__ __forceinline__ unsigned long long pair_u32(uint32_t lo, uint32_t hi) {
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ float pair_lo(unsigned long long v) {
+    return __uint_as_float(static_cast<uint32_t>(v));
+}
+__device__ __forceinline__ float pair_hi(unsigned long long v) {
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
 }
 
-// Block = 8 warps covering BT = 8*WT tokens x BE = 8*WE experts; each warp
-// owns 8 tokens (four pairs, one per 64-bit accumulator) x 8 experts.  Token
-// chunks are stored pair-interleaved: for token pair p, lane j and h-step i
-// one 32-bit word holds the two tokens' bf16 x[h0 + j + 32 i]; a lane's 8
-// words (32 B) are two 16-byte halves, swapped for lanes with bit 2 set so
-// that the quarter-warp reading them hits distinct banks.
-template <int WT, int WE>
-__global__ void __launch_bounds__(256, 2) router_logits_tiled_kernel(
-    const uint16_t* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
-    int T, int E, int H, float* __restrict__ logits) {
-    constexpr int TP = 4, TE = 8;          // token pairs and experts per warp
-    constexpr int BT = 2 * TP * WT, BE = TE * WE;
-    constexpr int BP = BT / 2;             // token pairs per block
-    constexpr int XV = BP * (kChunk / 8);  // (pair, 8-h) units per chunk
-    constexpr int XR = (XV + 255) / 256;   // per thread
-    constexpr int WV = BE * (kChunk / 4);  // 16-byte weight vectors per chunk
-    static_assert(WT * WE == 8, "8 warps per block");
-    extern __shared__ __align__(16) uint8_t route_smem[];
-    // xs: [2][BP][32 lanes][2 halves][4 words]; ws: [2][BE][kChunk] fp32
-    uint32_t* xs = reinterpret_cast<uint32_t*>(route_smem);
-    auto ws = reinterpret_cast<float(*)[BE][kChunk]>(route_smem + 2 * BP * 32 * 8 * 4);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wt = warp / WE, we = warp % WE;
-    const int t0 = blockIdx.x * BT, e0 = blockIdx.y * BE;
-    const int nc = (H + kChunk - 1) / kChunk;
-
-    uint4 xa[XR], xb[XR];
-    auto load_x = [&](int c) {
-        const int h0 = c * kChunk;
+// TMA-fed path (H % KC == 0, 16-byte aligned rows).  KC-wide column chunks
+// of a BT-token x tile (bf16, [BT][KC]) and a BE-expert router-weight tile
+// (fp32, [BE][KC]) stream through a STAGES-deep ring in their natural
+// layout; WTW x WEW warps each own TT tokens x 8 experts.  Lane 0 of warp 0
+// also keeps the ring full: at chunk c it refills the stage of chunk c - 2
+// once every warp has released it, so the ring runs STAGES - 2 chunks ahead
+// and no warp is spent on loads alone (a block of 8 warps leaves each SM
+// sub-partition two warps and the full register budget).  In every 64-wide
+// round of a chunk lane j reads its pair h = 2j, 2j+1 as one 32-bit word
+// per token (both bf16 values) and one 64-bit word per expert --
+// conflict-free, since the 32 lanes cover consecutive words.  Two tokens
+// share one fma.rn.f32x2 (x of both tokens times the weight duplicated into
+// both halves), so a lane accumulates TT/2 x 8 packed pairs = TT x 8 partial
+// sums, each in exactly the pinned order.  The 32 partials of every logit
+// are then reduced by a transposing xor-butterfly: at level s lanes l and l^s
+// add their halves of the remaining values, which is the pinned pairwise
+// tree, and each lane ends with TT/4 finished logits.  Every ring wait is
+// bounded: a wait that gives up raises an abort flag, records
+// GBMOE_ERR_TIMEOUT and the block stores nothing.
+// Level S of the transposing butterfly over the first N values: the lane
+// keeps the upper half iff (lane & S) and adds the partner's copy of it.
+template <int NV, int N, int S>
+__device__ __forceinline__ void transpose_butterfly(float (&v)[NV], int lane) {
+    const bool up = (lane & S) != 0;
 #pragma unroll
-        for (int r = 0; r < XR; ++r) {
-            const int idx = tid + r * 256;
-            xa[r] = xb[r] = make_uint4(0, 0, 0, 0);
-            if (idx < XV) {
-                const int pr = idx / (kChunk / 8), q = idx % (kChunk / 8);
-                const int t = t0 + 2 * pr, h = h0 + 8 * q;
-                if (h < H) {
-                    if (t < T)
-                        xa[r] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + h));
-                    if (t + 1 < T)
-                        xb[r] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t + 1) * H + h));
-                }
-            }
-        }
-    };
-    auto store_x = [&](int buf) {
-#pragma unroll
-        for (int r = 0; r < XR; ++r) {
-            const int idx = tid + r * 256;
-            if (idx < XV) {
-                const int pr = idx / (kChunk / 8), q = idx % (kChunk / 8);
-                const int i = q >> 2, j0 = (q & 3) * 8;
-                const uint32_t va[4] = {xa[r].x, xa[r].y, xa[r].z, xa[r].w};
-                const uint32_t vb[4] = {xb[r].x, xb[r].y, xb[r].z, xb[r].w};
-                uint32_t* dst = xs + (buf * BP + pr) * 256;
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int j = j0 + jj;
-                    const uint32_t lo = (jj & 1) ? (va[jj >> 1] >> 16) : (va[jj >> 1] & 0xffffu);
-                    const uint32_t hi = (jj & 1) ? (vb[jj >> 1] >> 16) : (vb[jj >> 1] & 0xffffu);
-                    const int half = (i >> 2) ^ ((j >> 2) & 1);
-                    dst[j * 8 + half * 4 + (i & 3)] = lo | (hi << 16);
-                }
-            }
-        }
-    };
-    auto load_w = [&](int c, int buf) {
-        const int h0 = c * kChunk;
-        for (int idx = tid; idx < WV; idx += 256) {
-            const int row = idx / (kChunk / 4), q = idx % (kChunk / 4);
-            const int e = e0 + row, h = h0 + 4 * q;
-            if (e < E && h < H) cp_async16(&ws[buf][row][4 * q], w + static_cast<size_t>(e) * H + h);
-        }
-        cp_async_commit();
-    };
-
-    unsigned long long acc[TP][TE];
-#pragma unroll
-    for (int a = 0; a < TP; ++a)
-#pragma unroll
-        for (int b = 0; b < TE; ++b) acc[a][b] = 0ull;
-
-    load_w(0, 0);
-    load_x(0);
-    store_x(0);
-    cp_async_wait_all();
-    __syncthreads();
-    const int sw = (lane >> 2) & 1;
-    for (int c = 0; c < nc; ++c) {
-        const int buf = c & 1;
-        if (c + 1 < nc) {
-            load_w(c + 1, buf ^ 1);
-            load_x(c + 1);
-        }
-        const int n_i = min(8, (H - c * kChunk) / 32);
-        uint32_t xp[TP][8];  // word i of token pair a: (x[t][h], x[t+1][h]), h = h0 + lane + 32 i
-#pragma unroll
-        for (int a = 0; a < TP; ++a) {
-            const uint32_t* src = xs + (buf * BP + wt * TP + a) * 256 + lane * 8;
-            const uint4 v0 = *reinterpret_cast<const uint4*>(src + 4 * sw);
-            const uint4 v1 = *reinterpret_cast<const uint4*>(src + 4 * (sw ^ 1));
-            xp[a][0] = v0.x; xp[a][1] = v0.y; xp[a][2] = v0.z; xp[a][3] = v0.w;
-            xp[a][4] = v1.x; xp[a][5] = v1.y; xp[a][6] = v1.z; xp[a][7] = v1.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i < n_i) {
-                unsigned long long wd[TE];
-#pragma unroll
-                for (int b = 0; b < TE; ++b) {
-                    const float wv = ws[buf][we * TE + b][32 * i + lane];
-                    wd[b] = pack2(wv, wv);
-                }
-#pragma unroll
-                for (int a = 0; a < TP; ++a) {
-                    const uint32_t pk = xp[a][i];
-                    const unsigned long long xv =
-                        pack2(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u));
-#pragma unroll
-                    for (int b = 0; b < TE; ++b) acc[a][b] = fma2(xv, wd[b], acc[a][b]);
-                }
-            }
-        }
-        if (c + 1 < nc) store_x(buf ^ 1);
-        cp_async_wait_all();
-        __syncthreads();
+    for (int i = 0; i < N / 2; ++i) {
+        const float send = up ? v[i] : v[i + N / 2];
+        const float keep = up ? v[i + N / 2] : v[i];
+        v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, S));
     }
+    if constexpr (S > 1) transpose_butterfly<NV, N / 2, S / 2>(v, lane);
+}
+
+template <int TT, int WTW, int WEW, int KC, int STAGES, int LAG_ = 1>
+struct RouterTile {
+    static constexpr int TE = 8;
+    static constexpr int KC_ = KC;
+    static constexpr int LAG = LAG_;  // chunks between a stage's release and its refill
+    static constexpr int BT = TT * WTW, BE = TE * WEW;
+    static constexpr int WARPS = WTW * WEW;
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int X_BYTES = BT * KC * 2;
+    static constexpr int W_BYTES = BE * KC * 4;
+    static constexpr int STAGE_BYTES = X_BYTES + W_BYTES;
+    static constexpr int OFF_BARS = STAGES * STAGE_BYTES;
+    static constexpr int SMEM_BYTES = OFF_BARS + 2 * STAGES * 8 + 16 + 128;  // + base alignment
+    static_assert(TT % 4 == 0 && TT * TE >= 32, "the transposing reduction needs >= 32 values");
+    static_assert(KC % 64 == 0 && KC <= 256, "chunks are whole 64-wide rounds, <= 256 (TMA box)");
+    static_assert(STAGE_BYTES % 128 == 0, "stage alignment");
+    static_assert(STAGES > LAG && STAGES <= 32, "ring depth");
+};
+
+constexpr uint64_t kRouteWaitNs = 2000000000ull;
+
+template <int TT, int WTW, int WEW, int KC, int STAGES, int LAG_ = 1>
+__global__ void __launch_bounds__(RouterTile<TT, WTW, WEW, KC, STAGES, LAG_>::THREADS, 1)
+router_logits_tma_kernel(const __grid_constant__ CUtensorMap mx,
+                         const __grid_constant__ CUtensorMap mw, const float* __restrict__ bias,
+                         int T, int E, int H, float* __restrict__ logits, int* status) {
+    using L = RouterTile<TT, WTW, WEW, KC, STAGES, LAG_>;
+    constexpr int TE = L::TE, NP = TT / 2, NV = TT * TE;
+    extern __shared__ uint8_t route_smem[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(route_smem) + 127) & ~static_cast<uintptr_t>(127));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BARS);
+    uint64_t* empty = full + STAGES;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * L::BT, e0 = blockIdx.y * L::BE;
+    const int nc = H / KC;
+    const bool producer = warp == 0 && lane == 0;
+    const uint64_t pol = l2_policy_evict_last();  // both tiles are re-read by other blocks
+
+    auto issue = [&](int c) {
+        const int st = c % STAGES;
+        mbar_arrive_expect_tx(full + st, L::STAGE_BYTES);
+        uint8_t* xs = smem + st * L::STAGE_BYTES;
+        tma_load_2d(xs, &mx, full + st, c * KC, t0, pol);
+        tma_load_2d(xs + L::X_BYTES, &mw, full + st, c * KC, e0, pol);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, L::WARPS);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    int issued = 0;  // chunks whose loads lane 0 of warp 0 has issued
+    if (producer) {
+        tma_prefetch_desc(&mx);
+        tma_prefetch_desc(&mw);
+        for (; issued < min(STAGES, nc); ++issued) issue(issued);
+    }
+
+    const int wt = warp / WEW, we = warp % WEW;
+    unsigned long long acc[NP][TE];
 #pragma unroll
-    for (int a = 0; a < TP; ++a)
+    for (int a = 0; a < NP; ++a)
 #pragma unroll
-        for (int b = 0; b < TE; ++b)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const float part = __uint_as_float(static_cast<uint32_t>(acc[a][b] >> (32 * u)));
-                const float v = warp_sum_tree(part);
-                const int t = t0 + wt * 2 * TP + 2 * a + u, e = e0 + we * TE + b;
-                if (lane == ((a * 2 * TE + u * TE + b) & 31) && t < T && e < E)
-                    logits[static_cast<size_t>(t) * E + e] = bias ? __fadd_rn(v, __ldg(bias + e)) : v;
+        for (int e = 0; e < TE; ++e) acc[a][e] = 0ull;
+    bool ok = true;
+    for (int c = 0; c < nc; ++c) {
+        const int stage = c % STAGES;
+        const uint32_t phase = static_cast<uint32_t>(c / STAGES) & 1u;
+        if (warp == 0) {
+            if (lane == 0 && c >= L::LAG && issued < nc) {
+                const int cp = c - L::LAG;  // issued == cp + STAGES here
+                if (mbar_wait_bounded(empty + cp % STAGES, static_cast<uint32_t>(cp / STAGES) & 1u,
+                                      abort_flag, status, kRouteWaitNs))
+                    issue(issued++);
             }
+            __syncwarp();
+        }
+        // every lane waits; the vote keeps the warp together if one gives up
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(full + stage, phase, abort_flag, status, kRouteWaitNs))) {
+            ok = false;
+            break;
+        }
+        const uint8_t* xs = smem + stage * L::STAGE_BYTES;
+        const uint32_t* xrow = reinterpret_cast<const uint32_t*>(xs) + (wt * TT) * (KC / 2) + lane;
+        const unsigned long long* wrow =
+            reinterpret_cast<const unsigned long long*>(xs + L::X_BYTES) + (we * TE) * (KC / 2) +
+            lane;
+#pragma unroll
+        for (int r = 0; r < KC / 64; ++r) {
+            uint32_t xw[TT];
+#pragma unroll
+            for (int t = 0; t < TT; ++t) xw[t] = xrow[t * (KC / 2) + r * 32];
+            unsigned long long wp[TE];
+#pragma unroll
+            for (int e = 0; e < TE; ++e) wp[e] = wrow[e * (KC / 2) + r * 32];
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                unsigned long long xv[NP];
+#pragma unroll
+                for (int a = 0; a < NP; ++a) {
+                    const uint32_t u0 = xw[2 * a], u1 = xw[2 * a + 1];
+                    xv[a] = m ? pair_u32(u0 & 0xffff0000u, u1 & 0xffff0000u)
+                              : pair_u32(u0 << 16, u1 << 16);
+                }
+#pragma unroll
+                for (int e = 0; e < TE; ++e) {
+                    const uint32_t v = m ? __float_as_uint(pair_hi(wp[e]))
+                                         : __float_as_uint(pair_lo(wp[e]));
+                    const unsigned long long wd = pair_u32(v, v);
+#pragma unroll
+                    for (int a = 0; a < NP; ++a) acc[a][e] = fma2(xv[a], wd, acc[a][e]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + stage);
+    }
+    if (!ok) {
+        if (producer) {  // let every copy this thread issued land before the block exits
+            for (int c = max(0, issued - STAGES); c < issued; ++c)
+                mbar_wait_timeout(full + c % STAGES, static_cast<uint32_t>(c / STAGES) & 1u,
+                                  200000000ull);
+        }
+        return;
+    }
+
+    // v[(a*8 + e)*2 + u]: token wt*TT + 2a + u, expert we*8 + e
+    float v[NV];
+#pragma unroll
+    for (int a = 0; a < NP; ++a)
+#pragma unroll
+        for (int e = 0; e < TE; ++e) {
+            v[(a * TE + e) * 2] = pair_lo(acc[a][e]);
+            v[(a * TE + e) * 2 + 1] = pair_hi(acc[a][e]);
+        }
+    transpose_butterfly<NV, NV, 16>(v, lane);
+    // the lane holds values p = base + i, i < NV/32, base from its lane bits
+    constexpr int NL = NV / 32;
+    const int base = (((lane >> 4) & 1) * (NV / 2)) + (((lane >> 3) & 1) * (NV / 4)) +
+                     (((lane >> 2) & 1) * (NV / 8)) + (((lane >> 1) & 1) * (NV / 16)) +
+                     ((lane & 1) * (NV / 32));
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+        const int p = base + i;
+        const int u = p & 1, e = (p >> 1) % TE, a = (p >> 1) / TE;
+        const int t = t0 + wt * TT + 2 * a + u, ex = e0 + we * TE + e;
+        if (t < T && ex < E)
+            logits[static_cast<size_t>(t) * E + ex] = bias ? __fadd_rn(v[i], __ldg(bias + ex)) : v[i];
+    }
 }
 
 // ----------------------------------------------------------- selection
-struct Cand {
-    bool ok;
-    float v;
-    int idx;
-};
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-    return a.ok && (!b.ok || a.v > b.v || (a.v == b.v && a.idx < b.idx));
+// Monotone map of fp32 onto u32 (a larger value gives a larger key; -0 is
+// folded onto +0 so that equal values tie).  Key 0 means "no candidate".
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ Cand warp_argmax(Cand c) {
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        Cand o;
-        o.ok = __shfl_xor_sync(0xffffffffu, static_cast<int>(c.ok), s) != 0;
-        o.v = __shfl_xor_sync(0xffffffffu, c.v, s);
-        o.idx = __shfl_xor_sync(0xffffffffu, c.idx, s);
-        if (better(o, c)) c = o;
-    }
-    return c;
+
+// Lane holding the largest key, the lowest such lane on ties; -1 if no lane
+// has a candidate.
+__device__ __forceinline__ int warp_pick(uint32_t key) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+    if (m == 0u) return -1;
+    return __ffs(__ballot_sync(0xffffffffu, key == m)) - 1;
 }
 
 template <int EPL>
@@ -333,7 +373,13 @@ __device__ __forceinline__ float pick(const float (&a)[EPL], int idx) {
     return v;
 }
 
-// One warp per token.  Lane L holds experts e = L + 32 i, i < EPL.
+// One warp per token.  Lane L holds the EPL consecutive experts
+// e = EPL*L + i, so expert order is (lane, slot) order: a warp-wide
+// "largest key, lowest lane" pick after an in-lane "largest value, lowest
+// slot" pick is exactly "largest value, lowest expert index".  When every
+// expert group spans a power-of-two block of whole lanes (E = 256 in 8 groups:
+// 4 lanes of 8 experts each) the group top-2 is an in-lane top-2 merged
+// across the block; other shapes take a loop over the groups.
 template <int EPL>
 __global__ void __launch_bounds__(256) route_select_kernel(const RouteArgs a, int* status) {
     const int lane = threadIdx.x & 31;
@@ -342,30 +388,37 @@ __global__ void __launch_bounds__(256) route_select_kernel(const RouteArgs a, in
     const gbmoe_route_cfg& c = a.cfg;
     const int E = c.E_log, k = c.top_k;
     const float* lrow = a.logits + static_cast<size_t>(t) * E;
+    const int eb = EPL * lane;
 
     float sc[EPL];
+    if (EPL % 4 == 0 && E % 4 == 0 && eb + EPL <= E &&
+        (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        sc[i] = e < E ? lrow[e] : 0.0f;
+        for (int i = 0; i < EPL; i += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(lrow + eb + i);
+            sc[i] = v.x;
+            sc[i + 1] = v.y;
+            sc[i + 2] = v.z;
+            sc[i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) sc[i] = eb + i < E ? lrow[eb + i] : 0.0f;
     }
     if (c.scoring == GBMOE_SCORE_SOFTMAX) {
         float m = kNegInf;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-            if (lane + 32 * i < E) m = fmaxf(m, sc[i]);
+            if (eb + i < E) m = fmaxf(m, sc[i]);
 #pragma unroll
         for (int s = 16; s >= 1; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+        // denominator in the pinned order: partial j takes e = j, j+32, ...
         float part = 0.0f;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (lane + 32 * i < E) {
-                sc[i] = pinned_exp(__fsub_rn(sc[i], m));
-                part = __fadd_rn(part, sc[i]);
-            }
+        for (int e = lane; e < E; e += 32) part = __fadd_rn(part, pinned_exp(__fsub_rn(lrow[e], m)));
         const float S = warp_sum_tree(part);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) sc[i] = __fdiv_rn(sc[i], S);
+        for (int i = 0; i < EPL; ++i)
+            if (eb + i < E) sc[i] = __fdiv_rn(pinned_exp(__fsub_rn(sc[i], m)), S);
     } else if (c.scoring == GBMOE_SCORE_SIGMOID) {
 #pragma unroll
         for (int i = 0; i < EPL; ++i) sc[i] = pinned_sigmoid(sc[i]);
@@ -392,7 +445,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(const RouteArgs a, in
         }
         for (int j = 0; j < k; ++j) {
             const int ej = __shfl_sync(0xffffffffu, e, j);
-            const float s = __shfl_sync(0xffffffffu, pick<EPL>(sc, ej >> 5), ej & 31);
+            const float s = __shfl_sync(0xffffffffu, pick<EPL>(sc, ej % EPL), ej / EPL);
             if (lane == j) {
                 my_e = ej;
                 my_s = s;
@@ -403,7 +456,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(const RouteArgs a, in
         uint32_t allowed = 0;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
+            const int e = eb + i;
             sel[i] = kNegInf;
             if (e < E) {
                 sel[i] = a.corr_bias ? __fadd_rn(sc[i], __ldg(a.corr_bias + e)) : sc[i];
@@ -412,13 +465,13 @@ __global__ void __launch_bounds__(256) route_select_kernel(const RouteArgs a, in
         }
         if (c.n_group > 1) {
             const int G = c.n_group, gs = E / G;
-            float my_g = 0.0f;
-            for (int g = 0; g < G; ++g) {
+            const bool top2 = c.group_score == GBMOE_GROUP_TOP2SUM && gs > 1;
+            const int lpg = gs / EPL;  // lanes per group on the fast path
+            if (gs % EPL == 0 && lpg <= 32 && (lpg & (lpg - 1)) == 0) {
                 float b1 = kNegInf, b2 = kNegInf;
 #pragma unroll
                 for (int i = 0; i < EPL; ++i) {
-                    const int e = lane + 32 * i;
-                    if (e < E && e / gs == g) {
+                    if ((allowed >> i) & 1u) {
                         const float v = sel[i];
                         if (v > b1) {
                             b2 = b1;
@@ -428,45 +481,81 @@ __global__ void __launch_bounds__(256) route_select_kernel(const RouteArgs a, in
                         }
                     }
                 }
-#pragma unroll
-                for (int s = 16; s >= 1; s >>= 1) {
+                for (int s = 1; s < lpg; s <<= 1) {
                     const float o1 = __shfl_xor_sync(0xffffffffu, b1, s);
                     const float o2 = __shfl_xor_sync(0xffffffffu, b2, s);
                     const float n2 = fmaxf(fminf(b1, o1), fmaxf(b2, o2));
                     b1 = fmaxf(b1, o1);
                     b2 = n2;
                 }
-                const float gsc =
-                    (c.group_score == GBMOE_GROUP_TOP2SUM && gs > 1) ? __fadd_rn(b1, b2) : b1;
-                if (lane == g) my_g = gsc;
-            }
-            uint32_t keep = 0;
-            for (int r = 0; r < c.topk_group; ++r) {
-                Cand cd{lane < G && !((keep >> lane) & 1u), my_g, lane};
-                cd = warp_argmax(cd);
-                keep |= 1u << cd.idx;
-            }
+                const float gsc = top2 ? __fadd_rn(b1, b2) : b1;
+                const bool leader = (lane % lpg) == 0 && eb < E;
+                bool kept = false;
+                for (int r = 0; r < c.topk_group; ++r) {
+                    const int wl = warp_pick(leader && !kept ? order_key(gsc) : 0u);
+                    if (lane == wl) kept = true;
+                }
+                kept = __shfl_sync(0xffffffffu, kept, lane & ~(lpg - 1));
+                if (!kept) allowed = 0;
+            } else {
+                int gid[EPL];
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !((keep >> (e / gs)) & 1u)) allowed &= ~(1u << i);
+                for (int i = 0; i < EPL; ++i) gid[i] = (eb + i) / gs;
+                float my_g = 0.0f;
+                for (int g = 0; g < G; ++g) {
+                    float b1 = kNegInf, b2 = kNegInf;
+#pragma unroll
+                    for (int i = 0; i < EPL; ++i) {
+                        if (((allowed >> i) & 1u) && gid[i] == g) {
+                            const float v = sel[i];
+                            if (v > b1) {
+                                b2 = b1;
+                                b1 = v;
+                            } else if (v > b2) {
+                                b2 = v;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int s = 16; s >= 1; s >>= 1) {
+                        const float o1 = __shfl_xor_sync(0xffffffffu, b1, s);
+                        const float o2 = __shfl_xor_sync(0xffffffffu, b2, s);
+                        const float n2 = fmaxf(fminf(b1, o1), fmaxf(b2, o2));
+                        b1 = fmaxf(b1, o1);
+                        b2 = n2;
+                    }
+                    if (lane == g) my_g = top2 ? __fadd_rn(b1, b2) : b1;
+                }
+                uint32_t keep = 0;
+                for (int r = 0; r < c.topk_group; ++r) {
+                    const int wl = warp_pick(lane < G && !((keep >> lane) & 1u) ? order_key(my_g) : 0u);
+                    if (wl >= 0) keep |= 1u << wl;
+                }
+#pragma unroll
+                for (int i = 0; i < EPL; ++i)
+                    if (!((keep >> gid[i]) & 1u)) allowed &= ~(1u << i);
             }
         }
         for (int j = 0; j < k; ++j) {
-            Cand cd{false, 0.0f, 0};
+            int bi = -1;
+            float bv = 0.0f;
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
-                if ((allowed >> i) & 1u) {
-                    const Cand o{true, sel[i], lane + 32 * i};
-                    if (better(o, cd)) cd = o;
+                if (((allowed >> i) & 1u) && (bi < 0 || sel[i] > bv)) {
+                    bi = i;
+                    bv = sel[i];
                 }
             }
-            cd = warp_argmax(cd);
-            const int be = cd.idx;
-            if (lane == (be & 31)) allowed &= ~(1u << (be >> 5));
-            const float s = __shfl_sync(0xffffffffu, pick<EPL>(sc, be >> 5), be & 31);
+            const int wl = warp_pick(bi >= 0 ? order_key(bv) : 0u);
+            if (wl < 0) {  // fewer allowed experts than k (excluded by validation)
+                record_error(status, GBMOE_ERR_DEVICE);
+                break;
+            }
+            const int wi = __shfl_sync(0xffffffffu, bi, wl);
+            if (lane == wl) allowed &= ~(1u << bi);
+            const float s = __shfl_sync(0xffffffffu, pick<EPL>(sc, wi), wl);
             if (lane == j) {
-                my_e = be;
+                my_e = EPL * wl + wi;
                 my_s = s;
             }
         }
@@ -511,34 +600,60 @@ __global__ void expert_counts_kernel(const int32_t* __restrict__ ids, int64_t n,
     }
 }
 
-template <int WT, int WE>
-constexpr int tiled_smem_bytes() {
-    return 2 * (4 * WT) * 32 * 8 * 4 + 2 * (8 * WE) * kChunk * 4;
+// Router-logit tile variants (measured on the 8192- and 128-token routers):
+// many tokens -> 16-token x 8-expert warp tiles, 2 x 4 warps (32 x 32
+// blocks); few tokens -> 4 x 8 warp tiles, 4 x 2 warps (16 x 16 blocks), so
+// that a decode batch still spreads over the GPU.  256-wide chunks (4-deep
+// ring) when H allows, else 128-wide (6-deep): fewer ring hand-offs per FMA.
+using RouterBig256 = RouterTile<16, 2, 4, 256, 4>;
+using RouterBig128 = RouterTile<16, 2, 4, 128, 6>;
+using RouterSmall256 = RouterTile<4, 4, 2, 256, 4>;
+using RouterSmall128 = RouterTile<4, 4, 2, 128, 6>;
+#define ROUTER_BIG256 router_logits_tma_kernel<16, 2, 4, 256, 4>
+#define ROUTER_BIG128 router_logits_tma_kernel<16, 2, 4, 128, 6>
+#define ROUTER_SMALL256 router_logits_tma_kernel<4, 4, 2, 256, 4>
+#define ROUTER_SMALL128 router_logits_tma_kernel<4, 4, 2, 128, 6>
+
+std::mutex g_route_attr_mu;
+bool g_route_attr_done[64];
+
+cudaError_t ensure_route_attrs(int device) {
+    std::lock_guard<std::mutex> lk(g_route_attr_mu);
+    if (device >= 0 && device < 64 && g_route_attr_done[device]) return cudaSuccess;
+    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(ROUTER_BIG256, a, RouterBig256::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ROUTER_BIG128, a, RouterBig128::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ROUTER_SMALL256, a, RouterSmall256::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ROUTER_SMALL128, a, RouterSmall128::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (device >= 0 && device < 64) g_route_attr_done[device] = true;
+    return cudaSuccess;
 }
 
-template <int WT, int WE>
-cudaError_t launch_tiled(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s) {
-    static bool attr_done[64];
-    static std::mutex mu;
-    constexpr int smem = tiled_smem_bytes<WT, WE>();
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        if (ctx.device < 0 || ctx.device >= 64 || !attr_done[ctx.device]) {
-            cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel<WT, WE>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess) return e;
-            if (ctx.device >= 0 && ctx.device < 64) attr_done[ctx.device] = true;
-        }
-    }
-    dim3 grid((a.T + 8 * WT - 1) / (8 * WT), (a.cfg.E_log + 8 * WE - 1) / (8 * WE));
-    router_logits_tiled_kernel<WT, WE><<<grid, 256, smem, s>>>(a.x, a.w_router, a.router_bias, a.T,
-                                                               a.cfg.E_log, a.H, a.logits);
+template <class L, class K>
+cudaError_t launch_router_tma(K kernel, const RouteArgs& a, const DevCtx& ctx, cudaStream_t s,
+                              bool* launched) {
+    *launched = false;
+    const int E = a.cfg.E_log;
+    CUtensorMap mx, mw;
+    if (!encode_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.H, a.T,
+                       static_cast<uint64_t>(a.H) * 2, L::KC_, L::BT, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.w_router, a.H, E,
+                       static_cast<uint64_t>(a.H) * 4, L::KC_, L::BE, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaSuccess;  // not encodable: the caller takes the generic path
+    const cudaError_t e = ensure_route_attrs(ctx.device);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.T + L::BT - 1) / L::BT, (E + L::BE - 1) / L::BE);
+    kernel<<<grid, L::THREADS, L::SMEM_BYTES, s>>>(mx, mw, a.router_bias, a.T, E, a.H, a.logits,
+                                                   ctx.status);
+    *launched = true;
     return cudaGetLastError();
 }
 
 template <int EPL>
 cudaError_t launch_select(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s) {
-    const int warps_per_block = 8;
+    // small batches: two tokens per block so that the warps spread over the SMs
+    const int warps_per_block = a.T >= 8 * ctx.num_sms ? 8 : 2;
     const int blocks = (a.T + warps_per_block - 1) / warps_per_block;
     route_select_kernel<EPL><<<blocks, 32 * warps_per_block, 0, s>>>(a, ctx.status);
     return cudaGetLastError();
@@ -549,18 +664,21 @@ cudaError_t launch_select(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s)
 cudaError_t launch_route(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
     const int E = a.cfg.E_log;
-    const bool tiled = a.w_router && a.H % 32 == 0 &&
-                       (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 &&
-                       (reinterpret_cast<uintptr_t>(a.w_router) & 15u) == 0;
-    if (tiled) {
-        // few tokens: one token tile of 8, 64 experts per block; many tokens:
-        // 16 x 32 tiles (more blocks, router weight re-read less often)
+    bool done = false;
+    if (a.w_router && a.H % 128 == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 &&
+        (reinterpret_cast<uintptr_t>(a.w_router) & 15u) == 0) {
+        const long big_blocks =
+            static_cast<long>((a.T + RouterBig256::BT - 1) / RouterBig256::BT) *
+            ((E + RouterBig256::BE - 1) / RouterBig256::BE);
+        const bool big = big_blocks >= 2L * ctx.num_sms, wide = a.H % 256 == 0;
         const cudaError_t err =
-            static_cast<long>((a.T + 15) / 16) * ((E + 31) / 32) >= 4L * ctx.num_sms
-                ? launch_tiled<2, 4>(a, ctx, s)
-                : launch_tiled<1, 8>(a, ctx, s);
+            big ? (wide ? launch_router_tma<RouterBig256>(ROUTER_BIG256, a, ctx, s, &done)
+                        : launch_router_tma<RouterBig128>(ROUTER_BIG128, a, ctx, s, &done))
+                : (wide ? launch_router_tma<RouterSmall256>(ROUTER_SMALL256, a, ctx, s, &done)
+                        : launch_router_tma<RouterSmall128>(ROUTER_SMALL128, a, ctx, s, &done));
         if (err != cudaSuccess) return err;
-    } else if (a.w_router) {
+    }
+    if (a.w_router && !done) {
         // small batches: thin token tiles so the grid still covers the GPU
         const long big_blocks = ((a.T + 31) / 32) * static_cast<long>((E + 31) / 32);
         if (big_blocks >= 2L * ctx.num_sms) {

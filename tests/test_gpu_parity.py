@@ -7,6 +7,8 @@ activations and outputs within |gpu - oracle| <= 1e-2 + 1e-2 |oracle| per
 element, plus a tighter diagnostic (max error <= 2 bf16 ulps of the output
 scale) because the small workloads' outputs are ~1e-2 in magnitude.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -75,6 +77,59 @@ def test_scoring_functions_bit_exact(built, scoring):
     o = gb.moe_route(cfg, logits=torch.from_numpy(l).to(DEV))
     ocfg = oracle.route_cfg(E, 32, scoring, renormalize=False, routed_scaling=1.0)
     ids, _, w = oracle.route(ocfg, l)
+    assert np.array_equal(_np(o["ids_log"]), ids)
+    assert np.array_equal(_np(o["weights"]).view(np.uint32), w.view(np.uint32))
+
+
+# router-logit paths: TMA tiles of 32 tokens x 32 experts (many tokens), of
+# 16 x 16 (few tokens, ragged token and expert tails), each with 256- and
+# 128-wide chunks (H % 256 == 0 or not), and the generic kernel for H not a
+# multiple of 128
+LOGIT_SHAPES = [(1024, 320, 256), (1024, 320, 384), (37, 40, 384), (1, 256, 7168),
+                (128, 256, 1024), (9, 8, 200), (300, 64, 96)]
+
+
+@pytest.mark.parametrize("shape", LOGIT_SHAPES)
+def test_router_logit_paths_bit_exact(built, shape):
+    gb = built
+    T, E, H = shape
+    rng = np.random.default_rng(T * 7 + E + H)
+    from tests.test_oracle_mlp import _bf16_bits
+    x = _bf16_bits(rng.standard_normal((T, H)))
+    w = (rng.standard_normal((E, H)) * 0.05).astype(np.float32)
+    b = rng.standard_normal(E).astype(np.float32)
+    cfg = gb.route_cfg(E, min(4, E), "sigmoid")
+    o = gb.moe_route(cfg, x=bf16_dev(x, DEV), w_router=torch.from_numpy(w).to(DEV),
+                     router_bias=torch.from_numpy(b).to(DEV))
+    assert gb.check_device_status() == 0
+    ref = oracle.router_logits(x, w, router_bias=b, nthreads=8)
+    assert np.array_equal(_np(o["logits"]).view(np.uint32), ref.view(np.uint32))
+
+
+# grouped top-k: lane-aligned groups (E=256/8, 384/8, 96/6) and the general
+# group loop (E=60/5, 40/4, 200/8); logits on a coarse grid so that scores,
+# group scores and selections tie often
+SELECT_CASES = [(256, 8, 4, 8, "top2sum"), (384, 8, 4, 8, "max"), (96, 6, 3, 6, "top2sum"),
+                (60, 5, 2, 7, "top2sum"), (40, 4, 2, 5, "max"), (200, 8, 3, 8, "top2sum")]
+
+
+@pytest.mark.parametrize("case", SELECT_CASES)
+@pytest.mark.parametrize("scoring", ["sigmoid", "softmax"])
+def test_grouped_selection_paths_bit_exact(built, case, scoring):
+    gb = built
+    E, G, kg, k, mode = case
+    T = 257
+    rng = np.random.default_rng(E + G + k)
+    l = (np.round(rng.standard_normal((T, E)) * 4) / 4).astype(np.float32)
+    cb = (np.round(rng.standard_normal(E) * 8) / 64).astype(np.float32)
+    cfg = gb.route_cfg(E, k, scoring, n_group=G, topk_group=kg, group_score=mode,
+                       routed_scaling=2.5)
+    o = gb.moe_route(cfg, logits=torch.from_numpy(l).to(DEV),
+                     corr_bias=torch.from_numpy(cb).to(DEV))
+    assert gb.check_device_status() == 0
+    ocfg = oracle.route_cfg(E, k, scoring, n_group=G, topk_group=kg, group_score=mode,
+                            routed_scaling=2.5)
+    ids, _, w = oracle.route(ocfg, l, corr_bias=cb)
     assert np.array_equal(_np(o["ids_log"]), ids)
     assert np.array_equal(_np(o["weights"]).view(np.uint32), w.view(np.uint32))
 
@@ -276,11 +331,11 @@ GEMM_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("shape", GEMM_SHAPES)
-def test_gemm_tile_variants(built, shape):
-    gb = built
+def _gemm_case(shape):
+    """Random bf16 tokens and expert weights for grouped GEMMs with the given
+    (H, I, rows per group), and the oracle's act and y."""
     H, I, rows = shape
-    rng = np.random.default_rng(H + I)
+    rng = np.random.default_rng(H + I + len(rows))
     P = len(rows)
     offs = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
     N = int(offs[-1])
@@ -293,15 +348,72 @@ def test_gemm_tile_variants(built, shape):
     y_o = np.zeros((N, H), np.float32)
     for p in range(P):
         if rows[p]:
-            a, y = oracle.expert_ffn_rows(xb[offs[p]:offs[p + 1]], *W[p])
+            a, y = oracle.expert_ffn_rows(xb[offs[p]:offs[p + 1]], *W[p], nthreads=4)
             act_o[offs[p]:offs[p + 1]] = a
             y_o[offs[p]:offs[p + 1]] = y
-    dev_offs = torch.from_numpy(offs).to(DEV)
-    wg = bf16_dev(np.stack([w[0] for w in W]), DEV)
-    wu = bf16_dev(np.stack([w[1] for w in W]), DEV)
-    wd = bf16_dev(np.stack([w[2] for w in W]), DEV)
-    act = gb.moe_gemm_gateup_act(bf16_dev(xb, DEV), dev_offs, wg, wu)
-    y = gb.moe_gemm_down(bf16_dev(act_o, DEV), dev_offs, wd)
+    dev = {"offs": torch.from_numpy(offs).to(DEV), "x": bf16_dev(xb, DEV),
+           "wg": bf16_dev(np.stack([w[0] for w in W]), DEV),
+           "wu": bf16_dev(np.stack([w[1] for w in W]), DEV),
+           "wd": bf16_dev(np.stack([w[2] for w in W]), DEV)}
+    return dev, act_o, y_o
+
+
+@pytest.mark.parametrize("shape", GEMM_SHAPES)
+def test_gemm_tile_variants(built, shape):
+    gb = built
+    d, act_o, y_o = _gemm_case(shape)
+    act = gb.moe_gemm_gateup_act(d["x"], d["offs"], d["wg"], d["wu"])
+    y = gb.moe_gemm_down(bf16_dev(act_o, DEV), d["offs"], d["wd"])
     assert gb.check_device_status() == 0
     assert_within_tol(_bf(act), synth.bf16_to_f32(act_o), f"act {shape}")
     assert_within_tol(_np(y), y_o, f"y {shape}")
+
+
+# both GEMMs through moe_expert_mlp: fused in one launch (groups averaging
+# < 96 rows, H % 256 == 0) or as two launches; the 64-group shape has more
+# tiles than SMs, so down tiles wait on gate/up tiles of other CTAs
+MLP_SHAPES = [
+    ((512, 128, [40, 3, 17, 0, 90]), True),
+    ((256, 256, [1, 0, 0, 7, 64, 33, 2, 95]), True),
+    ((1024, 512, [20 + (p * 7) % 23 for p in range(64)]), True),
+    ((768, 256, [513, 129]), False),
+    ((384, 128, [40, 3, 17, 0, 90]), False),
+]
+
+
+@pytest.mark.parametrize("shape,fused", MLP_SHAPES)
+def test_expert_mlp_fused_and_separate(built, shape, fused):
+    gb = built
+    H, I, rows = shape
+    assert gb.expert_mlp_fused(len(rows), sum(rows), H) == fused
+    d, act_o, y_o = _gemm_case(shape)
+    ready = torch.full((len(rows),), 12345, dtype=torch.int32, device=DEV)
+    offs = _np(d["offs"])
+    wd = _bf(d["wd"]).astype(np.float64)
+    for rd in (ready, None):
+        act, y = gb.moe_expert_mlp(d["x"], d["offs"], d["wg"], d["wu"], d["wd"], ready=rd)
+        assert gb.check_device_status() == 0
+        assert_within_tol(_bf(act), synth.bf16_to_f32(act_o), f"act {shape}")
+        # y is the down GEMM of the GPU's own activations (a one-ulp flip of a
+        # large bf16 activation moves y by more than the output tolerance, so
+        # y is checked against y = act . W_down^T taken in fp64 from those
+        # activations, to within fp32 accumulation error)
+        a64 = _bf(act).astype(np.float64)
+        y_ref = np.zeros_like(y_o, dtype=np.float64)
+        bound = np.zeros_like(y_ref)
+        for p in range(len(rows)):
+            r0, r1 = offs[p], offs[p + 1]
+            y_ref[r0:r1] = a64[r0:r1] @ wd[p].T
+            bound[r0:r1] = np.abs(a64[r0:r1]) @ np.abs(wd[p]).T
+        err = np.abs(_np(y).astype(np.float64) - y_ref)
+        assert np.all(err <= 2.0 ** -12 * bound + 1e-30), f"y {shape}: max err {err.max()}"
+        if rd is not None and fused:
+            # every gate/up tile of every group published exactly once: a group
+            # of r rows is cut into ceil(r / 128) equal token blocks (a multiple
+            # of 16 rows each), times I / 128 weight blocks
+            def blocks(r):
+                if r == 0:
+                    return 0
+                rpb = 16 * math.ceil(math.ceil(r / math.ceil(r / 128)) / 16)
+                return math.ceil(r / rpb)
+            assert _np(ready).tolist() == [(I // 128) * blocks(r) for r in rows]
