@@ -258,10 +258,12 @@ class Workload:
 
     def launches_per_step(self):
         cfg = self.cfg
-        # route: logits + select; permute: hist, column scan, scatter, gather;
-        # gate/up GEMM and down GEMM, or both in one fused launch (+2 for the
-        # shared expert); combine
-        return 2 + 4 + (1 if self.fused else 2) + (2 if cfg.shared_I else 0) + 1
+        # route: logits + select; permute: one block (N <= 4096, P <= 1024) or
+        # histogram, column scan, scatter; then the row gather; gate/up GEMM
+        # and down GEMM, or both in one fused launch (+2 for the shared
+        # expert); combine
+        perm = 2 if (cfg.N <= 4096 and cfg.P <= 1024) else 4
+        return 2 + perm + (1 if self.fused else 2) + (2 if cfg.shared_I else 0) + 1
 
 
 def time_device(fn, steps, warmup, torch, barrier=None):

@@ -169,15 +169,150 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) perm_scatter_kernel(
     }
 }
 
-__global__ void __launch_bounds__(256) perm_gather_kernel(const uint4* __restrict__ x, int64_t N,
-                                                          int vec_per_row,
-                                                          const int32_t* __restrict__ row_to_token,
-                                                          uint4* __restrict__ x_perm) {
-    for (int64_t r = blockIdx.x; r < N; r += gridDim.x) {
+// Small batches (N <= kSmallPermMaxN, P <= 1024): the whole permutation in
+// one block of 32 warps.  Warp w takes the contiguous flat range
+// [w*per, (w+1)*per); its per-expert counts, turned into an exclusive prefix
+// over warps, then the running count of its own earlier indices, give every
+// index its stable rank -- the same order as the multi-kernel path.
+constexpr int64_t kSmallPermMaxN = 4096;
+constexpr int kSmallPermMaxP = 1024;
+
+__global__ void __launch_bounds__(1024) perm_small_kernel(
+    const int32_t* __restrict__ ids, int64_t N, int k, int P, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ row_to_token,
+    int32_t* __restrict__ flat_to_row, int* status) {
+    extern __shared__ int32_t perm_sm[];
+    int32_t* hist = perm_sm;           // [32][P]: counts, then exclusive prefix, then running
+    int32_t* offs = perm_sm + 32 * P;  // [P]
+    __shared__ int wsum[32];
+    __shared__ int total;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 32 * P; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const int64_t per = (N + 31) / 32;
+    const int64_t f0 = min(N, warp * per), f1 = min(N, f0 + per);
+    const unsigned lt = (1u << lane) - 1u;
+    int32_t* h = hist + warp * P;
+    auto expert_of = [&](int64_t f) {
+        int p = -1;
+        if (f < f1) {
+            p = ids[f];
+            if (p < 0 || p >= P) p = -1;
+        }
+        return p;
+    };
+    // 1. per-warp counts
+    for (int64_t b0 = f0; b0 < f1; b0 += 32) {
+        const int64_t f = b0 + lane;
+        const int p = expert_of(f);
+        if (p < 0 && f < f1) record_error(status, GBMOE_ERR_DEVICE);
+        const unsigned peers = __match_any_sync(0xffffffffu, p);
+        if (p >= 0 && __popc(peers & lt) == 0) h[p] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // 2. exclusive prefix over warps, per expert; totals are the counts
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int v = hist[w * P + p];
+            hist[w * P + p] = run;
+            run += v;
+        }
+        offs[p] = run;
+    }
+    __syncthreads();
+    // 3. offsets = exclusive scan of the counts (one expert per thread)
+    {
+        const int p = threadIdx.x;
+        const int v = p < P ? offs[p] : 0;
+        int incl = v;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, s);
+            if (lane >= s) incl += o;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int wv = wsum[lane];
+            int wi = wv;
+#pragma unroll
+            for (int s = 1; s < 32; s <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, wi, s);
+                if (lane >= s) wi += o;
+            }
+            wsum[lane] = wi - wv;
+            if (lane == 31) total = wi;
+        }
+        __syncthreads();
+        const int ex = wsum[warp] + incl - v;
+        if (p < P) {
+            counts[p] = v;
+            offsets[p] = ex;
+            offs[p] = ex;
+        }
+        if (p == 0) offsets[P] = total;
+    }
+    __syncthreads();
+    // 4. rows, walking each range again in order
+    for (int64_t b0 = f0; b0 < f1; b0 += 32) {
+        const int64_t f = b0 + lane;
+        const int p = expert_of(f);
+        const unsigned peers = __match_any_sync(0xffffffffu, p);
+        const int rank = __popc(peers & lt);
+        if (p >= 0) {
+            const int r = offs[p] + h[p] + rank;
+            row_to_token[r] = static_cast<int32_t>(f / k);
+            flat_to_row[f] = r;
+        }
+        __syncwarp();
+        if (p >= 0 && rank == 0) h[p] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// x_perm[r] = x[row_to_token[r]]: one warp per row, four 16-byte loads in
+// flight per lane; x rows are kept in L2 (each is read k times), x_perm is
+// streamed out.
+__device__ __forceinline__ uint4 ld_keep(const uint4* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(32 * kGatherWarps) perm_gather_kernel(
+    const uint4* __restrict__ x, int64_t N, int vec_per_row,
+    const int32_t* __restrict__ row_to_token, uint4* __restrict__ x_perm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kGatherWarps + warp; r < N;
+         r += static_cast<int64_t>(gridDim.x) * kGatherWarps) {
         const int64_t t = row_to_token[r];
         const uint4* src = x + t * vec_per_row;
         uint4* dst = x_perm + r * vec_per_row;
-        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = __ldg(src + v);
+        for (int v0 = 0; v0 < vec_per_row; v0 += 128) {
+            uint4 buf[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u + lane;
+                if (v < vec_per_row) buf[u] = ld_keep(src + v, keep);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + 32 * u + lane;
+                if (v < vec_per_row) st_stream(dst + v, buf[u], stream);
+            }
+        }
     }
 }
 
@@ -198,21 +333,38 @@ cudaError_t launch_permute(const int32_t* ids_phys, int64_t N, int k, int E_phys
         if (e != cudaSuccess) return e;
         return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (P + 1), s);
     }
-    const PermWs w = perm_ws(ws, N, P);
-    const int64_t W = n_workers(N);
-    const int blocks = static_cast<int>((W + kWarpsPerBlock - 1) / kWarpsPerBlock);
-    const size_t smem = sizeof(int32_t) * P * kWarpsPerBlock;
-    perm_hist_kernel<<<blocks, 32 * kWarpsPerBlock, smem, s>>>(ids_phys, N, P, w.hist, w.done,
-                                                               ctx.status);
-    perm_colscan_kernel<<<P, 256, 0, s>>>(w.hist, W, P, counts, offsets, w.done);
-    perm_scatter_kernel<<<blocks, 32 * kWarpsPerBlock, smem, s>>>(ids_phys, N, k, P, w.hist,
-                                                                  offsets, row_to_token,
-                                                                  flat_to_row);
+    if (N <= kSmallPermMaxN && P <= kSmallPermMaxP) {
+        const size_t smem = sizeof(int32_t) * 33 * P;
+        static bool attr_done[64];
+        if (ctx.device >= 0 && ctx.device < 64 && !attr_done[ctx.device]) {
+            cudaError_t e = cudaFuncSetAttribute(perm_small_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(sizeof(int32_t) * 33 *
+                                                                  kSmallPermMaxP));
+            if (e != cudaSuccess) return e;
+            attr_done[ctx.device] = true;
+        }
+        perm_small_kernel<<<1, 1024, smem, s>>>(ids_phys, N, k, P, counts, offsets, row_to_token,
+                                                flat_to_row, ctx.status);
+    } else {
+        const PermWs w = perm_ws(ws, N, P);
+        const int64_t W = n_workers(N);
+        const int blocks = static_cast<int>((W + kWarpsPerBlock - 1) / kWarpsPerBlock);
+        const size_t smem = sizeof(int32_t) * P * kWarpsPerBlock;
+        perm_hist_kernel<<<blocks, 32 * kWarpsPerBlock, smem, s>>>(ids_phys, N, P, w.hist, w.done,
+                                                                   ctx.status);
+        perm_colscan_kernel<<<P, 256, 0, s>>>(w.hist, W, P, counts, offsets, w.done);
+        perm_scatter_kernel<<<blocks, 32 * kWarpsPerBlock, smem, s>>>(ids_phys, N, k, P, w.hist,
+                                                                      offsets, row_to_token,
+                                                                      flat_to_row);
+    }
     if (x_perm) {
         const int vec = H / 8;
-        const int grid = static_cast<int>(std::min<int64_t>(N, 8L * ctx.num_sms));
-        perm_gather_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), N, vec,
-                                                row_to_token, reinterpret_cast<uint4*>(x_perm));
+        const int64_t want = (N + kGatherWarps - 1) / kGatherWarps;
+        const int grid = static_cast<int>(std::min<int64_t>(want, 8L * ctx.num_sms));
+        perm_gather_kernel<<<grid, 32 * kGatherWarps, 0, s>>>(
+            reinterpret_cast<const uint4*>(x), N, vec, row_to_token,
+            reinterpret_cast<uint4*>(x_perm));
     }
     return cudaGetLastError();
 }

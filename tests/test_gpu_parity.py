@@ -170,6 +170,36 @@ def test_permute_bit_exact(built, name):
     assert np.array_equal(xp, case.inputs["x"][ref["row_to_token"]])
 
 
+# both permutation paths: one block for N = T*k <= 4096 (and P <= 1024), the
+# histogram / column-scan / scatter kernels above; skewed ids leave experts
+# empty and pile rows onto a few
+PERM_SHAPES = [(1, 1, 5), (3, 8, 1024), (512, 8, 256), (513, 8, 256), (1000, 8, 300),
+               (2048, 6, 1000), (4096, 8, 288)]
+
+
+@pytest.mark.parametrize("shape", PERM_SHAPES)
+def test_permute_paths_bit_exact(built, shape):
+    gb = built
+    T, k, P = shape
+    rng = np.random.default_rng(T + k + P)
+    # Zipf-like skew over experts, k distinct experts per token when possible
+    wts = 1.0 / np.arange(1, P + 1) ** 1.1
+    wts /= wts.sum()
+    ids = np.stack([rng.choice(P, size=k, replace=k > P, p=wts) for _ in range(T)]).astype(np.int32)
+    H = 64
+    from tests.test_oracle_mlp import _bf16_bits
+    x = _bf16_bits(rng.standard_normal((T, H)))
+    o = gb.moe_permute(torch.from_numpy(ids).to(DEV), P, x=bf16_dev(x, DEV))
+    assert gb.check_device_status() == 0
+    counts, offsets, r2t, f2r = oracle.permute(ids, P)
+    assert np.array_equal(_np(o["counts"]), counts)
+    assert np.array_equal(_np(o["offsets"]), offsets)
+    assert np.array_equal(_np(o["row_to_token"]), r2t)
+    assert np.array_equal(_np(o["flat_to_row"]), f2r)
+    xp = _np(o["x_perm"].view(torch.int16)).view(np.uint16)
+    assert np.array_equal(xp, x[r2t])
+
+
 @pytest.mark.parametrize("name", SMALL)
 def test_grouped_gemms(built, name):
     gb = built
