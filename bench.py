@@ -37,6 +37,7 @@ import statistics
 import subprocess
 import sys
 import threading
+import datetime
 import time
 
 import numpy as np
@@ -115,31 +116,40 @@ def profiled_traffic(kernel: str, wl: str):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) during the timed region."""
+    """nvidia-smi samples (every 50 ms) of SM clock, power and throttle reasons;
+    only samples taken between mark_start() and mark_end() are summarised."""
 
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 50):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         time.sleep(0.3)
         return self
 
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
+
     def __exit__(self, *a):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -149,22 +159,30 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, pw, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in getattr(self, "lines", []):
             f = [x.strip() for x in l.split(",")]
             try:
-                sm.append(float(f[0]))
-                mx = float(f[1])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                clk, m = float(f[1]), float(f[2])
             except (ValueError, IndexError):
                 continue
-            for n, v in zip(names, f[3:7]):
+            if self.t0 is not None and not (self.t0 <= ts <= self.t1):
+                continue
+            sm.append(clk)
+            mx = m
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
+            for n, v in zip(names, f[4:8]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_median": statistics.median(pw) if pw else None}
 
 
 # --------------------------------------------------------------- GPU path
@@ -412,7 +430,7 @@ def dist_setup():
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--secondary", default="prefill",
@@ -476,7 +494,9 @@ def main(argv=None):
         raise RuntimeError(f"device status {st} after the first forward")
 
     with ClockSampler(local) as clk:
+        clk.mark_start()
         secs = time_device(wl.forward, args.steps, args.warmup, torch, barrier)
+        clk.mark_end()
     clocks = clk.summary()
     times = [secs]
     if world > 1:
@@ -526,16 +546,23 @@ def main(argv=None):
         c2 = workload(args.secondary)
         w2 = Workload(c2, dev)
         w2.forward()
-        s2 = time_device(w2.forward, max(3, args.steps // 2), args.warmup, torch, barrier)
+        # long enough (>= ~1 s) for the clock samples to see the sustained,
+        # power-limited state of a prefill-sized step
+        est = time_device(w2.forward, 3, args.warmup, torch, barrier) / 3
+        steps2 = max(3, args.steps // 2, int(1.0 / max(est, 1e-6)))
+        with ClockSampler(local) as clk2:
+            clk2.mark_start()
+            s2 = time_device(w2.forward, steps2, 1, torch, barrier)
+            clk2.mark_end()
         stg2 = stage_times(w2, min(args.steps, 10), torch)
-        steps2 = max(3, args.steps // 2)
         flops = 2.0 * c2.N * (3 if w2.fused else 2) * c2.H * c2.I
         g1b = stg2["expert_mlp_fused" if w2.fused else "gemm_gateup"] / 1000.0
         peak_t = peaks["bf16_tflops_sustained"]
         line["prefill" if args.secondary == "prefill" else args.secondary] = {
             "workload": c2.name, "T": c2.T,
             "value": world * c2.T * steps2 / s2, "unit": UNIT,
-            "ms_per_step": 1000.0 * s2 / steps2, "stages_ms": stg2,
+            "ms_per_step": 1000.0 * s2 / steps2, "steps": steps2, "stages_ms": stg2,
+            "clocks": clk2.summary(),
             "layer_tflops": 2.0 * c2.N * 3 * c2.H * c2.I / (s2 / steps2) / 1e12,
             "roofline": {"kernel": "grouped_gemm gate/up + SwiGLU (tcgen05)", "bound": "tensor",
                          "achieved": flops / g1b / 1e12, "peak": peak_t, "unit": "TFLOP/s",

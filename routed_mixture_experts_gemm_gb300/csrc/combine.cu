@@ -7,10 +7,11 @@
 //
 // out[t] = bf16( sum_{j=0..k-1} w[t,j] * y[flat_to_row[t*k+j]] + shared_y[t] )
 // with y and shared_y in fp32, accumulated in fp32 with fused multiply-adds
-// in the fixed order j = 0..k-1, then the shared term; one CTA per token,
-// each thread owns 8 consecutive outputs (two 16-byte loads per expert row,
-// one 16-byte bf16 store).  Memory bound: reads (k+1)*H*4 bytes and writes
-// H*2 bytes per token.
+// in the fixed order j = 0..k-1, then the shared term.  Block (t, c) covers
+// 1024 outputs of token t: each thread owns 8 consecutive outputs, issues the
+// loads of up to 8 expert rows at once (two 16-byte loads each) and only then
+// folds them in order, so a token costs one memory round trip per 8 experts.
+// Memory bound: reads (k+1)*H*4 bytes and writes H*2 bytes per token.
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,11 +31,21 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float w, const float4& a, 
     acc[7] = __fmaf_rn(w, b.w, acc[7]);
 }
 
-__global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__ y,
-                                                      const int32_t* __restrict__ flat_to_row,
-                                                      const float* __restrict__ weights,
-                                                      const float4* __restrict__ shared_y, int k,
-                                                      int H, uint4* __restrict__ out) {
+constexpr int kCombineThreads = 128;
+constexpr int kCombineGroup = 8;  // expert rows whose loads are in flight together
+
+__device__ __forceinline__ float4 ld_stream(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+    const float4* __restrict__ y, const int32_t* __restrict__ flat_to_row,
+    const float* __restrict__ weights, const float4* __restrict__ shared_y, int k, int H,
+    uint4* __restrict__ out) {
     __shared__ int64_t rows[kMaxK];
     __shared__ float wts[kMaxK];
     const int t = blockIdx.x;
@@ -43,34 +54,44 @@ __global__ void __launch_bounds__(128) combine_kernel(const float4* __restrict__
         wts[threadIdx.x] = weights[static_cast<int64_t>(t) * k + threadIdx.x];
     }
     __syncthreads();
+    const int v = blockIdx.y * kCombineThreads + threadIdx.x;  // group of 8 outputs
+    if (v >= H / 8) return;
     const int v4_per_row = H / 4;  // float4 per fp32 row
-    for (int v = threadIdx.x; v < H / 8; v += blockDim.x) {
-        float acc[8];
+    float acc[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const float4* src = y + rows[j] * v4_per_row + 2 * v;
-            fma8(acc, wts[j], __ldg(src), __ldg(src + 1));
-        }
-        if (shared_y) {
-            const float4* src = shared_y + static_cast<int64_t>(t) * v4_per_row + 2 * v;
-            const float4 a = __ldg(src), b = __ldg(src + 1);
-            acc[0] = __fadd_rn(acc[0], a.x);
-            acc[1] = __fadd_rn(acc[1], a.y);
-            acc[2] = __fadd_rn(acc[2], a.z);
-            acc[3] = __fadd_rn(acc[3], a.w);
-            acc[4] = __fadd_rn(acc[4], b.x);
-            acc[5] = __fadd_rn(acc[5], b.y);
-            acc[6] = __fadd_rn(acc[6], b.z);
-            acc[7] = __fadd_rn(acc[7], b.w);
-        }
-        uint32_t o[4];
+    for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += kCombineGroup) {
+        float4 a[kCombineGroup], b[kCombineGroup];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            o[q] = static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * q])) |
-                   (static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * q + 1])) << 16);
-        out[static_cast<int64_t>(t) * (H / 8) + v] = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int g = 0; g < kCombineGroup; ++g) {
+            if (j0 + g < k) {
+                const float4* src = y + rows[j0 + g] * v4_per_row + 2 * v;
+                a[g] = ld_stream(src);
+                b[g] = ld_stream(src + 1);
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < kCombineGroup; ++g)
+            if (j0 + g < k) fma8(acc, wts[j0 + g], a[g], b[g]);
     }
+    if (shared_y) {
+        const float4* src = shared_y + static_cast<int64_t>(t) * v4_per_row + 2 * v;
+        const float4 a = ld_stream(src), b = ld_stream(src + 1);
+        acc[0] = __fadd_rn(acc[0], a.x);
+        acc[1] = __fadd_rn(acc[1], a.y);
+        acc[2] = __fadd_rn(acc[2], a.z);
+        acc[3] = __fadd_rn(acc[3], a.w);
+        acc[4] = __fadd_rn(acc[4], b.x);
+        acc[5] = __fadd_rn(acc[5], b.y);
+        acc[6] = __fadd_rn(acc[6], b.z);
+        acc[7] = __fadd_rn(acc[7], b.w);
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        o[q] = static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * q])) |
+               (static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * q + 1])) << 16);
+    out[static_cast<int64_t>(t) * (H / 8) + v] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace
@@ -80,9 +101,10 @@ cudaError_t launch_combine(const float* y, const int32_t* flat_to_row, const flo
                            const DevCtx& ctx, cudaStream_t s) {
     (void)ctx;
     if (T == 0) return cudaSuccess;
-    combine_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const float4*>(y), flat_to_row, weights,
-                                     reinterpret_cast<const float4*>(shared_y), k, H,
-                                     reinterpret_cast<uint4*>(out));
+    const dim3 grid(T, (H / 8 + kCombineThreads - 1) / kCombineThreads);
+    combine_kernel<<<grid, kCombineThreads, 0, s>>>(
+        reinterpret_cast<const float4*>(y), flat_to_row, weights,
+        reinterpret_cast<const float4*>(shared_y), k, H, reinterpret_cast<uint4*>(out));
     return cudaGetLastError();
 }
 
