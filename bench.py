@@ -212,7 +212,6 @@ class Workload:
         self.offsets = e(P + 1, dt=torch.int32)
         self.r2t = e(N, dt=torch.int32)
         self.f2r = e(N, dt=torch.int32)
-        self.x_perm = e(N, cfg.H)
         self.act = e(N, cfg.I)
         self.y = e(N, cfg.H, dt=torch.float32)
         if cfg.shared_I:
@@ -245,18 +244,18 @@ class Workload:
                          rows, p(d["log2phy"]), p(d["replica_cnt"]), R, p(self.ids), p(self.idp),
                          p(self.w), None, s)
         ev[1].record(self.stream)
-        st |= L.moe_permute(p(self.idp), T, k, P, p(c.x), H, p(self.counts), p(self.offsets),
-                            p(self.r2t), p(self.f2r), p(self.x_perm), p(self.pws),
-                            self.pws.numel(), s)
+        # the permutation writes no x_perm: the gate/up GEMM gathers the rows
+        st |= L.moe_permute(p(self.idp), T, k, P, None, 0, p(self.counts), p(self.offsets),
+                            p(self.r2t), p(self.f2r), None, p(self.pws), self.pws.numel(), s)
         ev[2].record(self.stream)
         if self.fused:
-            st |= L.moe_expert_mlp(p(self.x_perm), p(self.offsets), P, N, H, I, p(d["w_gate"]),
-                                   p(d["w_up"]), p(d["w_down"]), p(self.act), p(self.y),
-                                   p(self.ready), s)
+            st |= L.moe_expert_mlp(p(c.x), p(self.r2t), T, p(self.offsets), P, N, H, I,
+                                   p(d["w_gate"]), p(d["w_up"]), p(d["w_down"]), p(self.act),
+                                   p(self.y), p(self.ready), s)
             ev[3].record(self.stream)
         else:
-            st |= L.moe_gemm_gateup_act(p(self.x_perm), p(self.offsets), P, N, H, I,
-                                        p(d["w_gate"]), p(d["w_up"]), 0, p(self.act), s)
+            st |= L.moe_gemm_gateup_act_rows(p(c.x), p(self.r2t), T, p(self.offsets), P, N, H,
+                                             I, p(d["w_gate"]), p(d["w_up"]), 0, p(self.act), s)
             ev[3].record(self.stream)
             st |= L.moe_gemm_down(p(self.act), p(self.offsets), P, N, H, I, p(d["w_down"]),
                                   p(self.y), s)
@@ -277,10 +276,10 @@ class Workload:
     def launches_per_step(self):
         cfg = self.cfg
         # route: logits + select; permute: one block (N <= 4096, P <= 1024) or
-        # histogram, column scan, scatter; then the row gather; gate/up GEMM
-        # and down GEMM, or both in one fused launch (+2 for the shared
+        # histogram, column scan, scatter (the GEMM gathers the rows); gate/up
+        # GEMM and down GEMM, or both in one fused launch (+2 for the shared
         # expert); combine
-        perm = 2 if (cfg.N <= 4096 and cfg.P <= 1024) else 4
+        perm = 1 if (cfg.N <= 4096 and cfg.P <= 1024) else 3
         return 2 + perm + (1 if self.fused else 2) + (2 if cfg.shared_I else 0) + 1
 
 
@@ -324,12 +323,13 @@ def stage_times(wl, steps, torch):
 
 def touched_bytes(cfg, counts, fused=False):
     """Algorithmic bytes of the gate/up GEMM: weights of experts with rows,
-    the permuted activations read and the SwiGLU output written.  Fused with
+    the hidden states read (each token row once: the GEMM gathers the routed
+    rows from x, repeats hit L2) and the SwiGLU output written.  Fused with
     the down GEMM: all three weight matrices of the touched experts, plus the
     activations read back and the fp32 expert outputs written."""
     touched = int((counts > 0).sum())
     w = touched * (3 if fused else 2) * cfg.I * cfg.H * 2
-    xa = cfg.N * cfg.H * 2 + cfg.N * cfg.I * 2
+    xa = cfg.T * cfg.H * 2 + cfg.N * cfg.I * 2
     if fused:
         xa += cfg.N * cfg.I * 2 + cfg.N * cfg.H * 4
     return w + xa, touched

@@ -230,6 +230,20 @@ int moe_gemm_gateup_act(const uint16_t* x_perm, const int32_t* offsets, int E_ph
                         uint16_t* act, gbmoe_stream_t stream);
 
 /*
+ * moe_gemm_gateup_act_rows — moe_gemm_gateup_act with the token operand
+ * gathered inside the GEMM: row r of the operand is x[row_to_token[r]], so no
+ * permuted copy of x is needed ("Stage 4": the dispatch's expert-sorted rows,
+ * read in place).
+ *   x [T, H] bf16; row_to_token [N] int32 (as written by moe_permute); the
+ *   other arguments as for moe_gemm_gateup_act.  An entry outside [0, T) is
+ *   read as row 0 and reported as GBMOE_ERR_DEVICE through the device status.
+ */
+int moe_gemm_gateup_act_rows(const uint16_t* x, const int32_t* row_to_token, int T,
+                             const int32_t* offsets, int E_phys, int N, int H, int I,
+                             const uint16_t* w_gate, const uint16_t* w_up, int activation,
+                             uint16_t* act, gbmoe_stream_t stream);
+
+/*
  * moe_gemm_down — grouped down GEMM ("Stage 4": grouped matmul down).
  *   y[r] = act[r] . w_down[p]^T for r in expert p's rows, fp32 accumulate,
  *   written in fp32 (inside the layer only the activation is rounded to bf16).
@@ -243,17 +257,25 @@ int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N
  * moe_expert_mlp — both grouped GEMMs of the routed experts ("Stage 4":
  * grouped matmul gate/up -> SwiGLU -> grouped matmul down), exactly the
  * results of moe_gemm_gateup_act followed by moe_gemm_down, and the way
- * moe_forward runs them.  When gbmoe_expert_mlp_fused(E_phys, N, H) is 1 and
- * `ready` is non-NULL, the two run as one launch: the down tiles of an expert
- * start as soon as all of that expert's activation tiles are written.
- *   x_perm, offsets, w_gate, w_up, w_down, act, y as for the two calls above
- *   (act is written and then read back: it must not alias x_perm or y);
- *   ready: [E_phys] int32 device scratch, overwritten (NULL: two launches).
+ * moe_forward runs them.
+ *   x_rows, row_to_token, T: the token operand.  row_to_token NULL: x_rows is
+ *     x_perm [N, H] (T ignored).  Otherwise x_rows is the unpermuted x [T, H]
+ *     and row r of the operand is x[row_to_token[r]] (row_to_token [N] as
+ *     written by moe_permute), gathered inside the GEMM: no x_perm is needed.
+ *     An entry outside [0, T) is read as row 0 and reported as
+ *     GBMOE_ERR_DEVICE through the device status.
+ *   offsets, w_gate, w_up, w_down, act, y as for the two calls above (act is
+ *   written and then read back: it must not alias the token operand or y);
+ *   ready: [E_phys] int32 device scratch, overwritten.  When
+ *   gbmoe_expert_mlp_fused(E_phys, N, H) is 1 and ready is non-NULL the two
+ *   GEMMs run as one launch: the down tiles of an expert start as soon as all
+ *   of that expert's activation tiles are written (NULL: two launches).
  * Errors as for the two calls; a fused launch whose wait runs out records
  * GBMOE_ERR_TIMEOUT in the device status (gbmoe_check_device_status).
  */
-int moe_expert_mlp(const uint16_t* x_perm, const int32_t* offsets, int E_phys, int N, int H,
-                   int I, const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+int moe_expert_mlp(const uint16_t* x_rows, const int32_t* row_to_token, int T,
+                   const int32_t* offsets, int E_phys, int N, int H, int I,
+                   const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                    uint16_t* act, float* y, int32_t* ready, gbmoe_stream_t stream);
 
 /* 1 if moe_expert_mlp (and moe_forward) runs the two GEMMs as one launch for

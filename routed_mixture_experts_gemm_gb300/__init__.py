@@ -21,7 +21,7 @@ from . import _lib
 from ._lib import ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
 
 __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_permute",
-           "moe_gemm_gateup_act", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
+           "moe_gemm_gateup_act", "moe_gemm_gateup_act_rows", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
            "moe_combine", "MoELayer", "moe_forward",
            "moe_forward_host", "check_device_status", "library"]
 
@@ -142,6 +142,20 @@ def moe_gemm_gateup_act(x_perm, offsets, w_gate, w_up, act=None, stream=None):
     return act
 
 
+def moe_gemm_gateup_act_rows(x, row_to_token, offsets, w_gate, w_up, act=None, stream=None):
+    """moe_gemm_gateup_act with row r of the operand gathered as x[row_to_token[r]]."""
+    lib = _lib.load()
+    T, H = x.shape
+    N = row_to_token.shape[0]
+    P, I, _ = w_gate.shape
+    if act is None:
+        act = torch.empty((N, I), dtype=torch.bfloat16, device=x.device)
+    _check(lib.moe_gemm_gateup_act_rows(_ptr(x), _ptr(row_to_token), T, _ptr(offsets), P, N, H,
+                                        I, _ptr(w_gate), _ptr(w_up), ACT_SWIGLU, _ptr(act),
+                                        _stream(stream)), "moe_gemm_gateup_act_rows")
+    return act
+
+
 def moe_gemm_down(act, offsets, w_down, y=None, stream=None):
     """y = act W_down^T per expert group, fp32 output [N, H]."""
     lib = _lib.load()
@@ -154,21 +168,26 @@ def moe_gemm_down(act, offsets, w_down, y=None, stream=None):
     return y
 
 
-def moe_expert_mlp(x_perm, offsets, w_gate, w_up, w_down, act=None, y=None, ready=None,
-                   stream=None):
+def moe_expert_mlp(x_rows, offsets, w_gate, w_up, w_down, act=None, y=None, ready=None,
+                   row_to_token=None, stream=None):
     """Both grouped GEMMs (gate/up + SwiGLU, then down) as moe_forward runs them;
-    returns (act, y).  `ready` ([E_phys] int32 scratch) enables the fused launch."""
+    returns (act, y).  x_rows is x_perm [N, H], or with row_to_token [N] the
+    unpermuted x [T, H] whose rows the GEMM gathers.  `ready` ([E_phys] int32
+    scratch) enables the fused launch."""
     lib = _lib.load()
-    N, H = x_perm.shape
-    P, I, _ = w_gate.shape
-    dev = x_perm.device
+    P, I, H = w_gate.shape
+    if row_to_token is None:
+        N, T = x_rows.shape[0], 0
+    else:
+        N, T = row_to_token.shape[0], x_rows.shape[0]
+    dev = x_rows.device
     if act is None:
         act = torch.empty((N, I), dtype=torch.bfloat16, device=dev)
     if y is None:
         y = torch.empty((N, H), dtype=torch.float32, device=dev)
-    _check(lib.moe_expert_mlp(_ptr(x_perm), _ptr(offsets), P, N, H, I, _ptr(w_gate), _ptr(w_up),
-                              _ptr(w_down), _ptr(act), _ptr(y), _ptr(ready), _stream(stream)),
-           "moe_expert_mlp")
+    _check(lib.moe_expert_mlp(_ptr(x_rows), _ptr(row_to_token), T, _ptr(offsets), P, N, H, I,
+                              _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(act), _ptr(y),
+                              _ptr(ready), _stream(stream)), "moe_expert_mlp")
     return act, y
 
 

@@ -46,8 +46,11 @@ SIGNATURES = {
     "moe_permute": (_i, [_vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute_static": (_i, [_vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_gemm_gateup_act": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp]),
+    "moe_gemm_gateup_act_rows": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _i, _vp,
+                                      _vp]),
     "moe_gemm_down": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
-    "moe_expert_mlp": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_expert_mlp": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
+                            _vp]),
     "gbmoe_expert_mlp_fused": (_i, [_i, _i, _i]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
     "gbmoe_forward_workspace_size": (_sz, [_P(Layer), _i]),

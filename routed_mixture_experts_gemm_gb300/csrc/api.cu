@@ -67,7 +67,7 @@ struct FwdWs {
     int32_t *ids_log, *ids_phys, *counts, *offsets, *row_to_token, *flat_to_row, *ready;
     float* weights;
     void* perm;
-    uint16_t *x_perm, *act, *act_s;
+    uint16_t *act, *act_s;
     float *y, *ys;
     size_t bytes;
 };
@@ -87,7 +87,6 @@ FwdWs layout_fwd(const gbmoe_layer* L, int T, void* ws) {
     f.row_to_token = w.take<int32_t>(N);
     f.flat_to_row = w.take<int32_t>(N);
     f.perm = w.take<char>(permute_ws_bytes(static_cast<int64_t>(N), c.E_phys));
-    f.x_perm = w.take<uint16_t>(N * L->H);
     f.act = w.take<uint16_t>(N * L->I);
     f.y = w.take<float>(N * L->H);
     f.act_s = w.take<uint16_t>(static_cast<size_t>(T) * L->I_shared);
@@ -271,8 +270,27 @@ int moe_gemm_gateup_act(const uint16_t* x_perm, const int32_t* offsets, int E_ph
         return GBMOE_ERR_INVALID_ARG;
     const DevCtx* ctx = device_ctx();
     if (!ctx) return GBMOE_ERR_CUDA;
-    return launch_gemm_gateup(x_perm, offsets, E_phys, N, H, I, w_gate, w_up, act, *ctx,
-                              reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm_gateup(x_perm, nullptr, 0, offsets, E_phys, N, H, I, w_gate, w_up, act,
+                              *ctx, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_gemm_gateup_act_rows(const uint16_t* x, const int32_t* row_to_token, int T,
+                             const int32_t* offsets, int E_phys, int N, int H, int I,
+                             const uint16_t* w_gate, const uint16_t* w_up, int activation,
+                             uint16_t* act, gbmoe_stream_t stream) {
+    if (activation != GBMOE_ACT_SWIGLU) return GBMOE_ERR_UNSUPPORTED;
+    if (N < 0 || T < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
+    if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
+    if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
+    if (H % 128 || I % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (N == 0) return GBMOE_OK;
+    if (T < 1 || !x || !row_to_token || !w_gate || !w_up || !act) return GBMOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(act))
+        return GBMOE_ERR_INVALID_ARG;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return launch_gemm_gateup(x, row_to_token, T, offsets, E_phys, N, H, I, w_gate, w_up, act,
+                              *ctx, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N, int H, int I,
@@ -294,25 +312,29 @@ int gbmoe_expert_mlp_fused(int E_phys, int N, int H) {
     return gemm_fused_eligible(E_phys, N, H) ? 1 : 0;
 }
 
-int moe_expert_mlp(const uint16_t* x_perm, const int32_t* offsets, int E_phys, int N, int H,
-                   int I, const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+int moe_expert_mlp(const uint16_t* x_rows, const int32_t* row_to_token, int T,
+                   const int32_t* offsets, int E_phys, int N, int H, int I,
+                   const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                    uint16_t* act, float* y, int32_t* ready, gbmoe_stream_t stream) {
     if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
     if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
     if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
     if (H % 128 || I % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (row_to_token && T < 1) return GBMOE_ERR_INVALID_ARG;
     if (N == 0) return GBMOE_OK;
-    if (!x_perm || !w_gate || !w_up || !w_down || !act || !y) return GBMOE_ERR_INVALID_ARG;
-    if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+    if (!x_rows || !w_gate || !w_up || !w_down || !act || !y) return GBMOE_ERR_INVALID_ARG;
+    if (!aligned16(x_rows) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
         !aligned16(act) || !aligned16(y))
         return GBMOE_ERR_INVALID_ARG;
     const DevCtx* ctx = device_ctx();
     if (!ctx) return GBMOE_ERR_CUDA;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int src_rows = row_to_token ? T : N;
     if (ready && gemm_fused_eligible(E_phys, N, H))
-        return launch_gemm_mlp_fused(x_perm, offsets, E_phys, N, H, I, w_gate, w_up, w_down, act,
-                                     y, ready, *ctx, s);
-    int st = launch_gemm_gateup(x_perm, offsets, E_phys, N, H, I, w_gate, w_up, act, *ctx, s);
+        return launch_gemm_mlp_fused(x_rows, row_to_token, src_rows, offsets, E_phys, N, H, I,
+                                     w_gate, w_up, w_down, act, y, ready, *ctx, s);
+    int st = launch_gemm_gateup(x_rows, row_to_token, src_rows, offsets, E_phys, N, H, I, w_gate,
+                                w_up, act, *ctx, s);
     if (st) return st;
     return launch_gemm_down(act, offsets, E_phys, N, H, I, w_down, y, *ctx, s);
 }
@@ -366,19 +388,21 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
                  nullptr};
     st = status_from(launch_route(ra, *ctx, s));
     if (st) return st;
-    // 2. dispatch: counts, offsets, stable permutation, x_perm ("Stage 4" AllGather row)
+    // 2. dispatch: counts, offsets, stable permutation ("Stage 4" AllGather
+    // row); the permuted rows are not materialised: the gate/up GEMM gathers
+    // them from x through row_to_token
     st = status_from(launch_permute(ip, N, c.top_k, c.E_phys, x, L->H, cn, f.offsets,
-                                    f.row_to_token, f.flat_to_row, f.x_perm, f.perm, *ctx, s));
+                                    f.row_to_token, f.flat_to_row, nullptr, f.perm, *ctx, s));
     if (st) return st;
     // 3-4. grouped gate/up + SwiGLU, grouped down ("Stage 4": unified_apply_mlp);
     // one fused launch for small groups
     if (gemm_fused_eligible(c.E_phys, N, L->H)) {
-        st = launch_gemm_mlp_fused(f.x_perm, f.offsets, c.E_phys, N, L->H, L->I, L->w_gate,
-                                   L->w_up, L->w_down, f.act, f.y, f.ready, *ctx, s);
+        st = launch_gemm_mlp_fused(x, f.row_to_token, T, f.offsets, c.E_phys, N, L->H, L->I,
+                                   L->w_gate, L->w_up, L->w_down, f.act, f.y, f.ready, *ctx, s);
         if (st) return st;
     } else {
-        st = launch_gemm_gateup(f.x_perm, f.offsets, c.E_phys, N, L->H, L->I, L->w_gate,
-                                L->w_up, f.act, *ctx, s);
+        st = launch_gemm_gateup(x, f.row_to_token, T, f.offsets, c.E_phys, N, L->H, L->I,
+                                L->w_gate, L->w_up, f.act, *ctx, s);
         if (st) return st;
         st = launch_gemm_down(f.act, f.offsets, c.E_phys, N, L->H, L->I, L->w_down, f.y, *ctx,
                               s);
@@ -387,8 +411,8 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
     // 5. shared expert over all tokens in order (one group)
     const float* ys = nullptr;
     if (L->I_shared) {
-        st = launch_gemm_gateup(x, nullptr, 1, T, L->H, L->I_shared, L->w_gate_shared,
-                                L->w_up_shared, f.act_s, *ctx, s);
+        st = launch_gemm_gateup(x, nullptr, 0, nullptr, 1, T, L->H, L->I_shared,
+                                L->w_gate_shared, L->w_up_shared, f.act_s, *ctx, s);
         if (st) return st;
         st = launch_gemm_down(f.act_s, nullptr, 1, T, L->H, L->I_shared, L->w_down_shared, f.ys,
                               *ctx, s);

@@ -18,21 +18,28 @@
 // sharing one token operand; y = acc kept in fp32 (only the activation is
 // rounded to bf16 inside the layer).
 //
-// One persistent CTA per SM; warp 0 issues TMA loads (128B-swizzled K-major
-// tiles), warp 1 issues tcgen05.mma and owns TMEM (2 accumulator buffers so
-// the epilogue of tile i overlaps the main loop of tile i+1, except for the
-// 256-token tiles whose accumulators fill TMEM), warps 2-9 (two per TMEM
-// lane quarter) drain TMEM with tcgen05.ld and write coalesced rows straight
-// from registers.  Tiles are ordered (expert, weight block, token block) so
-// CTAs working on the token blocks of one expert read the same weight tile at
-// the same time (one HBM read, L2 hits after).  The tile table is built on
-// the device from the group offsets: no host synchronisation.
+// One persistent CTA per SM with four roles: warp 0 streams the weight boxes
+// by TMA (128B-swizzled K-major tiles) through the A ring; warps 10-13 fill
+// the B ring with the token rows -- by TMA from a row-contiguous operand, or,
+// for the gate/up GEMM of the layer, gathered straight from the unpermuted
+// hidden states: row r of the tile is x[row_to_token[r]], copied in 16-byte
+// pieces (cp.async) into the same swizzled layout, so the permuted copy of x
+// is never written; warp 1 issues tcgen05.mma and owns TMEM (2 accumulator
+// buffers so the epilogue of tile i overlaps the main loop of tile i+1,
+// except for the 256-token tiles whose accumulators fill TMEM); warps 2-9
+// (two per TMEM lane quarter) drain TMEM with tcgen05.ld and write coalesced
+// rows straight from registers.  Tiles are ordered (expert, weight block,
+// token block) so CTAs working on the token blocks of one expert read the
+// same weight tile at the same time (one HBM read, L2 hits after).  The tile
+// table is built on the device from the group offsets: no host
+// synchronisation.
 //
 // Fused mode (small groups): one cooperative launch walks every gate/up tile
 // and then every down tile; a down tile of expert p waits (bounded) until all
 // of p's gate/up tiles have published their activations, so the down GEMM
 // fills the last wave of the gate/up GEMM instead of waiting for the launch
-// boundary.
+// boundary (its weights already stream while it waits: the A ring does not
+// depend on the activations).
 //
 // Every pipeline wait is bounded (wall-clock limit); a wait that gives up
 // raises an abort flag seen by all roles, records GBMOE_ERR_TIMEOUT, lets
@@ -56,8 +63,11 @@ constexpr int UMMA_K = 16;       // K per tcgen05.mma kind::f16
 constexpr int BOX_ROWS = 16;     // granularity of the token dimension (MMA N step, smallest box)
 constexpr int EPI_COLS = 16;     // tokens per epilogue pass (one tcgen05.ld x16)
 constexpr int EPI_WARPS = 8;     // two warps per TMEM lane quarter, alternating passes
+constexpr int LOADER_WARPS = 4;  // B ring
+constexpr int LOADER_THREADS = 32 * LOADER_WARPS;
+constexpr int LOADER_WARP0 = 2 + EPI_WARPS;
 constexpr int MAX_GROUPS = 1024;
-constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA/TMEM, rest epilogue
+constexpr int NUM_THREADS = 32 * (LOADER_WARP0 + LOADER_WARPS);
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
@@ -70,27 +80,31 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //   kFused:    kSwiGLU tiles, then kDownPair tiles, in one launch
 constexpr int kSwiGLU = 0, kDown = 1, kDownPair = 2, kFused = 3;
 
-template <int NUM_A, int BN, int STAGES, int ACC_BUFS, int BK>
+// Shared memory: a ring of SA weight stages (NUM_A boxes of 128 rows x BK)
+// and a ring of SB token stages (up to BN rows x BK).
+template <int NUM_A, int BN, int SA, int SB, int ACC_BUFS, int BK>
 struct Layout {
     static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int A_STAGE = NUM_A * A_BYTES;
     static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
     static constexpr int TMEM_COLS = ACC_BUFS * ACC_COLS;
     static constexpr int TABLE_INTS = MAX_GROUPS + 4;
-    static constexpr int OFF_TBS = STAGES * STAGE_BYTES;      // prefix of token blocks
+    static constexpr int OFF_B = SA * A_STAGE;
+    static constexpr int OFF_TBS = OFF_B + SB * B_BYTES;      // prefix of token blocks
     static constexpr int OFF_GSTART = OFF_TBS + TABLE_INTS * 4;
     static constexpr int OFF_GCNT = OFF_GSTART + TABLE_INTS * 4;
     static constexpr int OFF_SCAN = OFF_GCNT + TABLE_INTS * 4;
     static constexpr int OFF_BARS = OFF_SCAN + NUM_THREADS * 4 + 16;
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+    static constexpr int NUM_BARS = 2 * SA + 2 * SB + 4 + 1;
     static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
     static constexpr int END = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of 2");
-    static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte alignment");
+    static_assert(A_STAGE % 1024 == 0 && B_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(BK == 64 || BK == 32, "stage K is one 128- or 64-byte swizzled row");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(SA >= 2 && SB >= 2 && SA <= 16 && SB <= 16, "ring depth");
     static_assert(BN % BOX_ROWS == 0 && BN % (2 * EPI_COLS) == 0 && BN <= 256, "tile width");
 };
 
@@ -108,6 +122,11 @@ struct GemmArgs {
     int K;                   // reduction length
     void* out;               // [n_rows, R]: bf16 (gate/up + SwiGLU) or fp32 (down)
     int* status;
+    // Gathered token operand of the first GEMM (null: rows of the B maps):
+    // row r of the operand is gather_src[gather_rows[r]], gather_src [src_rows, K].
+    const int32_t* gather_rows;
+    const uint16_t* gather_src;
+    int src_rows;
 };
 
 // The second GEMM of the fused mode (paired down tiles) and the per-group
@@ -157,23 +176,27 @@ __device__ __forceinline__ Tile decode_tile(int tau, const int* tbs, const int* 
     return t;
 }
 
-// Barrier over the epilogue threads that also ANDs a flag across them, so
-// all epilogue warps take the same branch after a bounded wait.
-__device__ __forceinline__ bool epi_bar_all(bool v) {
+// Barrier over `NT` threads on named barrier `ID` that also ANDs a flag
+// across them, so that all take the same branch after a bounded wait.
+template <int ID, int NT>
+__device__ __forceinline__ bool bar_all(bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred pi, po;\n\t"
         "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.and.pred po, 1, %2, pi;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
         "selp.u32 %0, 1, 0, po;\n\t}"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "n"(32 * EPI_WARPS)
+        : "r"(static_cast<uint32_t>(v)), "n"(ID), "n"(NT)
         : "memory");
     return r != 0;
 }
+__device__ __forceinline__ bool epi_bar_all(bool v) { return bar_all<1, 32 * EPI_WARPS>(v); }
 __device__ __forceinline__ void epi_bar_sync() {
     asm volatile("bar.sync 2, %0;" ::"n"(32 * EPI_WARPS) : "memory");
 }
+__device__ __forceinline__ bool loader_bar_all(bool v) { return bar_all<3, LOADER_THREADS>(v); }
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -187,6 +210,25 @@ __device__ __forceinline__ void red_release_add_gpu(int* p, int v) {
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// Order this thread's completed generic-proxy shared-memory writes (cp.async)
+// before async-proxy reads of them (tcgen05.mma).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(src), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_one() {  // all but the newest group landed
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 // silu(g) * u = g * u / (1 + e^-g); the result is rounded to bf16, so the
 // fast exponential and division (a few ulp of fp32) are far below its ulp.
@@ -194,7 +236,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int NUM_A, int BN, int STAGES, int MODE, int ACC_BUFS, int BK>
+template <int NUM_A, int BN, int SA, int SB, int MODE, int ACC_BUFS, int BK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__ GemmMaps m2,
                     const GemmArgs args, const FusedArgs fz) {
@@ -202,7 +244,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     constexpr int MODE1 = FUSED ? kSwiGLU : MODE;  // mode of the first GEMM's tiles
     static_assert(MODE1 != kDown || NUM_A == 1, "down tiles have one A operand");
     static_assert(MODE1 == kDown || NUM_A == 2, "gate/up and paired tiles have two");
-    using L = Layout<NUM_A, BN, STAGES, ACC_BUFS, BK>;
+    using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -211,11 +253,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     int* gcnt = reinterpret_cast<int*>(smem + L::OFF_GCNT);
     int* scan = reinterpret_cast<int*>(smem + L::OFF_SCAN);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BARS);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* tfull = bars + 2 * STAGES;
-    uint64_t* tempty = bars + 2 * STAGES + 2;
-    uint64_t* drain = bars + 2 * STAGES + 4;
+    uint64_t* afull = bars;
+    uint64_t* aempty = afull + SA;
+    uint64_t* bfull = aempty + SA;
+    uint64_t* bempty = bfull + SB;
+    uint64_t* tfull = bempty + SB;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
 
@@ -227,9 +271,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 
     // ---- set-up: barriers, TMEM, tile table
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(afull + s, 1);
+            mbar_init(aempty + s, 1);
+        }
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(bfull + s, 1);
+            mbar_init(bempty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + b, 1);
@@ -307,9 +355,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 
     // ---------------------------------------------------------- roles
     if (warp == 0 && lane == 0) {
-        // TMA producer
+        // A producer: weight boxes by TMA
         const uint64_t pol_w = l2_policy_evict_first();
-        const uint64_t pol_x = l2_policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
         uint32_t armed = 0;          // bit s: stage s has been armed at least once
@@ -323,54 +370,23 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const int R = second ? fz.R : args.R;
             const int KB = (second ? fz.K : args.K) / BK;
             const int a_row = tl.p * R + tl.rblk * (mode == kDownPair ? 2 * BM : BM);
-            const int n_load = (tl.n_valid + BOX_ROWS - 1) / BOX_ROWS * BOX_ROWS;
-            const uint32_t bytes = NUM_A * L::A_BYTES + n_load * BK * 2;
-            if (FUSED && second) {
-                // all gate/up tiles of this group must have published their rows
-                const int need = rb1 * token_blocks(gcnt[tl.p], BN);
-                const uint64_t t0 = global_timer_ns();
-                bool ok = true;
-                for (uint32_t it = 0; ld_acquire_gpu(fz.ready + tl.p) < need; ++it) {
-                    if ((it & 63u) == 63u) {
-                        if (*abort_flag) { ok = false; break; }
-                        if (global_timer_ns() - t0 > kWaitLimitNs) {
-                            *abort_flag = 1;
-                            record_error(args.status, GBMOE_ERR_TIMEOUT);
-                            ok = false;
-                            break;
-                        }
-                    }
-                }
-                if (!ok) break;
-                fence_proxy_async_global();
-            }
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
-                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, args.status,
+                if (!mbar_wait_bounded(aempty + stage, phase ^ 1u, abort_flag, args.status,
                                        kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(full + stage, bytes);
-                uint8_t* sA = smem + stage * L::STAGE_BYTES;
-                tma_load_2d(sA, &m.a0, full + stage, kb * BK, a_row, pol_w);
+                mbar_arrive_expect_tx(afull + stage, NUM_A * L::A_BYTES);
+                uint8_t* sA = smem + stage * L::A_STAGE;
+                tma_load_2d(sA, &m.a0, afull + stage, kb * BK, a_row, pol_w);
                 if (mode == kSwiGLU)
-                    tma_load_2d(sA + L::A_BYTES, &m.a1, full + stage, kb * BK, a_row, pol_w);
+                    tma_load_2d(sA + L::A_BYTES, &m.a1, afull + stage, kb * BK, a_row, pol_w);
                 if (mode == kDownPair)
-                    tma_load_2d(sA + L::A_BYTES, &m.a0, full + stage, kb * BK, a_row + BM, pol_w);
-                // token rows in as few boxes as possible (128/64/32/16 rows)
-                uint8_t* sB = sA + NUM_A * L::A_BYTES;
-                for (int off = 0; off < n_load;) {
-                    const int rem = n_load - off;
-                    const int box = rem >= 128 ? 128 : rem >= 64 ? 64 : rem >= 32 ? 32 : 16;
-                    const CUtensorMap* mb = box == 128 ? &m.b128 : box == 64 ? &m.b64
-                                          : box == 32 ? &m.b32 : &m.b16;
-                    tma_load_2d(sB + off * BK * 2, mb, full + stage, kb * BK, tl.row0 + off, pol_x);
-                    off += box;
-                }
+                    tma_load_2d(sA + L::A_BYTES, &m.a0, afull + stage, kb * BK, a_row + BM, pol_w);
                 armed |= 1u << stage;
                 armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) {
+                if (++stage == SA) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -378,14 +394,161 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             if (!ok) break;
         }
         if (*abort_flag) {  // let every copy this thread issued land before exit
-            for (int s = 0; s < STAGES; ++s)
+            for (int s = 0; s < SA; ++s)
                 if ((armed >> s) & 1u)
-                    mbar_wait_timeout(full + s, (armed_phase >> s) & 1u, kDrainLimitNs);
+                    mbar_wait_timeout(afull + s, (armed_phase >> s) & 1u, kDrainLimitNs);
+        }
+    } else if (warp >= LOADER_WARP0) {
+        // B loaders: token rows, by TMA (lead thread) or gathered by cp.async
+        // (every loader thread copies one fixed 16-byte column of every 16th
+        // row of the tile).  A gathered stage is published once the next one
+        // has been issued (two stages in flight) and every loader's copies of
+        // it have landed: each thread waits for its own older copies and
+        // fences them for the tensor cores' proxy, and the barrier orders all
+        // of that before the lead thread's arrive.  A stage is published
+        // before the lead thread waits for the next free slot, which needs
+        // only stages SB or more behind: no cycle.
+        const int li = tid - 32 * LOADER_WARP0;
+        const bool lead = li == 0;
+        const int chunk = li & 7;       // 16-byte column of the 128-byte row
+        const int rbase = li >> 3;      // rows rbase + 16u
+        constexpr int RSTEP = LOADER_THREADS / 8;
+        constexpr int RPT = BN / RSTEP;  // rows per thread
+        static_assert(BN % RSTEP == 0, "loader rows");
+        const uint64_t pol_x = l2_policy_evict_last();
+        // without gathered rows the lead thread alone streams the B ring
+        const bool solo = args.gather_rows == nullptr;
+        auto all_agree = [&](bool v) { return solo ? v : loader_bar_all(v); };
+        int stage = 0;
+        uint32_t phase = 0;
+        int pend = -1;                  // gathered stage whose copies are not yet published
+        uint32_t armed = 0, armed_phase = 0;  // TMA-armed stages (lead thread)
+        bool ok = !solo || lead;
+        for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
+            bool second;
+            Tile tl;
+            job(tau, second, tl);
+            const bool gather = !second && !solo && BK == 64;
+            if (FUSED && second) {
+                // publish a pending gathered stage before waiting: the MMA
+                // needs it to finish the very gate/up tiles waited for
+                if (pend >= 0) {
+                    cp_async_wait_all();
+                    fence_proxy_async_shared();
+                    ok = loader_bar_all(true);
+                    if (lead) mbar_arrive(bfull + pend);
+                    pend = -1;
+                }
+                // all gate/up tiles of this group must have published their rows
+                bool got = true;
+                if (lead) {
+                    const int need = rb1 * token_blocks(gcnt[tl.p], BN);
+                    const uint64_t t0 = global_timer_ns();
+                    for (uint32_t it = 0; ld_acquire_gpu(fz.ready + tl.p) < need; ++it) {
+                        if ((it & 63u) == 63u) {
+                            if (*abort_flag) { got = false; break; }
+                            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                                *abort_flag = 1;
+                                record_error(args.status, GBMOE_ERR_TIMEOUT);
+                                got = false;
+                                break;
+                            }
+                        }
+                    }
+                    fence_proxy_async_global();
+                }
+                if (!all_agree(got)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const GemmMaps& m = second ? m2 : m1;
+            const int KB = (second ? fz.K : args.K) / BK;
+            const int n_load = (tl.n_valid + BOX_ROWS - 1) / BOX_ROWS * BOX_ROWS;
+            // gathered rows of this thread: source element offsets (-1: none)
+            int64_t src[RPT];
+            if (gather) {
+#pragma unroll
+                for (int u = 0; u < RPT; ++u) {
+                    const int r = rbase + RSTEP * u;
+                    src[u] = -1;
+                    if (r < tl.n_valid) {
+                        int t = args.gather_rows[tl.row0 + r];
+                        if (t < 0 || t >= args.src_rows) {
+                            record_error(args.status, GBMOE_ERR_DEVICE);
+                            t = 0;
+                        }
+                        src[u] = static_cast<int64_t>(t) * args.K + chunk * 8;
+                    }
+                }
+            }
+            for (int kb = 0; kb < KB; ++kb) {
+                bool free_ok = true;
+                if (lead)
+                    free_ok = mbar_wait_bounded(bempty + stage, phase ^ 1u, abort_flag,
+                                                args.status, kWaitLimitNs);
+                if (!all_agree(free_ok)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sB = smem + L::OFF_B + stage * L::B_BYTES;
+                if (gather) {
+                    const uint32_t sb = smem_u32(sB);
+#pragma unroll
+                    for (int u = 0; u < RPT; ++u) {
+                        if (src[u] >= 0) {
+                            const int r = rbase + RSTEP * u;
+                            const uint32_t dst = sb + r * 128 + ((chunk ^ (r & 7)) << 4);
+                            cp_async16(dst, args.gather_src + src[u] + kb * BK, pol_x);
+                        }
+                    }
+                    cp_async_commit();
+                    // publish the previous gathered stage: this thread's copies
+                    // of it have landed (only the newest group may be in flight)
+                    if (pend >= 0) {
+                        cp_async_wait_one();
+                        fence_proxy_async_shared();
+                        loader_bar_all(true);
+                        if (lead) mbar_arrive(bfull + pend);
+                    }
+                    pend = stage;
+                } else if (lead) {
+                    mbar_arrive_expect_tx(bfull + stage, n_load * BK * 2);
+                    // token rows in as few boxes as possible (128/64/32/16 rows)
+                    for (int off = 0; off < n_load;) {
+                        const int rem = n_load - off;
+                        const int box = rem >= 128 ? 128 : rem >= 64 ? 64 : rem >= 32 ? 32 : 16;
+                        const CUtensorMap* mb = box == 128 ? &m.b128 : box == 64 ? &m.b64
+                                              : box == 32 ? &m.b32 : &m.b16;
+                        tma_load_2d(sB + off * BK * 2, mb, bfull + stage, kb * BK, tl.row0 + off,
+                                    pol_x);
+                        off += box;
+                    }
+                    armed |= 1u << stage;
+                    armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+                }
+                if (++stage == SB) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (pend >= 0) {  // publish the last gathered stage
+            cp_async_wait_all();
+            fence_proxy_async_shared();
+            const bool all = loader_bar_all(ok);
+            if (lead && all) mbar_arrive(bfull + pend);
+        }
+        cp_async_wait_all();
+        if (lead && *abort_flag) {  // let every TMA copy issued land before exit
+            for (int s = 0; s < SB; ++s)
+                if ((armed >> s) & 1u)
+                    mbar_wait_timeout(bfull + s, (armed_phase >> s) & 1u, kDrainLimitNs);
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
-        int stage = 0, acc = 0;
-        uint32_t phase = 0, acc_phase = 0;
+        int as = 0, bs = 0, acc = 0;
+        uint32_t aph = 0, bph = 0, acc_phase = 0;
         bool issued = false;
         for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
             bool second;
@@ -401,14 +564,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const uint32_t d0 = tmem_base + acc * L::ACC_COLS;
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
-                if (!mbar_wait_bounded(full + stage, phase, abort_flag, args.status,
-                                       kWaitLimitNs)) {
+                if (!mbar_wait_bounded(afull + as, aph, abort_flag, args.status, kWaitLimitNs) ||
+                    !mbar_wait_bounded(bfull + bs, bph, abort_flag, args.status, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sA = smem_u32(smem + stage * L::STAGE_BYTES);
-                const uint32_t sB = sA + NUM_A * L::A_BYTES;
+                const uint32_t sA = smem_u32(smem + as * L::A_STAGE);
+                const uint32_t sB = smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
 #pragma unroll
                 for (int ks = 0; ks < BK / UMMA_K; ++ks) {
                     const uint64_t bdesc = smem_desc_kmajor<BK>(sB + ks * UMMA_K * 2);
@@ -420,10 +583,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     }
                 }
                 issued = true;
-                umma_commit(empty + stage);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                umma_commit(aempty + as);
+                umma_commit(bempty + bs);
+                if (++as == SA) {
+                    as = 0;
+                    aph ^= 1u;
+                }
+                if (++bs == SB) {
+                    bs = 0;
+                    bph ^= 1u;
                 }
             }
             if (!ok) break;
@@ -437,7 +605,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             umma_commit(drain);
             mbar_wait_timeout(drain, 0u, kDrainLimitNs);
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < LOADER_WARP0) {
         // epilogue: TMEM -> registers -> (activation) -> global.  Warp w may
         // only read TMEM lanes 32*(w%4)..+31; the two warps of each lane
         // quarter take alternate 16-token passes.
@@ -532,20 +700,25 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 // (32-wide stages with the 64B swizzle were measured slower: per-stage costs
 // outweigh the extra lookahead).  Below 96 rows per group with H % 256 == 0
 // moe_forward runs the two GEMMs fused in one launch (their tiles share one
-// layout).
+// layout).  Ring depths (weight stages, token stages) fill the shared memory.
 constexpr int kBK = 64;
 constexpr long kLargeGateUpRows = 96;
-using Gemm1Small = Layout<2, 128, 4, 2, kBK>;
-using Gemm1Large = Layout<2, 256, 3, 1, kBK>;
-using Gemm2Small = Layout<1, 128, 6, 2, kBK>;
-using Gemm2Large = Layout<1, 256, 4, 2, kBK>;
-using Gemm2Pair = Layout<2, 128, 4, 2, kBK>;
-#define GEMM1_SMALL grouped_gemm_kernel<2, 128, 4, kSwiGLU, 2, kBK>
-#define GEMM1_LARGE grouped_gemm_kernel<2, 256, 3, kSwiGLU, 1, kBK>
-#define GEMM2_SMALL grouped_gemm_kernel<1, 128, 6, kDown, 2, kBK>
-#define GEMM2_LARGE grouped_gemm_kernel<1, 256, 4, kDown, 2, kBK>
-#define GEMM2_PAIR grouped_gemm_kernel<2, 128, 4, kDownPair, 2, kBK>
-#define GEMM_FUSED grouped_gemm_kernel<2, 128, 4, kFused, 2, kBK>
+constexpr int kG1S_A = 4, kG1S_B = 4;
+constexpr int kG1L_A = 3, kG1L_B = 3;
+constexpr int kG2S_A = 6, kG2S_B = 6;
+constexpr int kG2L_A = 4, kG2L_B = 4;
+constexpr int kG2P_A = 4, kG2P_B = 4;
+using Gemm1Small = Layout<2, 128, kG1S_A, kG1S_B, 2, kBK>;
+using Gemm1Large = Layout<2, 256, kG1L_A, kG1L_B, 1, kBK>;
+using Gemm2Small = Layout<1, 128, kG2S_A, kG2S_B, 2, kBK>;
+using Gemm2Large = Layout<1, 256, kG2L_A, kG2L_B, 2, kBK>;
+using Gemm2Pair = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK>;
+#define GEMM1_SMALL grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kSwiGLU, 2, kBK>
+#define GEMM1_LARGE grouped_gemm_kernel<2, 256, kG1L_A, kG1L_B, kSwiGLU, 1, kBK>
+#define GEMM2_SMALL grouped_gemm_kernel<1, 128, kG2S_A, kG2S_B, kDown, 2, kBK>
+#define GEMM2_LARGE grouped_gemm_kernel<1, 256, kG2L_A, kG2L_B, kDown, 2, kBK>
+#define GEMM2_PAIR grouped_gemm_kernel<2, 128, kG2P_A, kG2P_B, kDownPair, 2, kBK>
+#define GEMM_FUSED grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kFused, 2, kBK>
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -625,15 +798,20 @@ bool gemm_fused_eligible(int groups, int n_rows, int H) {
     return n_rows > 0 && n_rows < kLargeGateUpRows * groups && H % 256 == 0;
 }
 
-int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* offsets, int groups, int n_rows,
-                       int H, int I, const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
+int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* row_to_token, int src_rows,
+                       const int32_t* offsets, int groups, int n_rows, int H, int I,
+                       const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
                        const DevCtx& ctx, cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
     GemmMaps m;
-    if (!make_gemm_maps(&m, w_gate, w_up, static_cast<uint64_t>(groups) * I, x_rows, n_rows, H))
+    // with gathered rows the token maps go unused; they are encoded over the
+    // source rows only to be valid
+    if (!make_gemm_maps(&m, w_gate, w_up, static_cast<uint64_t>(groups) * I, x_rows,
+                        row_to_token ? src_rows : n_rows, H))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
-    const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
+    const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
+                     row_to_token, row_to_token ? x_rows : nullptr, src_rows};
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
@@ -653,7 +831,7 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
     if (!make_gemm_maps(&m, w_down, nullptr, static_cast<uint64_t>(groups) * H, act, n_rows, I))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
-    const GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status};
+    const GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0};
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (H % 256 == 0) {
         const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
@@ -668,18 +846,21 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 
-int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* offsets, int groups, int n_rows,
-                          int H, int I, const uint16_t* w_gate, const uint16_t* w_up,
-                          const uint16_t* w_down, uint16_t* act, float* y, int* ready,
-                          const DevCtx& ctx, cudaStream_t s) {
+int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* row_to_token, int src_rows,
+                          const int32_t* offsets, int groups, int n_rows, int H, int I,
+                          const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                          uint16_t* act, float* y, int* ready, const DevCtx& ctx,
+                          cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
     GemmMaps m1, m2;
-    if (!make_gemm_maps(&m1, w_gate, w_up, static_cast<uint64_t>(groups) * I, x_rows, n_rows, H) ||
+    if (!make_gemm_maps(&m1, w_gate, w_up, static_cast<uint64_t>(groups) * I, x_rows,
+                        row_to_token ? src_rows : n_rows, H) ||
         !make_gemm_maps(&m2, w_down, nullptr, static_cast<uint64_t>(groups) * H, act, n_rows, I))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     if (cudaMemsetAsync(ready, 0, sizeof(int) * groups, s) != cudaSuccess) return GBMOE_ERR_CUDA;
-    const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status};
+    const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
+                     row_to_token, row_to_token ? x_rows : nullptr, src_rows};
     const FusedArgs f{H, I, y, ready};
     // every CTA must be resident (down tiles wait on gate/up tiles of other
     // CTAs): a cooperative launch of at most one CTA per SM

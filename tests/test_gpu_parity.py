@@ -412,7 +412,8 @@ MLP_SHAPES = [
 
 
 @pytest.mark.parametrize("shape,fused", MLP_SHAPES)
-def test_expert_mlp_fused_and_separate(built, shape, fused):
+@pytest.mark.parametrize("gather", [False, True])
+def test_expert_mlp_fused_and_separate(built, shape, fused, gather):
     gb = built
     H, I, rows = shape
     assert gb.expert_mlp_fused(len(rows), sum(rows), H) == fused
@@ -420,8 +421,19 @@ def test_expert_mlp_fused_and_separate(built, shape, fused):
     ready = torch.full((len(rows),), 12345, dtype=torch.int32, device=DEV)
     offs = _np(d["offs"])
     wd = _bf(d["wd"]).astype(np.float64)
+    src, r2t = d["x"], None
+    if gather:
+        # the same operand rows, gathered from a shuffled source with extra rows
+        N = d["x"].shape[0]
+        rng = np.random.default_rng(N + H)
+        T = N + 37
+        place = rng.permutation(T)[:N]
+        xs = torch.zeros((T, H), dtype=torch.bfloat16, device=DEV)
+        xs[torch.from_numpy(place).to(DEV)] = d["x"]
+        src, r2t = xs, torch.from_numpy(place.astype(np.int32)).to(DEV)
     for rd in (ready, None):
-        act, y = gb.moe_expert_mlp(d["x"], d["offs"], d["wg"], d["wu"], d["wd"], ready=rd)
+        act, y = gb.moe_expert_mlp(src, d["offs"], d["wg"], d["wu"], d["wd"], ready=rd,
+                                   row_to_token=r2t)
         assert gb.check_device_status() == 0
         assert_within_tol(_bf(act), synth.bf16_to_f32(act_o), f"act {shape}")
         # y is the down GEMM of the GPU's own activations (a one-ulp flip of a
