@@ -355,8 +355,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 
     // ---------------------------------------------------------- roles
     if (warp == 0 && lane == 0) {
-        // A producer: weight boxes by TMA
-        const uint64_t pol_w = l2_policy_evict_first();
+        // A producer: weight boxes by TMA.  A weight tile read by one CTA is
+        // streamed through L2 (evict first); one shared by several token
+        // blocks stays at normal priority until the other CTAs have read it.
+        const uint64_t pol_once = l2_policy_evict_first(), pol_shared = l2_policy_evict_normal();
         int stage = 0;
         uint32_t phase = 0;
         uint32_t armed = 0;          // bit s: stage s has been armed at least once
@@ -370,6 +372,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const int R = second ? fz.R : args.R;
             const int KB = (second ? fz.K : args.K) / BK;
             const int a_row = tl.p * R + tl.rblk * (mode == kDownPair ? 2 * BM : BM);
+            const uint64_t pol_w = token_blocks(gcnt[tl.p], BN) > 1 ? pol_shared : pol_once;
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait_bounded(aempty + stage, phase ^ 1u, abort_flag, args.status,
