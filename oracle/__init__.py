@@ -32,6 +32,12 @@ SOFTMAX, SIGMOID, SQRTSOFTPLUS = 0, 1, 2
 GROUP_MAX, GROUP_TOP2SUM = 0, 1
 _SCORING = {"softmax": SOFTMAX, "sigmoid": SIGMOID, "sqrtsoftplus": SQRTSOFTPLUS}
 _GROUP = {"max": GROUP_MAX, "top2sum": GROUP_TOP2SUM}
+# gated activations of the expert MLP (reading R15)
+ACTIVATIONS = {"swiglu": 0, "swiglu_oai": 1, "geglu": 2, "geglu_tanh": 3}
+
+
+def _act(a) -> int:
+    return ACTIVATIONS[a] if isinstance(a, str) else int(a)
 
 
 class RouteCfg(ctypes.Structure):
@@ -104,15 +110,17 @@ def _L():
             lib.oracle_expert_counts.restype = None
             lib.oracle_permute.argtypes = [vp, i, i, i, vp, vp, vp, vp]
             lib.oracle_permute.restype = None
-            lib.oracle_expert_ffn_rows.argtypes = [vp, i64, i, i, vp, vp, vp, vp, vp, i]
+            lib.orc_act_value.argtypes = [i, ctypes.c_double, ctypes.c_double]
+            lib.orc_act_value.restype = ctypes.c_double
+            lib.oracle_expert_ffn_rows.argtypes = [vp, i64, i, i, vp, vp, vp, i, vp, vp, i]
             lib.oracle_expert_ffn_rows.restype = None
-            lib.oracle_ffn_grouped.argtypes = [vp, vp, vp, i, i, i, vp, vp, vp, vp, vp, i]
+            lib.oracle_ffn_grouped.argtypes = [vp, vp, vp, i, i, i, vp, vp, vp, i, vp, vp, i]
             lib.oracle_ffn_grouped.restype = None
             lib.oracle_combine.argtypes = [vp, vp, vp, vp, i, i, i, vp]
             lib.oracle_combine.restype = None
             lib.oracle_moe_forward.argtypes = (
                 [ctypes.POINTER(RouteCfg), vp, i, i, i, vp, vp, vp, vp, vp, vp, i64, vp, vp, i,
-                 vp, vp, vp, i, vp, vp, vp] + [vp] * 12 + [i])
+                 vp, vp, vp, i, i, vp, vp, vp] + [vp] * 12 + [i])
             lib.oracle_moe_forward.restype = i
             _lib = lib
     return _lib
@@ -218,20 +226,25 @@ def permute(ids_phys, P):
 
 
 # --- expert MLP (Stage 4: grouped gate/up -> activation -> grouped down) ---
-def expert_ffn_rows(x_rows, wg, wu, wd, nthreads=None):
-    """act [n, I] (bf16 bits) and y [n, H] (fp32) of rows through one SwiGLU expert."""
+def act_value(activation, g, u) -> float:
+    """The gated activation of one (g, u) pair in double (reading R15)."""
+    return _L().orc_act_value(_act(activation), float(g), float(u))
+
+
+def expert_ffn_rows(x_rows, wg, wu, wd, nthreads=None, activation="swiglu"):
+    """act [n, I] (bf16 bits) and y [n, H] (fp32) of rows through one gated expert."""
     x_rows = _c(x_rows, np.uint16)
     n, H = x_rows.shape
     I = wg.shape[0]
     act = np.empty((n, I), dtype=np.uint16)
     y = np.empty((n, H), dtype=np.float32)
     _L().oracle_expert_ffn_rows(_p(x_rows), n, H, I, _p(_c(wg, np.uint16)), _p(_c(wu, np.uint16)),
-                                _p(_c(wd, np.uint16)), _p(act), _p(y),
+                                _p(_c(wd, np.uint16)), _act(activation), _p(act), _p(y),
                                 nthreads or default_threads())
     return act, y
 
 
-def ffn_grouped(x, row_to_token, offsets, wg, wu, wd, nthreads=None):
+def ffn_grouped(x, row_to_token, offsets, wg, wu, wd, nthreads=None, activation="swiglu"):
     x = _c(x, np.uint16)
     P, I, H = wg.shape
     N = int(offsets[P])
@@ -239,7 +252,8 @@ def ffn_grouped(x, row_to_token, offsets, wg, wu, wd, nthreads=None):
     y = np.empty((N, H), dtype=np.float32)
     _L().oracle_ffn_grouped(_p(x), _p(_c(row_to_token, np.int32)), _p(_c(offsets, np.int32)), P, H,
                             I, _p(_c(wg, np.uint16)), _p(_c(wu, np.uint16)),
-                            _p(_c(wd, np.uint16)), _p(act), _p(y), nthreads or default_threads())
+                            _p(_c(wd, np.uint16)), _act(activation), _p(act), _p(y),
+                            nthreads or default_threads())
     return act, y
 
 
@@ -258,7 +272,8 @@ def combine(y, flat_to_row, weights, ys=None):
 
 def moe_forward(cfg: RouteCfg, x, H, I, w_router=None, logits=None, router_bias=None,
                 corr_bias=None, input_ids=None, tid2eid=None, log2phy=None, replica_cnt=None,
-                wg=None, wu=None, wd=None, shared=None, nthreads=None) -> dict:
+                wg=None, wu=None, wd=None, shared=None, nthreads=None,
+                activation="swiglu") -> dict:
     """The whole layer, stage by stage; returns every intermediate."""
     x = _c(x, np.uint16)
     T = x.shape[0]
@@ -287,7 +302,8 @@ def moe_forward(cfg: RouteCfg, x, H, I, w_router=None, logits=None, router_bias=
         _p(_c(router_bias, np.float32)), _p(lg), _p(_c(corr_bias, np.float32)),
         _p(_c(input_ids, np.int32)), _p(tt), 0 if tt is None else tt.shape[0], _p(lp),
         _p(_c(replica_cnt, np.int32)), 1 if lp is None else lp.shape[1],
-        _p(_c(wg, np.uint16)), _p(_c(wu, np.uint16)), _p(_c(wd, np.uint16)), Is, _p(sg), _p(su),
+        _p(_c(wg, np.uint16)), _p(_c(wu, np.uint16)), _p(_c(wd, np.uint16)), _act(activation),
+        Is, _p(sg), _p(su),
         _p(sd), _p(o["ids_log"]), _p(o["ids_phys"]), _p(o["weights"]), _p(o["counts"]),
         _p(o["offsets"]), _p(o["row_to_token"]), _p(o["flat_to_row"]), _p(o["act"]), _p(o["y"]),
         _p(o.get("act_s")), _p(o.get("ys")), _p(o["out"]), nthreads or default_threads())
@@ -296,7 +312,7 @@ def moe_forward(cfg: RouteCfg, x, H, I, w_router=None, logits=None, router_bias=
     return o
 
 
-def run_config(mcfg, inputs=None, weights=None, nthreads=None) -> dict:
+def run_config(mcfg, inputs=None, weights=None, nthreads=None, activation="swiglu") -> dict:
     """Oracle forward of a synth.MoEConfig from its seeded inputs."""
     import synth
     d = inputs if inputs is not None else synth.make_inputs(mcfg)
@@ -307,4 +323,5 @@ def run_config(mcfg, inputs=None, weights=None, nthreads=None) -> dict:
                        router_bias=d["router_bias"], corr_bias=d["corr_bias"],
                        input_ids=d["input_ids"], tid2eid=d["tid2eid"], log2phy=pl.log2phy,
                        replica_cnt=pl.replica_cnt, wg=weights[0], wu=weights[1], wd=weights[2],
-                       shared=synth.shared_weights_host(mcfg), nthreads=nthreads)
+                       shared=synth.shared_weights_host(mcfg), nthreads=nthreads,
+                       activation=activation)

@@ -49,6 +49,8 @@
  *   R8 replica of logical e for token t: log2phy[e][t mod replica_cnt[e]].
  *   R9 permutation: stable counting sort of the flat index f = t*k + j by
  *      physical expert; row r = offsets[p] + rank of f among equal p.
+ *   R15 activation branches (named, not defined, by the page): SwiGLU,
+ *      clipped SwiGLU-OAI, GeGLU (erf), GeGLU (tanh); see orc_act_value.
  *   R10 rounding points: only the activation is rounded to bf16 inside the
  *      layer (it is the input of the down matmul): act = bf16(silu(g) * u)
  *      with g, u held in fp32; the expert outputs y = act . Wd and the shared
@@ -383,10 +385,36 @@ void oracle_permute(const int32_t* ids_phys, int T, int k, int P, int32_t* count
 }
 
 /* ----------------------------------------------------------- expert MLP */
-/* One row through one SwiGLU expert (R10).
+/* R15: the gated activations of the gate/up output ("Stage 4" activation
+ * branches; the pages name them, the formulas are the usual definitions):
+ *   0 SwiGLU:             silu(g) * u,  silu(g) = g / (1 + e^-g)
+ *   1 clipped SwiGLU-OAI: g' = min(g, 7), u' = clamp(u, -7, 7),
+ *                         g' * sigmoid(1.702 g') * (u' + 1)
+ *   2 GeGLU (erf):        0.5 g (1 + erf(g / sqrt 2)) * u
+ *   3 GeGLU (tanh):       0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) * u
+ * in double on the fp32 values of g and u. */
+double orc_act_value(int act, double g, double u) {
+    switch (act) {
+        case 1: {
+            const double gc = g < 7.0 ? g : 7.0;
+            const double uc = u < -7.0 ? -7.0 : (u > 7.0 ? 7.0 : u);
+            return gc / (1.0 + exp(-1.702 * gc)) * (uc + 1.0);
+        }
+        case 2:
+            return 0.5 * g * (1.0 + erf(g / sqrt(2.0))) * u;
+        case 3: {
+            const double c = sqrt(2.0 / 3.14159265358979323846);
+            return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g))) * u;
+        }
+        default:
+            return g / (1.0 + exp(-g)) * u;
+    }
+}
+
+/* One row through one gated expert MLP (R10, R15).
  * wg, wu: [I, H]; wd: [H, I]; act_out [I] as bf16 bits, y_out [H] fp32. */
 void orc_ffn_row(const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
-                 const uint16_t* wd, int H, int I, uint16_t* act_out, float* y_out) {
+                 const uint16_t* wd, int H, int I, int act, uint16_t* act_out, float* y_out) {
     for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         const uint16_t* rg = wg + (size_t)i * H;
@@ -397,8 +425,7 @@ void orc_ffn_row(const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
             u += xv * bf16_to_f32(ru[h]);
         }
         double gf = (float)g, uf = (float)u;
-        double silu = gf / (1.0 + exp(-gf));
-        act_out[i] = f32_to_bf16((float)(silu * uf));
+        act_out[i] = f32_to_bf16((float)orc_act_value(act, gf, uf));
     }
     for (int h = 0; h < H; ++h) {
         double acc = 0.0;
@@ -411,7 +438,7 @@ void orc_ffn_row(const uint16_t* x, const uint16_t* wg, const uint16_t* wu,
 typedef struct {
     const uint16_t *x, *wg, *wu, *wd;
     const int32_t *row_to_token, *row_expert;
-    int H, I;
+    int H, I, act_kind;
     uint16_t* act;
     float* y;
 } orc_ffn_ctx;
@@ -422,14 +449,14 @@ static void orc_ffn_task(void* c_, int64_t r) {
     int64_t p = c->row_expert ? c->row_expert[r] : 0;
     const size_t HI = (size_t)c->H * c->I;
     orc_ffn_row(c->x + (size_t)t * c->H, c->wg + p * HI, c->wu + p * HI, c->wd + p * HI, c->H,
-                c->I, c->act + (size_t)r * c->I, c->y + (size_t)r * c->H);
+                c->I, c->act_kind, c->act + (size_t)r * c->I, c->y + (size_t)r * c->H);
 }
 
 /* Rows of n inputs through one expert: act [n, I] bf16, y [n, H] fp32. */
 void oracle_expert_ffn_rows(const uint16_t* x, int64_t n, int H, int I, const uint16_t* wg,
-                            const uint16_t* wu, const uint16_t* wd, uint16_t* act,
+                            const uint16_t* wu, const uint16_t* wd, int act_kind, uint16_t* act,
                             float* y, int nthreads) {
-    orc_ffn_ctx c = {x, wg, wu, wd, NULL, NULL, H, I, act, y};
+    orc_ffn_ctx c = {x, wg, wu, wd, NULL, NULL, H, I, act_kind, act, y};
     orc_parallel_for(n, nthreads, orc_ffn_task, &c);
 }
 
@@ -438,12 +465,12 @@ void oracle_expert_ffn_rows(const uint16_t* x, int64_t n, int H, int I, const ui
  * wg/wu [P, I, H], wd [P, H, I]; act [N, I] bf16, y [N, H] fp32. */
 void oracle_ffn_grouped(const uint16_t* x, const int32_t* row_to_token, const int32_t* offsets,
                         int P, int H, int I, const uint16_t* wg, const uint16_t* wu,
-                        const uint16_t* wd, uint16_t* act, float* y, int nthreads) {
+                        const uint16_t* wd, int act_kind, uint16_t* act, float* y, int nthreads) {
     int64_t N = offsets[P];
     int32_t* row_expert = (int32_t*)malloc(sizeof(int32_t) * (N > 0 ? N : 1));
     for (int p = 0; p < P; ++p)
         for (int32_t r = offsets[p]; r < offsets[p + 1]; ++r) row_expert[r] = p;
-    orc_ffn_ctx c = {x, wg, wu, wd, row_to_token, row_expert, H, I, act, y};
+    orc_ffn_ctx c = {x, wg, wu, wd, row_to_token, row_expert, H, I, act_kind, act, y};
     orc_parallel_for(N, nthreads, orc_ffn_task, &c);
     free(row_expert);
 }
@@ -477,7 +504,7 @@ int oracle_moe_forward(const orc_route_cfg* c, const uint16_t* x, int T, int H, 
                        const float* corr_bias, const int32_t* input_ids,
                        const int32_t* tid2eid, int64_t V, const int32_t* log2phy,
                        const int32_t* replica_cnt, int R, const uint16_t* wg,
-                       const uint16_t* wu, const uint16_t* wd, int I_shared,
+                       const uint16_t* wu, const uint16_t* wd, int act_kind, int I_shared,
                        const uint16_t* wg_s, const uint16_t* wu_s, const uint16_t* wd_s,
                        int32_t* ids_log, int32_t* ids_phys, float* weights, int32_t* counts,
                        int32_t* offsets, int32_t* row_to_token, int32_t* flat_to_row,
@@ -488,10 +515,12 @@ int oracle_moe_forward(const orc_route_cfg* c, const uint16_t* x, int T, int H, 
                           R, ids_log, ids_phys, weights);
     if (rc) return rc;
     oracle_permute(ids_phys, T, c->k, c->P, counts, offsets, row_to_token, flat_to_row);
-    oracle_ffn_grouped(x, row_to_token, offsets, c->P, H, I, wg, wu, wd, act, y, nthreads);
+    oracle_ffn_grouped(x, row_to_token, offsets, c->P, H, I, wg, wu, wd, act_kind, act, y,
+                       nthreads);
     const float* ysp = NULL;
     if (wg_s) {
-        oracle_expert_ffn_rows(x, T, H, I_shared, wg_s, wu_s, wd_s, act_s, ys, nthreads);
+        oracle_expert_ffn_rows(x, T, H, I_shared, wg_s, wu_s, wd_s, act_kind, act_s, ys,
+                               nthreads);
         ysp = ys;
     }
     oracle_combine(y, flat_to_row, weights, ysp, T, c->k, H, out);
