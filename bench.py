@@ -250,7 +250,7 @@ class Workload:
         ev[2].record(self.stream)
         if self.fused:
             st |= L.moe_expert_mlp(p(c.x), p(self.r2t), T, p(self.offsets), P, N, H, I,
-                                   p(d["w_gate"]), p(d["w_up"]), p(d["w_down"]), p(self.act),
+                                   p(d["w_gate"]), p(d["w_up"]), p(d["w_down"]), 0, p(self.act),
                                    p(self.y), p(self.ready), s)
             ev[3].record(self.stream)
         else:

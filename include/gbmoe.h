@@ -53,8 +53,19 @@ enum gbmoe_status {
 enum { GBMOE_SCORE_SOFTMAX = 0, GBMOE_SCORE_SIGMOID = 1, GBMOE_SCORE_SQRTSOFTPLUS = 2 };
 /* group score used by grouped top-k */
 enum { GBMOE_GROUP_MAX = 0, GBMOE_GROUP_TOP2SUM = 1 };
-/* activation of the gate/up GEMM epilogue */
-enum { GBMOE_ACT_SWIGLU = 0 };
+/* Gated activation of the gate/up GEMM epilogue, act = f(g, u) on the fp32
+ * gate and up projections, rounded to bf16 ("Stage 4" activation branches):
+ *   GBMOE_ACT_SWIGLU       silu(g) * u, silu(g) = g / (1 + e^-g)
+ *   GBMOE_ACT_SWIGLU_OAI   clipped: g' = min(g, 7), u' = clamp(u, -7, 7),
+ *                          g' * sigmoid(1.702 g') * (u' + 1)
+ *   GBMOE_ACT_GEGLU        0.5 g (1 + erf(g / sqrt 2)) * u
+ *   GBMOE_ACT_GEGLU_TANH   0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) * u */
+enum {
+    GBMOE_ACT_SWIGLU = 0,
+    GBMOE_ACT_SWIGLU_OAI = 1,
+    GBMOE_ACT_GEGLU = 2,
+    GBMOE_ACT_GEGLU_TANH = 3
+};
 
 /*
  * Routing settings ("Runner Initialization": grouped top-k settings,
@@ -106,6 +117,7 @@ typedef struct gbmoe_layer {
     const uint16_t* w_gate_shared;/* [I_shared, H] bf16 or NULL */
     const uint16_t* w_up_shared;  /* [I_shared, H] bf16 or NULL */
     const uint16_t* w_down_shared;/* [H, I_shared] bf16 or NULL */
+    int activation;               /* GBMOE_ACT_*, of the routed and the shared experts */
 } gbmoe_layer;
 
 /* Text for a status code (static storage). */
@@ -216,10 +228,11 @@ int moe_permute_static(const int32_t* ids_phys, int T, int k, int E_phys, const 
 
 /*
  * moe_gemm_gateup_act — grouped gate/up GEMM with the activation fused into
- * its epilogue ("Stage 4": grouped matmul gate/up -> activation; SwiGLU).
+ * its epilogue ("Stage 4": grouped matmul gate/up -> activation).
  * For each expert p and each row r in [offsets[p], offsets[p+1]):
  *   g = x_perm[r] . w_gate[p]^T,  u = x_perm[r] . w_up[p]^T   (fp32 accumulate)
- *   act[r, i] = bf16(silu(g_i) * u_i),  silu(g) = g / (1 + e^-g)
+ *   act[r, i] = bf16(f(g_i, u_i)), f the GBMOE_ACT_* `activation`
+ *   (GBMOE_ERR_UNSUPPORTED for any other value)
  *   x_perm [N, H] bf16; offsets [E_phys + 1] int32 on the device, or NULL for a
  *   single group of N rows (E_phys must then be 1); w_gate, w_up [E_phys, I, H]
  *   bf16; act [N, I] bf16 out.  H, I multiples of 128; 16-byte aligned pointers.
@@ -264,7 +277,8 @@ int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N
  *     written by moe_permute), gathered inside the GEMM: no x_perm is needed.
  *     An entry outside [0, T) is read as row 0 and reported as
  *     GBMOE_ERR_DEVICE through the device status.
- *   offsets, w_gate, w_up, w_down, act, y as for the two calls above (act is
+ *   offsets, w_gate, w_up, w_down, activation, act, y as for the two calls
+ *   above (act is
  *   written and then read back: it must not alias the token operand or y);
  *   ready: [E_phys] int32 device scratch, overwritten.  When
  *   gbmoe_expert_mlp_fused(E_phys, N, H) is 1 and ready is non-NULL the two
@@ -276,7 +290,8 @@ int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N
 int moe_expert_mlp(const uint16_t* x_rows, const int32_t* row_to_token, int T,
                    const int32_t* offsets, int E_phys, int N, int H, int I,
                    const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
-                   uint16_t* act, float* y, int32_t* ready, gbmoe_stream_t stream);
+                   int activation, uint16_t* act, float* y, int32_t* ready,
+                   gbmoe_stream_t stream);
 
 /* 1 if moe_expert_mlp (and moe_forward) runs the two GEMMs as one launch for
  * this shape (groups averaging fewer than 96 rows, H a multiple of 256). */

@@ -18,7 +18,7 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
+from ._lib import ACTIVATION, ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
 
 __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_permute",
            "moe_gemm_gateup_act", "moe_gemm_gateup_act_rows", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
@@ -129,20 +129,28 @@ def moe_permute(ids_phys, E_phys: int, x=None, ws=None, stream=None) -> dict:
     return o
 
 
-def moe_gemm_gateup_act(x_perm, offsets, w_gate, w_up, act=None, stream=None):
-    """act = bf16(silu(x W_gate^T) * (x W_up^T)) per expert group; offsets None = one group."""
+def _act(activation) -> int:
+    return ACTIVATION[activation] if isinstance(activation, str) else int(activation)
+
+
+def moe_gemm_gateup_act(x_perm, offsets, w_gate, w_up, act=None, stream=None,
+                        activation="swiglu"):
+    """act = bf16(f(x W_gate^T, x W_up^T)) per expert group, f the gated
+    activation ("swiglu", "swiglu_oai", "geglu", "geglu_tanh"); offsets None =
+    one group."""
     lib = _lib.load()
     N, H = x_perm.shape
     P, I, _ = w_gate.shape
     if act is None:
         act = torch.empty((N, I), dtype=torch.bfloat16, device=x_perm.device)
     _check(lib.moe_gemm_gateup_act(_ptr(x_perm), _ptr(offsets), P, N, H, I, _ptr(w_gate),
-                                   _ptr(w_up), ACT_SWIGLU, _ptr(act), _stream(stream)),
+                                   _ptr(w_up), _act(activation), _ptr(act), _stream(stream)),
            "moe_gemm_gateup_act")
     return act
 
 
-def moe_gemm_gateup_act_rows(x, row_to_token, offsets, w_gate, w_up, act=None, stream=None):
+def moe_gemm_gateup_act_rows(x, row_to_token, offsets, w_gate, w_up, act=None, stream=None,
+                             activation="swiglu"):
     """moe_gemm_gateup_act with row r of the operand gathered as x[row_to_token[r]]."""
     lib = _lib.load()
     T, H = x.shape
@@ -151,7 +159,7 @@ def moe_gemm_gateup_act_rows(x, row_to_token, offsets, w_gate, w_up, act=None, s
     if act is None:
         act = torch.empty((N, I), dtype=torch.bfloat16, device=x.device)
     _check(lib.moe_gemm_gateup_act_rows(_ptr(x), _ptr(row_to_token), T, _ptr(offsets), P, N, H,
-                                        I, _ptr(w_gate), _ptr(w_up), ACT_SWIGLU, _ptr(act),
+                                        I, _ptr(w_gate), _ptr(w_up), _act(activation), _ptr(act),
                                         _stream(stream)), "moe_gemm_gateup_act_rows")
     return act
 
@@ -169,7 +177,7 @@ def moe_gemm_down(act, offsets, w_down, y=None, stream=None):
 
 
 def moe_expert_mlp(x_rows, offsets, w_gate, w_up, w_down, act=None, y=None, ready=None,
-                   row_to_token=None, stream=None):
+                   row_to_token=None, stream=None, activation="swiglu"):
     """Both grouped GEMMs (gate/up + SwiGLU, then down) as moe_forward runs them;
     returns (act, y).  x_rows is x_perm [N, H], or with row_to_token [N] the
     unpermuted x [T, H] whose rows the GEMM gathers.  `ready` ([E_phys] int32
@@ -186,8 +194,9 @@ def moe_expert_mlp(x_rows, offsets, w_gate, w_up, w_down, act=None, y=None, read
     if y is None:
         y = torch.empty((N, H), dtype=torch.float32, device=dev)
     _check(lib.moe_expert_mlp(_ptr(x_rows), _ptr(row_to_token), T, _ptr(offsets), P, N, H, I,
-                              _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(act), _ptr(y),
-                              _ptr(ready), _stream(stream)), "moe_expert_mlp")
+                              _ptr(w_gate), _ptr(w_up), _ptr(w_down), _act(activation),
+                              _ptr(act), _ptr(y), _ptr(ready), _stream(stream)),
+           "moe_expert_mlp")
     return act, y
 
 
@@ -219,7 +228,8 @@ class MoELayer:
     """
 
     def __init__(self, cfg: RouteCfg, w_router, w_gate, w_up, w_down, router_bias=None,
-                 corr_bias=None, tid2eid=None, log2phy=None, replica_cnt=None, shared=None):
+                 corr_bias=None, tid2eid=None, log2phy=None, replica_cnt=None, shared=None,
+                 activation="swiglu"):
         self.cfg = cfg
         self._keep = [w_router, w_gate, w_up, w_down, router_bias, corr_bias, tid2eid, log2phy,
                       replica_cnt] + list(shared or [])
@@ -232,7 +242,7 @@ class MoELayer:
                        _ptr(tid2eid), 0 if tid2eid is None else tid2eid.shape[0], _ptr(log2phy),
                        _ptr(replica_cnt), 1 if log2phy is None else log2phy.shape[1],
                        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s[0]), _ptr(s[1]),
-                       _ptr(s[2]))
+                       _ptr(s[2]), _act(activation))
         self._ws = None
 
     def workspace_size(self, T_max: int, host: bool = False) -> int:

@@ -13,6 +13,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: 
 SCORE = {"softmax": 0, "sigmoid": 1, "sqrtsoftplus": 2}
 GROUP = {"max": 0, "top2sum": 1}
 ACT_SWIGLU = 0
+ACTIVATION = {"swiglu": 0, "swiglu_oai": 1, "geglu": 2, "geglu_tanh": 3}
 
 # every function the header declares, with (restype, argtypes)
 _vp, _i, _i64, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -30,7 +31,7 @@ class Layer(ctypes.Structure):
                 ("tid2eid", _vp), ("tid2eid_rows", _i64), ("log2phy", _vp),
                 ("replica_cnt", _vp), ("R_max", _i), ("w_gate", _vp), ("w_up", _vp),
                 ("w_down", _vp), ("w_gate_shared", _vp), ("w_up_shared", _vp),
-                ("w_down_shared", _vp)]
+                ("w_down_shared", _vp), ("activation", _i)]
 
 
 _P = ctypes.POINTER
@@ -49,8 +50,8 @@ SIGNATURES = {
     "moe_gemm_gateup_act_rows": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _i, _vp,
                                       _vp]),
     "moe_gemm_down": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
-    "moe_expert_mlp": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
-                            _vp]),
+    "moe_expert_mlp": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp,
+                            _vp, _vp]),
     "gbmoe_expert_mlp_fused": (_i, [_i, _i, _i]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
     "gbmoe_forward_workspace_size": (_sz, [_P(Layer), _i]),

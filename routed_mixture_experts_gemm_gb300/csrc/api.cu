@@ -27,6 +27,8 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxGroups = 32;
 
+bool valid_activation(int a) { return a >= GBMOE_ACT_SWIGLU && a <= GBMOE_ACT_GEGLU_TANH; }
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
@@ -111,6 +113,7 @@ int check_layer(const gbmoe_layer* L) {
     if (!L->log2phy && c.E_phys != c.E_log) return GBMOE_ERR_INVALID_ARG;
     if (L->I_shared && (!L->w_gate_shared || !L->w_up_shared || !L->w_down_shared))
         return GBMOE_ERR_INVALID_ARG;
+    if (!valid_activation(L->activation)) return GBMOE_ERR_UNSUPPORTED;
     return GBMOE_OK;
 }
 
@@ -259,7 +262,7 @@ int moe_permute(const int32_t* ids_phys, int T, int k, int E_phys, const uint16_
 int moe_gemm_gateup_act(const uint16_t* x_perm, const int32_t* offsets, int E_phys, int N, int H,
                         int I, const uint16_t* w_gate, const uint16_t* w_up, int activation,
                         uint16_t* act, gbmoe_stream_t stream) {
-    if (activation != GBMOE_ACT_SWIGLU) return GBMOE_ERR_UNSUPPORTED;
+    if (!valid_activation(activation)) return GBMOE_ERR_UNSUPPORTED;
     if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
     if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
     if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
@@ -270,15 +273,15 @@ int moe_gemm_gateup_act(const uint16_t* x_perm, const int32_t* offsets, int E_ph
         return GBMOE_ERR_INVALID_ARG;
     const DevCtx* ctx = device_ctx();
     if (!ctx) return GBMOE_ERR_CUDA;
-    return launch_gemm_gateup(x_perm, nullptr, 0, offsets, E_phys, N, H, I, w_gate, w_up, act,
-                              *ctx, reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm_gateup(x_perm, nullptr, 0, offsets, E_phys, N, H, I, w_gate, w_up,
+                              activation, act, *ctx, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int moe_gemm_gateup_act_rows(const uint16_t* x, const int32_t* row_to_token, int T,
                              const int32_t* offsets, int E_phys, int N, int H, int I,
                              const uint16_t* w_gate, const uint16_t* w_up, int activation,
                              uint16_t* act, gbmoe_stream_t stream) {
-    if (activation != GBMOE_ACT_SWIGLU) return GBMOE_ERR_UNSUPPORTED;
+    if (!valid_activation(activation)) return GBMOE_ERR_UNSUPPORTED;
     if (N < 0 || T < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
     if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
     if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
@@ -289,8 +292,8 @@ int moe_gemm_gateup_act_rows(const uint16_t* x, const int32_t* row_to_token, int
         return GBMOE_ERR_INVALID_ARG;
     const DevCtx* ctx = device_ctx();
     if (!ctx) return GBMOE_ERR_CUDA;
-    return launch_gemm_gateup(x, row_to_token, T, offsets, E_phys, N, H, I, w_gate, w_up, act,
-                              *ctx, reinterpret_cast<cudaStream_t>(stream));
+    return launch_gemm_gateup(x, row_to_token, T, offsets, E_phys, N, H, I, w_gate, w_up,
+                              activation, act, *ctx, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int moe_gemm_down(const uint16_t* act, const int32_t* offsets, int E_phys, int N, int H, int I,
@@ -315,7 +318,9 @@ int gbmoe_expert_mlp_fused(int E_phys, int N, int H) {
 int moe_expert_mlp(const uint16_t* x_rows, const int32_t* row_to_token, int T,
                    const int32_t* offsets, int E_phys, int N, int H, int I,
                    const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
-                   uint16_t* act, float* y, int32_t* ready, gbmoe_stream_t stream) {
+                   int activation, uint16_t* act, float* y, int32_t* ready,
+                   gbmoe_stream_t stream) {
+    if (!valid_activation(activation)) return GBMOE_ERR_UNSUPPORTED;
     if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
     if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
     if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
@@ -332,9 +337,9 @@ int moe_expert_mlp(const uint16_t* x_rows, const int32_t* row_to_token, int T,
     const int src_rows = row_to_token ? T : N;
     if (ready && gemm_fused_eligible(E_phys, N, H))
         return launch_gemm_mlp_fused(x_rows, row_to_token, src_rows, offsets, E_phys, N, H, I,
-                                     w_gate, w_up, w_down, act, y, ready, *ctx, s);
+                                     w_gate, w_up, w_down, activation, act, y, ready, *ctx, s);
     int st = launch_gemm_gateup(x_rows, row_to_token, src_rows, offsets, E_phys, N, H, I, w_gate,
-                                w_up, act, *ctx, s);
+                                w_up, activation, act, *ctx, s);
     if (st) return st;
     return launch_gemm_down(act, offsets, E_phys, N, H, I, w_down, y, *ctx, s);
 }
@@ -398,11 +403,12 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
     // one fused launch for small groups
     if (gemm_fused_eligible(c.E_phys, N, L->H)) {
         st = launch_gemm_mlp_fused(x, f.row_to_token, T, f.offsets, c.E_phys, N, L->H, L->I,
-                                   L->w_gate, L->w_up, L->w_down, f.act, f.y, f.ready, *ctx, s);
+                                   L->w_gate, L->w_up, L->w_down, L->activation, f.act, f.y,
+                                   f.ready, *ctx, s);
         if (st) return st;
     } else {
         st = launch_gemm_gateup(x, f.row_to_token, T, f.offsets, c.E_phys, N, L->H, L->I,
-                                L->w_gate, L->w_up, f.act, *ctx, s);
+                                L->w_gate, L->w_up, L->activation, f.act, *ctx, s);
         if (st) return st;
         st = launch_gemm_down(f.act, f.offsets, c.E_phys, N, L->H, L->I, L->w_down, f.y, *ctx,
                               s);
@@ -412,7 +418,8 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
     const float* ys = nullptr;
     if (L->I_shared) {
         st = launch_gemm_gateup(x, nullptr, 0, nullptr, 1, T, L->H, L->I_shared,
-                                L->w_gate_shared, L->w_up_shared, f.act_s, *ctx, s);
+                                L->w_gate_shared, L->w_up_shared, L->activation, f.act_s, *ctx,
+                                s);
         if (st) return st;
         st = launch_gemm_down(f.act_s, nullptr, 1, T, L->H, L->I_shared, L->w_down_shared, f.ys,
                               *ctx, s);

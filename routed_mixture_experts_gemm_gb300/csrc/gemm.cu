@@ -127,6 +127,7 @@ struct GemmArgs {
     const int32_t* gather_rows;
     const uint16_t* gather_src;
     int src_rows;
+    int act;                 // gated activation of the gate/up epilogue (GBMOE_ACT_*)
 };
 
 // The second GEMM of the fused mode (paired down tiles) and the per-group
@@ -230,10 +231,29 @@ __device__ __forceinline__ void cp_async_wait_one() {  // all but the newest gro
     asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
-// silu(g) * u = g * u / (1 + e^-g); the result is rounded to bf16, so the
-// fast exponential and division (a few ulp of fp32) are far below its ulp.
+// The gated activations (the result is rounded to bf16, so the fast
+// exponential and division -- a few ulp of fp32 -- are far below its ulp):
+// silu(g) * u = g * u / (1 + e^-g); the clipped variant caps the gate at 7,
+// clamps the up projection to [-7, 7] and uses sigmoid(1.702 g) (u + 1);
+// GeGLU with erf, or with the tanh approximation of the normal CDF.
 __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+__device__ __forceinline__ float gated_act(int act, float g, float u) {
+    switch (act) {
+        case GBMOE_ACT_SWIGLU_OAI: {
+            const float gc = fminf(g, 7.0f);
+            const float uc = fminf(fmaxf(u, -7.0f), 7.0f);
+            return __fdividef(gc, 1.0f + __expf(-1.702f * gc)) * (uc + 1.0f);
+        }
+        case GBMOE_ACT_GEGLU:
+            return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f)) * u;
+        case GBMOE_ACT_GEGLU_TANH:
+            return 0.5f * g * (1.0f + tanhf(0.79788456080286536f * (g + 0.044715f * g * g * g))) *
+                   u;
+        default:
+            return silu_mul(g, u);
+    }
 }
 
 template <int NUM_A, int BN, int SA, int SB, int MODE, int ACC_BUFS, int BK>
@@ -644,8 +664,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     uint32_t u[16];
                     tmem_ld_32x32b_x16(tb + BN + c0, u);
                     tmem_ld_wait();
+                    if (args.act == GBMOE_ACT_SWIGLU) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) v[c] = silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c]));
+                        for (int c = 0; c < 16; ++c)
+                            v[c] = silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c]));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            v[c] = gated_act(args.act, __uint_as_float(g[c]), __uint_as_float(u[c]));
+                    }
                 } else {
                     tmem_ld_wait();
 #pragma unroll
@@ -803,8 +830,8 @@ bool gemm_fused_eligible(int groups, int n_rows, int H) {
 
 int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* row_to_token, int src_rows,
                        const int32_t* offsets, int groups, int n_rows, int H, int I,
-                       const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
-                       const DevCtx& ctx, cudaStream_t s) {
+                       const uint16_t* w_gate, const uint16_t* w_up, int activation,
+                       uint16_t* act, const DevCtx& ctx, cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
     GemmMaps m;
     // with gathered rows the token maps go unused; they are encoded over the
@@ -814,7 +841,7 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* row_to_token, int 
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
-                     row_to_token, row_to_token ? x_rows : nullptr, src_rows};
+                     row_to_token, row_to_token ? x_rows : nullptr, src_rows, activation};
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
@@ -834,7 +861,7 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
     if (!make_gemm_maps(&m, w_down, nullptr, static_cast<uint64_t>(groups) * H, act, n_rows, I))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
-    const GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0};
+    const GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (H % 256 == 0) {
         const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
@@ -852,8 +879,8 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
 int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* row_to_token, int src_rows,
                           const int32_t* offsets, int groups, int n_rows, int H, int I,
                           const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
-                          uint16_t* act, float* y, int* ready, const DevCtx& ctx,
-                          cudaStream_t s) {
+                          int activation, uint16_t* act, float* y, int* ready,
+                          const DevCtx& ctx, cudaStream_t s) {
     if (n_rows == 0) return GBMOE_OK;
     GemmMaps m1, m2;
     if (!make_gemm_maps(&m1, w_gate, w_up, static_cast<uint64_t>(groups) * I, x_rows,
@@ -863,7 +890,7 @@ int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* row_to_token, i
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     if (cudaMemsetAsync(ready, 0, sizeof(int) * groups, s) != cudaSuccess) return GBMOE_ERR_CUDA;
     const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
-                     row_to_token, row_to_token ? x_rows : nullptr, src_rows};
+                     row_to_token, row_to_token ? x_rows : nullptr, src_rows, activation};
     const FusedArgs f{H, I, y, ready};
     // every CTA must be resident (down tiles wait on gate/up tiles of other
     // CTAs): a cooperative launch of at most one CTA per SM

@@ -65,8 +65,8 @@ cudaError_t launch_permute(const int32_t* ids_phys, int64_t N, int k, int E_phys
 // rows [src_rows, H] that row r of the operand is gathered from.
 int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* row_to_token, int src_rows,
                        const int32_t* offsets, int groups, int n_rows, int H, int I,
-                       const uint16_t* w_gate, const uint16_t* w_up, uint16_t* act,
-                       const DevCtx& ctx, cudaStream_t s);
+                       const uint16_t* w_gate, const uint16_t* w_up, int activation,
+                       uint16_t* act, const DevCtx& ctx, cudaStream_t s);
 int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, int n_rows, int H,
                      int I, const uint16_t* w_down, float* y, const DevCtx& ctx,
                      cudaStream_t s);
@@ -78,8 +78,8 @@ bool gemm_fused_eligible(int groups, int n_rows, int H);
 int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* row_to_token, int src_rows,
                           const int32_t* offsets, int groups, int n_rows, int H, int I,
                           const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
-                          uint16_t* act, float* y, int* ready, const DevCtx& ctx,
-                          cudaStream_t s);
+                          int activation, uint16_t* act, float* y, int* ready,
+                          const DevCtx& ctx, cudaStream_t s);
 
 // --- combine (combine.cu) ---
 cudaError_t launch_combine(const float* y, const int32_t* flat_to_row, const float* weights,

@@ -38,7 +38,8 @@ def bf16_dev(bits, device):
     return _t(np.ascontiguousarray(bits, dtype=np.uint16), device, torch.bfloat16)
 
 
-def device_case(cfg: synth.MoEConfig, device, host_weights: Optional[bool] = None) -> Case:
+def device_case(cfg: synth.MoEConfig, device, host_weights: Optional[bool] = None,
+                activation: str = "swiglu") -> Case:
     import routed_mixture_experts_gemm_gb300 as gb
     d = synth.make_inputs(cfg)
     pl = d["placement"]
@@ -71,7 +72,8 @@ def device_case(cfg: synth.MoEConfig, device, host_weights: Optional[bool] = Non
                       use_hash=cfg.use_hash)
     layer = gb.MoELayer(rc, dev["w_router"], wg, wu, wd, router_bias=dev["router_bias"],
                         corr_bias=dev["corr_bias"], tid2eid=dev["tid2eid"],
-                        log2phy=dev["log2phy"], replica_cnt=dev["replica_cnt"], shared=shared)
+                        log2phy=dev["log2phy"], replica_cnt=dev["replica_cnt"], shared=shared,
+                        activation=activation)
     x = bf16_dev(d["x"], device)
     ids = _t(d["input_ids"], device)
     return Case(cfg, d, x, ids, layer, dev, wh)

@@ -248,6 +248,66 @@ def test_forward_end_to_end(built, name):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
+# the gated activation branches: each GEMM tile variant (128- and 256-token
+# gate/up tiles, contiguous and gathered operands) and the whole layer (fused
+# decode-sized and two-launch prefill-sized expert MLPs, shared expert)
+ACTS = ["swiglu_oai", "geglu", "geglu_tanh", "swiglu"]
+
+
+@pytest.mark.parametrize("act", ACTS)
+@pytest.mark.parametrize("rows", [[40, 3, 17, 0, 90], [150, 200, 300, 1, 0]])
+def test_gateup_activations(built, act, rows):
+    gb = built
+    H, I = 256, 256
+    rng = np.random.default_rng(len(rows) + sum(rows))
+    from tests.test_oracle_mlp import _bf16_bits
+    P = len(rows)
+    offs = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    N = int(offs[-1])
+    x = _bf16_bits(rng.standard_normal((N, H)))
+    # gate/up projections ~ N(0, 4^2): the clipped branch's caps at +-7 engage
+    wg = _bf16_bits(rng.standard_normal((P, I, H)) * 0.25)
+    wu = _bf16_bits(rng.standard_normal((P, I, H)) * 0.25)
+    wd = _bf16_bits(rng.standard_normal((P, H, I)) * 0.05)
+    act_o = np.zeros((N, I), np.uint16)
+    for p in range(P):
+        if rows[p]:
+            a, _ = oracle.expert_ffn_rows(x[offs[p]:offs[p + 1]], wg[p], wu[p], wd[p],
+                                          nthreads=4, activation=act)
+            act_o[offs[p]:offs[p + 1]] = a
+    d_offs = torch.from_numpy(offs).to(DEV)
+    dwg, dwu = bf16_dev(wg, DEV), bf16_dev(wu, DEV)
+    a1 = gb.moe_gemm_gateup_act(bf16_dev(x, DEV), d_offs, dwg, dwu, activation=act)
+    # gathered: the same rows from a reversed source
+    src = bf16_dev(x[::-1].copy(), DEV)
+    r2t = torch.arange(N - 1, -1, -1, dtype=torch.int32, device=DEV)
+    a2 = gb.moe_gemm_gateup_act_rows(src, r2t, d_offs, dwg, dwu, activation=act)
+    assert gb.check_device_status() == 0
+    ref = synth.bf16_to_f32(act_o)
+    assert_within_tol(_bf(a1), ref, f"act {act} {rows}")
+    assert_within_tol(_bf(a2), ref, f"act (gathered) {act} {rows}")
+
+
+@pytest.mark.parametrize("act", ["swiglu_oai", "geglu", "geglu_tanh"])
+@pytest.mark.parametrize("name", ["mini_decode", "mini_prefill", "mini_skew"])
+def test_forward_activations(built, act, name):
+    gb = built
+    cfg = synth.MINI[name]
+    case = device_case(cfg, DEV, host_weights=True, activation=act)
+    ref = oracle.run_config(cfg, inputs=case.inputs, weights=case.weights_host, activation=act)
+    out = gb.moe_forward(case.layer, case.x, input_ids=case.input_ids)
+    assert gb.check_device_status() == 0
+    assert_within_tol(_bf(out), synth.bf16_to_f32(ref["out"]), f"out {act} {name}")
+
+
+def test_unknown_activation_is_rejected(built):
+    gb = built
+    x = torch.zeros((16, 128), dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros((1, 128, 128), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(gb.GbmoeError):
+        gb.moe_gemm_gateup_act(x, None, w, w, activation=7)
+
+
 def test_forward_matches_golden_fixture(built):
     from tests.test_golden import load_tiny
     gb = built
