@@ -122,6 +122,10 @@ def _L():
                 [ctypes.POINTER(RouteCfg), vp, i, i, i, vp, vp, vp, vp, vp, vp, i64, vp, vp, i,
                  vp, vp, vp, i, i, vp, vp, vp] + [vp] * 12 + [i])
             lib.oracle_moe_forward.restype = i
+            lib.oracle_rmsnorm_row.argtypes = [vp, i, vp, f, vp]
+            lib.oracle_rmsnorm_row.restype = None
+            lib.oracle_latent_tail.argtypes = [vp, i, i, vp, f, vp, i, vp, vp, i]
+            lib.oracle_latent_tail.restype = None
             _lib = lib
     return _lib
 
@@ -325,3 +329,25 @@ def run_config(mcfg, inputs=None, weights=None, nthreads=None, activation="swigl
                        replica_cnt=pl.replica_cnt, wg=weights[0], wu=weights[1], wd=weights[2],
                        shared=synth.shared_weights_host(mcfg), nthreads=nthreads,
                        activation=activation)
+
+
+# --- latent MoE tail (LatentMoERunner page, tier 1 with one rank; reading R16) ---
+def rmsnorm_row(v_bits, w_bits, eps: float) -> np.ndarray:
+    """bf16 RMSNorm of one row in the pinned fp32 order (reading R16)."""
+    v = _c(v_bits, np.uint16)
+    z = np.empty_like(v)
+    _L().oracle_rmsnorm_row(_p(v), v.shape[0], _p(_c(w_bits, np.uint16)), float(eps), _p(z))
+    return z
+
+
+def latent_tail(latent, up_proj, norm_w=None, eps: float = 1e-6, shared=None,
+                nthreads=None) -> np.ndarray:
+    """out [T, Hm] = bf16(rmsnorm(latent) . up_proj^T + shared) (bf16 bits in and out)."""
+    latent = _c(latent, np.uint16)
+    up = _c(up_proj, np.uint16)
+    T, L = latent.shape
+    Hm = up.shape[0]
+    out = np.empty((T, Hm), dtype=np.uint16)
+    _L().oracle_latent_tail(_p(latent), T, L, _p(_c(norm_w, np.uint16)), float(eps), _p(up), Hm,
+                            _p(_c(shared, np.uint16)), _p(out), nthreads or default_threads())
+    return out

@@ -49,6 +49,8 @@
  *   R8 replica of logical e for token t: log2phy[e][t mod replica_cnt[e]].
  *   R9 permutation: stable counting sort of the flat index f = t*k + j by
  *      physical expert; row r = offsets[p] + rank of f among equal p.
+ *   R16 latent-MoE tail with one rank (NVIDIA LatentMoERunner page, tier 1):
+ *      out = bf16(rmsnorm(latent) . up_proj^T + shared); see oracle_latent_tail.
  *   R15 activation branches (named, not defined, by the page): SwiGLU,
  *      clipped SwiGLU-OAI, GeGLU (erf), GeGLU (tanh); see orc_act_value.
  *   R10 rounding points: only the activation is rounded to bf16 inside the
@@ -525,4 +527,66 @@ int oracle_moe_forward(const orc_route_cfg* c, const uint16_t* x, int T, int H, 
     }
     oracle_combine(y, flat_to_row, weights, ysp, T, c->k, H, out);
     return 0;
+}
+
+/* ------------------------------------------------------- latent MoE tail */
+/*
+ * R16: the post-MoE tail of a latent MoE on one GPU (the NVIDIA LatentMoERunner
+ * page, tier 1 "_overlap_allreduce_tail" with tensor parallelism 1, where the
+ * all-reduces are identities): out = bf16(norm(latent) . up_proj^T + shared).
+ * norm is the standard RMSNorm with weight w and epsilon eps, taken in fp32 in
+ * a pinned order and rounded to bf16 (the bf16 input of the up-projection):
+ *   s = sum over l of v_l^2 as 32 partial sums (partial j takes l = j, j+32,
+ *       ... ascending with fma) and the pairwise tree s = 16, 8, 4, 2, 1;
+ *   r = 1 / sqrt(s / L + eps)   (IEEE division and square root);
+ *   z_l = bf16((v_l * r) * w_l).
+ * Without a norm weight z = latent.  The up-projection accumulates in double;
+ * shared may be NULL.
+ */
+void oracle_rmsnorm_row(const uint16_t* v, int L, const uint16_t* w, float eps, uint16_t* z) {
+    float p[32];
+    for (int j = 0; j < 32; ++j) p[j] = 0.0f;
+    for (int l = 0; l < L; ++l) {
+        const float x = bf16_to_f32(v[l]);
+        p[l & 31] = fmaf(x, x, p[l & 31]);
+    }
+    for (int s = 16; s >= 1; s >>= 1)
+        for (int i = 0; i < s; ++i) p[i] = p[i] + p[i + s];
+    const float r = 1.0f / sqrtf(p[0] / (float)L + eps);
+    for (int l = 0; l < L; ++l) z[l] = f32_to_bf16((bf16_to_f32(v[l]) * r) * bf16_to_f32(w[l]));
+}
+
+typedef struct {
+    const uint16_t *latent, *w, *up, *shared;
+    int L, Hm;
+    float eps;
+    uint16_t* out;
+} orc_tail_ctx;
+
+static void orc_tail_task(void* c_, int64_t t) {
+    orc_tail_ctx* c = (orc_tail_ctx*)c_;
+    const uint16_t* v = c->latent + (size_t)t * c->L;
+    uint16_t* z = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)c->L);
+    if (!z) return;
+    if (c->w)
+        oracle_rmsnorm_row(v, c->L, c->w, c->eps, z);
+    else
+        memcpy(z, v, sizeof(uint16_t) * (size_t)c->L);
+    for (int h = 0; h < c->Hm; ++h) {
+        double acc = 0.0;
+        const uint16_t* u = c->up + (size_t)h * c->L;
+        for (int l = 0; l < c->L; ++l) acc += (double)bf16_to_f32(z[l]) * bf16_to_f32(u[l]);
+        const float yf = (float)acc;
+        const float sh = c->shared ? bf16_to_f32(c->shared[(size_t)t * c->Hm + h]) : 0.0f;
+        c->out[(size_t)t * c->Hm + h] = f32_to_bf16(yf + sh);
+    }
+    free(z);
+}
+
+/* latent [T, L], w [L] or NULL, up [Hm, L], shared [T, Hm] or NULL -> out [T, Hm]. */
+void oracle_latent_tail(const uint16_t* latent, int T, int L, const uint16_t* w, float eps,
+                        const uint16_t* up, int Hm, const uint16_t* shared, uint16_t* out,
+                        int nthreads) {
+    orc_tail_ctx c = {latent, w, up, shared, L, Hm, eps, out};
+    orc_parallel_for(T, nthreads, orc_tail_task, &c);
 }
