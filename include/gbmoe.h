@@ -310,6 +310,27 @@ int moe_combine(const float* y, const int32_t* flat_to_row, const float* weights
                 const float* shared_y, int T, int k, int H, uint16_t* out,
                 gbmoe_stream_t stream);
 
+/*
+ * moe_latent_tail — the post-MoE tail of a latent MoE on one GPU (the NVIDIA
+ * LatentMoERunner page, tier-1 tail "_overlap_allreduce_tail": reduce the
+ * routed latent output, RMSNorm, up-project to the hidden size with the
+ * replicated weight, add the shared-expert output; with one rank the
+ * reductions are identities):
+ *   z[t] = bf16(rmsnorm(latent[t]))  (fp32: r = 1/sqrt(sum_l v_l^2 / L + eps),
+ *          z_l = bf16((v_l * r) * norm_w[l]); norm_w NULL: z = latent)
+ *   out[t, h] = bf16(sum_l z[t, l] * up_proj[h, l] + shared[t, h])  (fp32 accumulate)
+ *   latent [T, L] bf16; norm_w [L] bf16 or NULL; eps >= 0; up_proj [Hm, L]
+ *   bf16 (row h = output channel); shared [T, Hm] bf16 or NULL; out [T, Hm]
+ *   bf16.  L and Hm multiples of 128 (else GBMOE_ERR_UNSUPPORTED); 16-byte
+ *   aligned pointers.  ws: device scratch of
+ *   gbmoe_latent_tail_workspace_size(T, L, Hm) bytes (GBMOE_ERR_WORKSPACE if
+ *   smaller).
+ */
+size_t gbmoe_latent_tail_workspace_size(int T, int L, int Hm);
+int moe_latent_tail(const uint16_t* latent, int T, int L, const uint16_t* norm_w, float eps,
+                    const uint16_t* up_proj, int Hm, const uint16_t* shared, uint16_t* out,
+                    void* ws, size_t ws_bytes, gbmoe_stream_t stream);
+
 /* Scratch bytes moe_forward needs for any T <= T_max (sized from capacity,
  * not from the runtime token count). */
 size_t gbmoe_forward_workspace_size(const gbmoe_layer* L, int T_max);

@@ -22,7 +22,7 @@ from ._lib import ACTIVATION, ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
 
 __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_permute",
            "moe_gemm_gateup_act", "moe_gemm_gateup_act_rows", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
-           "moe_combine", "MoELayer", "moe_forward",
+           "moe_combine", "moe_latent_tail", "MoELayer", "moe_forward",
            "moe_forward_host", "check_device_status", "library"]
 
 
@@ -214,6 +214,25 @@ def moe_combine(y, flat_to_row, weights, shared_y=None, out=None, stream=None):
         out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
     _check(lib.moe_combine(_ptr(y), _ptr(flat_to_row), _ptr(weights), _ptr(shared_y), T, k, H,
                            _ptr(out), _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_latent_tail(latent, up_proj, norm_w=None, eps=1e-6, shared=None, out=None, ws=None,
+                    stream=None):
+    """out = bf16(rmsnorm(latent) . up_proj^T + shared): the latent-MoE tail on
+    one GPU.  latent [T, L], up_proj [Hm, L], norm_w [L] or None, shared
+    [T, Hm] or None (bf16 device tensors)."""
+    lib = _lib.load()
+    T, L = latent.shape
+    Hm = up_proj.shape[0]
+    if out is None:
+        out = torch.empty((T, Hm), dtype=torch.bfloat16, device=latent.device)
+    need = lib.gbmoe_latent_tail_workspace_size(T, L, Hm)
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=latent.device)
+    _check(lib.moe_latent_tail(_ptr(latent), T, L, _ptr(norm_w), float(eps), _ptr(up_proj), Hm,
+                               _ptr(shared), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_latent_tail")
     return out
 
 

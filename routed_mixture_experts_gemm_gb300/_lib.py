@@ -54,6 +54,9 @@ SIGNATURES = {
                             _vp, _vp]),
     "gbmoe_expert_mlp_fused": (_i, [_i, _i, _i]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "gbmoe_latent_tail_workspace_size": (_sz, [_i, _i, _i]),
+    "moe_latent_tail": (_i, [_vp, _i, _i, _vp, ctypes.c_float, _vp, _i, _vp, _vp, _vp, _sz,
+                             _vp]),
     "gbmoe_forward_workspace_size": (_sz, [_P(Layer), _i]),
     "moe_forward": (_i, [_P(Layer), _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "gbmoe_forward_host_workspace_size": (_sz, [_P(Layer), _i]),

@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libgbmoe.so")
-SOURCES = ["api.cu", "route.cu", "permute.cu", "permute_static.cu", "gemm.cu", "combine.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "permute_static.cu", "gemm.cu", "combine.cu",
+           "tail.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

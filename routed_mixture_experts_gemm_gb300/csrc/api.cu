@@ -358,6 +358,29 @@ int moe_combine(const float* y, const int32_t* flat_to_row, const float* weights
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t gbmoe_latent_tail_workspace_size(int T, int L, int Hm) {
+    if (T < 0 || L <= 0 || Hm <= 0) return 0;
+    return latent_tail_ws_bytes(T, L, Hm);
+}
+
+int moe_latent_tail(const uint16_t* latent, int T, int L, const uint16_t* norm_w, float eps,
+                    const uint16_t* up_proj, int Hm, const uint16_t* shared, uint16_t* out,
+                    void* ws, size_t ws_bytes, gbmoe_stream_t stream) {
+    if (T < 0 || L <= 0 || Hm <= 0) return GBMOE_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps > 1e30f) return GBMOE_ERR_INVALID_ARG;
+    if (L % 128 || Hm % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (T == 0) return GBMOE_OK;
+    if (!latent || !up_proj || !out || !ws) return GBMOE_ERR_INVALID_ARG;
+    if (!aligned16(latent) || !aligned16(up_proj) || !aligned16(out) || !aligned16(ws) ||
+        (shared && !aligned16(shared)))
+        return GBMOE_ERR_INVALID_ARG;
+    if (ws_bytes < latent_tail_ws_bytes(T, L, Hm)) return GBMOE_ERR_WORKSPACE;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return launch_latent_tail(latent, T, L, norm_w, eps, up_proj, Hm, shared, out, ws, *ctx,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t gbmoe_forward_workspace_size(const gbmoe_layer* L, int T_max) {
     if (check_layer(L) || T_max < 0) return 0;
     return layout_fwd(L, T_max, nullptr).bytes;

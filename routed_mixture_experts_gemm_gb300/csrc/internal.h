@@ -81,6 +81,12 @@ int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* row_to_token, i
                           int activation, uint16_t* act, float* y, int* ready,
                           const DevCtx& ctx, cudaStream_t s);
 
+// --- latent-MoE tail (tail.cu) ---
+size_t latent_tail_ws_bytes(int T, int L, int Hm);
+int launch_latent_tail(const uint16_t* latent, int T, int L, const uint16_t* norm_w, float eps,
+                       const uint16_t* up_proj, int Hm, const uint16_t* shared, uint16_t* out,
+                       void* ws, const DevCtx& ctx, cudaStream_t s);
+
 // --- combine (combine.cu) ---
 cudaError_t launch_combine(const float* y, const int32_t* flat_to_row, const float* weights,
                            const float* shared_y, int T, int k, int H, uint16_t* out,
