@@ -122,6 +122,15 @@ def _L():
                 [ctypes.POINTER(RouteCfg), vp, i, i, i, vp, vp, vp, vp, vp, vp, i64, vp, vp, i,
                  vp, vp, vp, i, i, vp, vp, vp] + [vp] * 12 + [i])
             lib.oracle_moe_forward.restype = i
+            lib.orc_f32_to_e4m3.argtypes = [f]
+            lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
+            lib.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_to_f32.restype = f
+            lib.oracle_quantize_rows.argtypes = [vp, i64, i, vp, vp]
+            lib.oracle_quantize_rows.restype = None
+            lib.oracle_ffn_grouped_fp8.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp,
+                                                   vp, i, vp, vp, i]
+            lib.oracle_ffn_grouped_fp8.restype = None
             lib.oracle_rmsnorm_row.argtypes = [vp, i, vp, f, vp]
             lib.oracle_rmsnorm_row.restype = None
             lib.oracle_latent_tail.argtypes = [vp, i, i, vp, f, vp, i, vp, vp, i]
@@ -351,3 +360,40 @@ def latent_tail(latent, up_proj, norm_w=None, eps: float = 1e-6, shared=None,
     _L().oracle_latent_tail(_p(latent), T, L, _p(_c(norm_w, np.uint16)), float(eps), _p(up), Hm,
                             _p(_c(shared, np.uint16)), _p(out), nthreads or default_threads())
     return out
+
+
+# --- FP8 experts (Stage 4 quantized paths, W8A8FP; reading R17) ---
+def f32_to_e4m3(x: float) -> int:
+    """OCP FP8 E4M3 code of an fp32 value: round to nearest even, saturate to +-448."""
+    return int(_L().orc_f32_to_e4m3(float(x)))
+
+
+def e4m3_to_f32(code: int) -> float:
+    return float(_L().orc_e4m3_to_f32(int(code)))
+
+
+def quantize_rows(x_bits):
+    """bf16 rows [n, K] -> (E4M3 codes uint8 [n, K], fp32 scales [n]), s = amax / 448."""
+    x = _c(x_bits, np.uint16)
+    n, K = x.shape
+    q = np.empty((n, K), dtype=np.uint8)
+    sc = np.empty(n, dtype=np.float32)
+    _L().oracle_quantize_rows(_p(x), n, K, _p(q), _p(sc))
+    return q, sc
+
+
+def ffn_grouped_fp8(xq, sx, row_to_token, offsets, wg, sg, wu, su, wd, sd, nthreads=None,
+                    activation="swiglu"):
+    """FP8 grouped expert MLP: act [N, I] bf16 bits, y [N, H] fp32 (reading R17)."""
+    xq = _c(xq, np.uint8)
+    P, I, H = wg.shape
+    N = int(offsets[P])
+    act = np.empty((N, I), dtype=np.uint16)
+    y = np.empty((N, H), dtype=np.float32)
+    _L().oracle_ffn_grouped_fp8(_p(xq), _p(_c(sx, np.float32)), _p(_c(row_to_token, np.int32)),
+                                _p(_c(offsets, np.int32)), P, H, I, _p(_c(wg, np.uint8)),
+                                _p(_c(sg, np.float32)), _p(_c(wu, np.uint8)),
+                                _p(_c(su, np.float32)), _p(_c(wd, np.uint8)),
+                                _p(_c(sd, np.float32)), _act(activation), _p(act), _p(y),
+                                nthreads or default_threads())
+    return act, y

@@ -49,6 +49,9 @@
  *   R8 replica of logical e for token t: log2phy[e][t mod replica_cnt[e]].
  *   R9 permutation: stable counting sort of the flat index f = t*k + j by
  *      physical expert; row r = offsets[p] + rank of f among equal p.
+ *   R17 FP8 experts (W8A8FP): OCP E4M3 codes with one fp32 scale per row
+ *      (weights per output channel, activations per token / routed row); see
+ *      orc_f32_to_e4m3 and orc_ffn_row_fp8.
  *   R16 latent-MoE tail with one rank (NVIDIA LatentMoERunner page, tier 1):
  *      out = bf16(rmsnorm(latent) . up_proj^T + shared); see oracle_latent_tail.
  *   R15 activation branches (named, not defined, by the page): SwiGLU,
@@ -589,4 +592,149 @@ void oracle_latent_tail(const uint16_t* latent, int T, int L, const uint16_t* w,
                         int nthreads) {
     orc_tail_ctx c = {latent, w, up, shared, L, Hm, eps, out};
     orc_parallel_for(T, nthreads, orc_tail_task, &c);
+}
+
+/* ------------------------------------------------------------ FP8 experts */
+/*
+ * R17: FP8 experts ("Stage 4": quantized paths include W8A8FP; the page gives
+ * no scale layout).  OCP FP8 E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa
+ * bits, no infinities, largest finite 448, subnormals down to 2^-9.  A row is
+ * quantized with one fp32 scale s = amax / 448 (s = 1 for an all-zero row):
+ * q = e4m3(x / s) with IEEE division, round to nearest even and saturation
+ * to +-448.  Weights: one scale per output channel (row); activations: one
+ * scale per token / routed row, computed when they are produced.
+ */
+static double orc_ldexp(double m, int e) { return ldexp(m, e); }
+
+/* fp32 -> E4M3 code, round to nearest even, saturating to +-448 (NaN -> 0x7f). */
+uint8_t orc_f32_to_e4m3(float xf) {
+    const double x = (double)xf;
+    if (x != x) return 0x7f;
+    const uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7e);      /* saturate: 1.75 * 2^8 */
+    /* the representable magnitudes: subnormal k * 2^-9 (k < 8), normal
+     * (8 + m) * 2^(e-10) for e = 1..15, m = 0..7; round a to the nearest
+     * multiple of the spacing of its binade, ties to even */
+    int e;
+    frexp(a, &e);                                          /* a = f * 2^e, 0.5 <= f < 1 */
+    int be = e - 1 + 7;                                    /* biased exponent of a */
+    if (be < 1) be = 1;                                    /* subnormal binade: spacing 2^-9 */
+    const double spacing = orc_ldexp(1.0, be - 7 - 3);
+    double k = a / spacing;                                /* exact (power-of-two division) */
+    double kr = floor(k);
+    const double rem = k - kr;
+    if (rem > 0.5 || (rem == 0.5 && fmod(kr, 2.0) == 1.0)) kr += 1.0;
+    /* kr * spacing is the rounded magnitude; re-encode (may carry into the next binade) */
+    const double r = kr * spacing;
+    if (r >= 448.0) return (uint8_t)(sign | 0x7e);
+    if (r == 0.0) return sign;
+    int e2;
+    frexp(r, &e2);
+    int bexp = e2 - 1 + 7;
+    if (bexp < 1) {                                        /* subnormal: r = mant * 2^-9 */
+        const int mant = (int)(r / orc_ldexp(1.0, -9));
+        return (uint8_t)(sign | mant);
+    }
+    const int mant = (int)(r / orc_ldexp(1.0, bexp - 7 - 3)) - 8;
+    return (uint8_t)(sign | (bexp << 3) | mant);
+}
+
+/* E4M3 code -> value (exact in fp32). */
+float orc_e4m3_to_f32(uint8_t c) {
+    const int s = c >> 7, be = (c >> 3) & 15, m = c & 7;
+    if (be == 15 && m == 7) return NAN;
+    const double v = be == 0 ? m * orc_ldexp(1.0, -9) : (8 + m) * orc_ldexp(1.0, be - 10);
+    return (float)(s ? -v : v);
+}
+
+/* One row of n values (bf16 bits, or fp32 when xf != NULL) -> codes + scale. */
+float oracle_quantize_row(const uint16_t* xb, const float* xf, int n, uint8_t* q) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        const float v = fabsf(xf ? xf[i] : bf16_to_f32(xb[i]));
+        if (v > amax) amax = v;
+    }
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int i = 0; i < n; ++i) q[i] = orc_f32_to_e4m3((xf ? xf[i] : bf16_to_f32(xb[i])) / s);
+    return s;
+}
+
+/* rows [n, K] bf16 -> codes [n, K] + scales [n] */
+void oracle_quantize_rows(const uint16_t* x, int64_t n, int K, uint8_t* q, float* s) {
+    for (int64_t r = 0; r < n; ++r) s[r] = oracle_quantize_row(x + r * K, NULL, K, q + r * K);
+}
+
+/*
+ * One routed row through one FP8 expert: xq [H] codes with scale sx; wgq, wuq
+ * [I, H] codes with per-row scales sg, su [I]; wdq [H, I] codes with sd [H].
+ * g = (sum q_x q_g) sx sg, u likewise (double), act = bf16(f(g, u)) (R15);
+ * act is quantized per row (aq, sa) and y = (sum q_a q_d) sa sd in fp32.
+ */
+void orc_ffn_row_fp8(const uint8_t* xq, float sx, const uint8_t* wgq, const float* sg,
+                     const uint8_t* wuq, const float* su, const uint8_t* wdq, const float* sd,
+                     int H, int I, int act, uint16_t* act_out, float* y_out) {
+    float* actf = (float*)malloc(sizeof(float) * (size_t)I);
+    uint8_t* aq = (uint8_t*)malloc((size_t)I);
+    if (!actf || !aq) { free(actf); free(aq); return; }
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        const uint8_t* rg = wgq + (size_t)i * H;
+        const uint8_t* ru = wuq + (size_t)i * H;
+        for (int h = 0; h < H; ++h) {
+            const double xv = orc_e4m3_to_f32(xq[h]);
+            g += xv * orc_e4m3_to_f32(rg[h]);
+            u += xv * orc_e4m3_to_f32(ru[h]);
+        }
+        const double gf = (float)((float)g * sx * sg[i]), uf = (float)((float)u * sx * su[i]);
+        act_out[i] = f32_to_bf16((float)orc_act_value(act, gf, uf));
+        actf[i] = bf16_to_f32(act_out[i]);
+    }
+    const float sa = oracle_quantize_row(NULL, actf, I, aq);
+    for (int h = 0; h < H; ++h) {
+        double acc = 0.0;
+        const uint8_t* rd = wdq + (size_t)h * I;
+        for (int i = 0; i < I; ++i) acc += (double)orc_e4m3_to_f32(aq[i]) * orc_e4m3_to_f32(rd[i]);
+        y_out[h] = (float)acc * sa * sd[h];
+    }
+    free(actf);
+    free(aq);
+}
+
+typedef struct {
+    const uint8_t* xq;
+    const float* sx;
+    const uint8_t *wg, *wu, *wd;
+    const float *sg, *su, *sd;
+    const int32_t *row_to_token, *row_expert;
+    int H, I, act_kind;
+    uint16_t* act;
+    float* y;
+} orc_ffn8_ctx;
+
+static void orc_ffn8_task(void* c_, int64_t r) {
+    orc_ffn8_ctx* c = (orc_ffn8_ctx*)c_;
+    const int64_t t = c->row_to_token[r];
+    const int64_t p = c->row_expert[r];
+    const size_t HI = (size_t)c->H * c->I;
+    orc_ffn_row_fp8(c->xq + (size_t)t * c->H, c->sx[t], c->wg + p * HI, c->sg + p * c->I,
+                    c->wu + p * HI, c->su + p * c->I, c->wd + p * HI, c->sd + p * c->H, c->H,
+                    c->I, c->act_kind, c->act + (size_t)r * c->I, c->y + (size_t)r * c->H);
+}
+
+/* Grouped FP8 MLP over the permuted rows (x quantized per token: xq [T, H], sx [T]);
+ * weight codes [P, I, H] / [P, H, I] with per-row scales [P, I] / [P, H]. */
+void oracle_ffn_grouped_fp8(const uint8_t* xq, const float* sx, const int32_t* row_to_token,
+                            const int32_t* offsets, int P, int H, int I, const uint8_t* wg,
+                            const float* sg, const uint8_t* wu, const float* su,
+                            const uint8_t* wd, const float* sd, int act_kind, uint16_t* act,
+                            float* y, int nthreads) {
+    int64_t N = offsets[P];
+    int32_t* row_expert = (int32_t*)malloc(sizeof(int32_t) * (N > 0 ? N : 1));
+    for (int p = 0; p < P; ++p)
+        for (int32_t r = offsets[p]; r < offsets[p + 1]; ++r) row_expert[r] = p;
+    orc_ffn8_ctx c = {xq, sx, wg, wu, wd, sg, su, sd, row_to_token, row_expert, H, I, act_kind,
+                      act, y};
+    orc_parallel_for(N, nthreads, orc_ffn8_task, &c);
+    free(row_expert);
 }
