@@ -311,6 +311,41 @@ int moe_combine(const float* y, const int32_t* flat_to_row, const float* weights
                 gbmoe_stream_t stream);
 
 /*
+ * moe_gemm_gateup_act_fp8 / moe_gemm_down_fp8 — the grouped GEMMs with FP8
+ * (E4M3) operands on the tensor cores (tcgen05 kind::f8f6f4), one fp32 scale
+ * per weight row and per token / routed row (reading of "Stage 4" W8A8FP):
+ *   g = (sum_h xq[t,h] wgq[p,i,h]) * sx[t] * sg[p,i], u likewise with wuq, su;
+ *   act[r, i] = bf16(f(g, u)), t = row_to_token[r] (row_to_token NULL: t = r,
+ *   xq holds the N permuted rows);
+ *   y[r, h] = (sum_i aq[r,i] wdq[p,h,i]) * sa[r] * sd[p,h]  (fp32).
+ *   xq [T or N, H] codes, sx [T or N]; wgq, wuq [E_phys, I, H] codes, sg, su
+ *   [E_phys, I]; aq [N, I] codes, sa [N]; wdq [E_phys, H, I] codes, sd
+ *   [E_phys, H].  H % 256 == 0 and I % 128 == 0 (else UNSUPPORTED); code
+ *   arrays 16-byte aligned.  Codes and scales come from moe_quantize_fp8_rows.
+ */
+int moe_gemm_gateup_act_fp8(const uint8_t* xq, const float* sx, const int32_t* row_to_token,
+                            int T, const int32_t* offsets, int E_phys, int N, int H, int I,
+                            const uint8_t* wgq, const float* sg, const uint8_t* wuq,
+                            const float* su, int activation, uint16_t* act,
+                            gbmoe_stream_t stream);
+int moe_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offsets, int E_phys,
+                      int N, int H, int I, const uint8_t* wdq, const float* sd, float* y,
+                      gbmoe_stream_t stream);
+
+/*
+ * moe_quantize_fp8_rows — FP8 (OCP E4M3) quantization of bf16 rows for the
+ * FP8 expert path ("Stage 4" quantized paths, W8A8FP): per row r
+ *   scales[r] = amax_k |x[r, k]| / 448  (1 for an all-zero row),
+ *   q[r, k] = e4m3(x[r, k] / scales[r])  (IEEE division, round to nearest
+ *   even, saturation to +-448).
+ *   x [n, K] bf16, K a multiple of 8 (else GBMOE_ERR_UNSUPPORTED), 16-byte
+ *   aligned; q [n, K] uint8 codes, 8-byte aligned; scales [n] fp32.  Used for
+ *   weights (one scale per output channel) and for hidden states (per token).
+ */
+int moe_quantize_fp8_rows(const uint16_t* x, int64_t n, int K, uint8_t* q, float* scales,
+                          gbmoe_stream_t stream);
+
+/*
  * moe_latent_tail — the post-MoE tail of a latent MoE on one GPU (the NVIDIA
  * LatentMoERunner page, tier-1 tail "_overlap_allreduce_tail": reduce the
  * routed latent output, RMSNorm, up-project to the hidden size with the

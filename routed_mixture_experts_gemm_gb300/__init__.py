@@ -22,7 +22,8 @@ from ._lib import ACTIVATION, ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
 
 __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_permute",
            "moe_gemm_gateup_act", "moe_gemm_gateup_act_rows", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
-           "moe_combine", "moe_latent_tail", "MoELayer", "moe_forward",
+           "moe_combine", "moe_quantize_fp8_rows",
+           "moe_gemm_gateup_act_fp8", "moe_gemm_down_fp8", "moe_latent_tail", "MoELayer", "moe_forward",
            "moe_forward_host", "check_device_status", "library"]
 
 
@@ -215,6 +216,50 @@ def moe_combine(y, flat_to_row, weights, shared_y=None, out=None, stream=None):
     _check(lib.moe_combine(_ptr(y), _ptr(flat_to_row), _ptr(weights), _ptr(shared_y), T, k, H,
                            _ptr(out), _stream(stream)), "moe_combine")
     return out
+
+
+def moe_quantize_fp8_rows(x, q=None, scales=None, stream=None):
+    """bf16 rows [n, K] -> (E4M3 codes uint8 [n, K], fp32 scales [n]), s = amax / 448."""
+    lib = _lib.load()
+    n, K = x.shape
+    if q is None:
+        q = torch.empty((n, K), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(n, dtype=torch.float32, device=x.device)
+    _check(lib.moe_quantize_fp8_rows(_ptr(x), n, K, _ptr(q), _ptr(scales), _stream(stream)),
+           "moe_quantize_fp8_rows")
+    return q, scales
+
+
+def moe_gemm_gateup_act_fp8(xq, sx, offsets, wgq, sg, wuq, su, row_to_token=None, act=None,
+                            activation="swiglu", stream=None):
+    """FP8 gate/up GEMM: act = bf16(f((xq wgq^T) sx sg, (xq wuq^T) sx su)); xq [T, H]
+    codes gathered through row_to_token [N] (or the N permuted rows)."""
+    lib = _lib.load()
+    P, I, H = wgq.shape
+    if row_to_token is None:
+        N, T = xq.shape[0], 0
+    else:
+        N, T = row_to_token.shape[0], xq.shape[0]
+    if act is None:
+        act = torch.empty((N, I), dtype=torch.bfloat16, device=xq.device)
+    _check(lib.moe_gemm_gateup_act_fp8(_ptr(xq), _ptr(sx), _ptr(row_to_token), T, _ptr(offsets),
+                                       P, N, H, I, _ptr(wgq), _ptr(sg), _ptr(wuq), _ptr(su),
+                                       _act(activation), _ptr(act), _stream(stream)),
+           "moe_gemm_gateup_act_fp8")
+    return act
+
+
+def moe_gemm_down_fp8(aq, sa, offsets, wdq, sd, y=None, stream=None):
+    """FP8 down GEMM: y = (aq wdq^T) sa sd in fp32 [N, H]."""
+    lib = _lib.load()
+    N, I = aq.shape
+    P, H, _ = wdq.shape
+    if y is None:
+        y = torch.empty((N, H), dtype=torch.float32, device=aq.device)
+    _check(lib.moe_gemm_down_fp8(_ptr(aq), _ptr(sa), _ptr(offsets), P, N, H, I, _ptr(wdq),
+                                 _ptr(sd), _ptr(y), _stream(stream)), "moe_gemm_down_fp8")
+    return y
 
 
 def moe_latent_tail(latent, up_proj, norm_w=None, eps=1e-6, shared=None, out=None, ws=None,

@@ -54,6 +54,10 @@ SIGNATURES = {
                             _vp, _vp]),
     "gbmoe_expert_mlp_fused": (_i, [_i, _i, _i]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "moe_quantize_fp8_rows": (_i, [_vp, _i64, _i, _vp, _vp, _vp]),
+    "moe_gemm_gateup_act_fp8": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
+                                     _i, _vp, _vp]),
+    "moe_gemm_down_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "gbmoe_latent_tail_workspace_size": (_sz, [_i, _i, _i]),
     "moe_latent_tail": (_i, [_vp, _i, _i, _vp, ctypes.c_float, _vp, _i, _vp, _vp, _vp, _sz,
                              _vp]),

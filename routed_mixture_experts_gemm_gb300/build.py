@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libgbmoe.so")
 SOURCES = ["api.cu", "route.cu", "permute.cu", "permute_static.cu", "gemm.cu", "combine.cu",
-           "tail.cu"]
+           "tail.cu", "quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

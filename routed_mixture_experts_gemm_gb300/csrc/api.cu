@@ -358,6 +358,57 @@ int moe_combine(const float* y, const int32_t* flat_to_row, const float* weights
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_gemm_gateup_act_fp8(const uint8_t* xq, const float* sx, const int32_t* row_to_token,
+                            int T, const int32_t* offsets, int E_phys, int N, int H, int I,
+                            const uint8_t* wgq, const float* sg, const uint8_t* wuq,
+                            const float* su, int activation, uint16_t* act,
+                            gbmoe_stream_t stream) {
+    if (!valid_activation(activation)) return GBMOE_ERR_UNSUPPORTED;
+    if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
+    if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
+    if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
+    if (H % 256 || I % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (N == 0) return GBMOE_OK;
+    if (row_to_token && T < 1) return GBMOE_ERR_INVALID_ARG;
+    if (!xq || !sx || !wgq || !sg || !wuq || !su || !act) return GBMOE_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(wgq) || !aligned16(wuq) || !aligned16(act))
+        return GBMOE_ERR_INVALID_ARG;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return launch_gemm_gateup_fp8(xq, sx, row_to_token, row_to_token ? T : N, offsets, E_phys, N,
+                                  H, I, wgq, sg, wuq, su, activation, act, *ctx,
+                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offsets, int E_phys,
+                      int N, int H, int I, const uint8_t* wdq, const float* sd, float* y,
+                      gbmoe_stream_t stream) {
+    if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
+    if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
+    if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
+    if (H % 256 || I % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (N == 0) return GBMOE_OK;
+    if (!aq || !sa || !wdq || !sd || !y) return GBMOE_ERR_INVALID_ARG;
+    if (!aligned16(aq) || !aligned16(wdq) || !aligned16(y)) return GBMOE_ERR_INVALID_ARG;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return launch_gemm_down_fp8(aq, sa, offsets, E_phys, N, H, I, wdq, sd, y, *ctx,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_quantize_fp8_rows(const uint16_t* x, int64_t n, int K, uint8_t* q, float* scales,
+                          gbmoe_stream_t stream) {
+    if (n < 0 || K <= 0) return GBMOE_ERR_INVALID_ARG;
+    if (K % 8) return GBMOE_ERR_UNSUPPORTED;
+    if (n == 0) return GBMOE_OK;
+    if (!x || !q || !scales || !aligned16(x) || (reinterpret_cast<uintptr_t>(q) & 7u))
+        return GBMOE_ERR_INVALID_ARG;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return status_from(launch_quantize_rows(x, n, K, q, scales, *ctx,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t gbmoe_latent_tail_workspace_size(int T, int L, int Hm) {
     if (T < 0 || L <= 0 || Hm <= 0) return 0;
     return latent_tail_ws_bytes(T, L, Hm);

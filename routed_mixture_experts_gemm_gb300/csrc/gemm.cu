@@ -57,7 +57,6 @@ namespace gbmoe {
 namespace {
 
 constexpr int BM = 128;          // weight rows per MMA (M)
-constexpr int UMMA_K = 16;       // K per tcgen05.mma kind::f16
 // K elements per pipeline stage (template parameter BK): 64 = one 128-byte
 // swizzled row (128B swizzle), 32 = one 64-byte row (64B swizzle).
 constexpr int BOX_ROWS = 16;     // granularity of the token dimension (MMA N step, smallest box)
@@ -81,12 +80,14 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kSwiGLU = 0, kDown = 1, kDownPair = 2, kFused = 3;
 
 // Shared memory: a ring of SA weight stages (NUM_A boxes of 128 rows x BK)
-// and a ring of SB token stages (up to BN rows x BK).
-template <int NUM_A, int BN, int SA, int SB, int ACC_BUFS, int BK>
+// and a ring of SB token stages (up to BN rows x BK); EB bytes per element
+// (2: bf16, 1: FP8 E4M3), a stage row is BK * EB = 128 (or 64) bytes.
+template <int NUM_A, int BN, int SA, int SB, int ACC_BUFS, int BK, int EB = 2>
 struct Layout {
-    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int ROW_BYTES = BK * EB;
+    static constexpr int A_BYTES = BM * ROW_BYTES;
     static constexpr int A_STAGE = NUM_A * A_BYTES;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = BN * ROW_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
     static constexpr int TMEM_COLS = ACC_BUFS * ACC_COLS;
     static constexpr int TABLE_INTS = MAX_GROUPS + 4;
@@ -102,7 +103,8 @@ struct Layout {
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of 2");
     static_assert(A_STAGE % 1024 == 0 && B_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
-    static_assert(BK == 64 || BK == 32, "stage K is one 128- or 64-byte swizzled row");
+    static_assert(ROW_BYTES == 128 || (EB == 2 && ROW_BYTES == 64),
+                  "stage K is one 128- or 64-byte swizzled row");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(SA >= 2 && SB >= 2 && SA <= 16 && SB <= 16, "ring depth");
     static_assert(BN % BOX_ROWS == 0 && BN % (2 * EPI_COLS) == 0 && BN <= 256, "tile width");
@@ -125,9 +127,15 @@ struct GemmArgs {
     // Gathered token operand of the first GEMM (null: rows of the B maps):
     // row r of the operand is gather_src[gather_rows[r]], gather_src [src_rows, K].
     const int32_t* gather_rows;
-    const uint16_t* gather_src;
+    const void* gather_src;
     int src_rows;
     int act;                 // gated activation of the gate/up epilogue (GBMOE_ACT_*)
+    // FP8 operands: the accumulator of output (row r, token column n) is
+    // scaled by tok_scale[token of n] and by w_scale0[weight row] (the gate, or
+    // the down weight; w_scale1: the up weight); null for bf16 operands
+    const float* tok_scale;
+    const float* w_scale0;
+    const float* w_scale1;
 };
 
 // The second GEMM of the fused mode (paired down tiles) and the per-group
@@ -256,7 +264,7 @@ __device__ __forceinline__ float gated_act(int act, float g, float u) {
     }
 }
 
-template <int NUM_A, int BN, int SA, int SB, int MODE, int ACC_BUFS, int BK>
+template <int NUM_A, int BN, int SA, int SB, int MODE, int ACC_BUFS, int BK, int EB = 2>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__ GemmMaps m2,
                     const GemmArgs args, const FusedArgs fz) {
@@ -264,7 +272,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     constexpr int MODE1 = FUSED ? kSwiGLU : MODE;  // mode of the first GEMM's tiles
     static_assert(MODE1 != kDown || NUM_A == 1, "down tiles have one A operand");
     static_assert(MODE1 == kDown || NUM_A == 2, "gate/up and paired tiles have two");
-    using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK>;
+    using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK, EB>;
+    static_assert(EB == 2 || !FUSED, "the FP8 path runs its GEMMs as two launches");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -451,7 +460,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             bool second;
             Tile tl;
             job(tau, second, tl);
-            const bool gather = !second && !solo && BK == 64;
+            const bool gather = !second && !solo && L::ROW_BYTES == 128;
             if (FUSED && second) {
                 // publish a pending gathered stage before waiting: the MMA
                 // needs it to finish the very gate/up tiles waited for
@@ -501,7 +510,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                             record_error(args.status, GBMOE_ERR_DEVICE);
                             t = 0;
                         }
-                        src[u] = static_cast<int64_t>(t) * args.K + chunk * 8;
+                        src[u] = static_cast<int64_t>(t) * args.K * EB + chunk * 16;
                     }
                 }
             }
@@ -522,7 +531,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                         if (src[u] >= 0) {
                             const int r = rbase + RSTEP * u;
                             const uint32_t dst = sb + r * 128 + ((chunk ^ (r & 7)) << 4);
-                            cp_async16(dst, args.gather_src + src[u] + kb * BK, pol_x);
+                            cp_async16(dst,
+                                       static_cast<const uint8_t*>(args.gather_src) + src[u] +
+                                           static_cast<int64_t>(kb) * L::ROW_BYTES,
+                                       pol_x);
                         }
                     }
                     cp_async_commit();
@@ -536,15 +548,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     }
                     pend = stage;
                 } else if (lead) {
-                    mbar_arrive_expect_tx(bfull + stage, n_load * BK * 2);
+                    mbar_arrive_expect_tx(bfull + stage, n_load * L::ROW_BYTES);
                     // token rows in as few boxes as possible (128/64/32/16 rows)
                     for (int off = 0; off < n_load;) {
                         const int rem = n_load - off;
                         const int box = rem >= 128 ? 128 : rem >= 64 ? 64 : rem >= 32 ? 32 : 16;
                         const CUtensorMap* mb = box == 128 ? &m.b128 : box == 64 ? &m.b64
                                               : box == 32 ? &m.b32 : &m.b16;
-                        tma_load_2d(sB + off * BK * 2, mb, bfull + stage, kb * BK, tl.row0 + off,
-                                    pol_x);
+                        tma_load_2d(sB + off * L::ROW_BYTES, mb, bfull + stage, kb * BK,
+                                    tl.row0 + off, pol_x);
                         off += box;
                     }
                     armed |= 1u << stage;
@@ -579,7 +591,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             job(tau, second, tl);
             const int KB = (second ? fz.K : args.K) / BK;
             const int n_mma = ((tl.n_valid + 15) / 16) * 16;
-            const uint32_t idesc = idesc_bf16_f32(BM, n_mma);
+            const uint32_t idesc = EB == 2 ? idesc_bf16_f32(BM, n_mma) : idesc_e4m3_f32(BM, n_mma);
             if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, args.status,
                                    kWaitLimitNs))
                 break;
@@ -595,14 +607,20 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 tc_fence_after();
                 const uint32_t sA = smem_u32(smem + as * L::A_STAGE);
                 const uint32_t sB = smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
+                // one MMA covers 32 bytes of K (16 bf16 or 32 FP8 elements)
 #pragma unroll
-                for (int ks = 0; ks < BK / UMMA_K; ++ks) {
-                    const uint64_t bdesc = smem_desc_kmajor<BK>(sB + ks * UMMA_K * 2);
+                for (int ks = 0; ks < L::ROW_BYTES / 32; ++ks) {
+                    const uint64_t bdesc = smem_desc_kmajor<L::ROW_BYTES / 2>(sB + ks * 32);
 #pragma unroll
                     for (int a = 0; a < NUM_A; ++a) {
                         const uint64_t adesc =
-                            smem_desc_kmajor<BK>(sA + a * L::A_BYTES + ks * UMMA_K * 2);
-                        umma_bf16(d0 + a * BN, adesc, bdesc, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+                            smem_desc_kmajor<L::ROW_BYTES / 2>(sA + a * L::A_BYTES + ks * 32);
+                        if (EB == 2)
+                            umma_bf16(d0 + a * BN, adesc, bdesc, idesc,
+                                      (kb > 0 || ks > 0) ? 1u : 0u);
+                        else
+                            umma_e4m3(d0 + a * BN, adesc, bdesc, idesc,
+                                      (kb > 0 || ks > 0) ? 1u : 0u);
                     }
                 }
                 issued = true;
@@ -657,33 +675,55 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             for (int c0 = half * EPI_COLS; c0 < tl.n_valid; c0 += 2 * EPI_COLS)
 #pragma unroll 1
             for (int ob = 0; ob < nout; ++ob) {
-                uint32_t g[16];
+                const int nr = min(EPI_COLS, tl.n_valid - c0);
+                const size_t col = static_cast<size_t>(tl.rblk) * wrows + ob * BM + r;
+                uint32_t g[16], u[16];
                 tmem_ld_32x32b_x16(tb + ob * BN + c0, g);
+                if (swiglu) tmem_ld_32x32b_x16(tb + BN + c0, u);
+                tmem_ld_wait();
+                float gv[16], uv[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    gv[c] = __uint_as_float(g[c]);
+                    uv[c] = swiglu ? __uint_as_float(u[c]) : 0.0f;
+                }
+                if (EB == 1) {
+                    // FP8 operands: (acc * token scale) * weight-row scale
+                    const size_t wrow = static_cast<size_t>(tl.p) * R + col;
+                    const float sw0 = args.w_scale0[wrow];
+                    const float sw1 = swiglu ? args.w_scale1[wrow] : 0.0f;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        float st = 0.0f;
+                        if (c < nr) {
+                            int tok = tl.row0 + c0 + c;
+                            if (args.gather_rows) {
+                                tok = args.gather_rows[tok];
+                                tok = (tok < 0 || tok >= args.src_rows) ? 0 : tok;
+                            }
+                            st = args.tok_scale[tok];
+                        }
+                        gv[c] = __fmul_rn(__fmul_rn(gv[c], st), sw0);
+                        if (swiglu) uv[c] = __fmul_rn(__fmul_rn(uv[c], st), sw1);
+                    }
+                }
                 float v[16];
                 if (swiglu) {
-                    uint32_t u[16];
-                    tmem_ld_32x32b_x16(tb + BN + c0, u);
-                    tmem_ld_wait();
                     if (args.act == GBMOE_ACT_SWIGLU) {
 #pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            v[c] = silu_mul(__uint_as_float(g[c]), __uint_as_float(u[c]));
+                        for (int c = 0; c < 16; ++c) v[c] = silu_mul(gv[c], uv[c]);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            v[c] = gated_act(args.act, __uint_as_float(g[c]), __uint_as_float(u[c]));
+                        for (int c = 0; c < 16; ++c) v[c] = gated_act(args.act, gv[c], uv[c]);
                     }
                 } else {
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(g[c]);
+                    for (int c = 0; c < 16; ++c) v[c] = gv[c];
                 }
                 // Lane r holds output column r for 16 consecutive token rows,
                 // so for each row the 32 lanes of a warp write 32 consecutive
                 // outputs (128 B of fp32 / 64 B of bf16): coalesced stores
                 // straight from registers.
-                const int nr = min(EPI_COLS, tl.n_valid - c0);
-                const size_t col = static_cast<size_t>(tl.rblk) * wrows + ob * BM + r;
                 uint8_t* base = outp + (static_cast<size_t>(tl.row0 + c0) * R + col) * out_elem;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
@@ -749,6 +789,14 @@ using Gemm2Pair = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK>;
 #define GEMM2_LARGE grouped_gemm_kernel<1, 256, kG2L_A, kG2L_B, kDown, 2, kBK>
 #define GEMM2_PAIR grouped_gemm_kernel<2, 128, kG2P_A, kG2P_B, kDownPair, 2, kBK>
 #define GEMM_FUSED grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kFused, 2, kBK>
+// FP8 E4M3 operands: 128-element stages (the same 128-byte rows)
+constexpr int kBK8 = 128;
+using Gemm1SmallF8 = Layout<2, 128, kG1S_A, kG1S_B, 2, kBK8, 1>;
+using Gemm1LargeF8 = Layout<2, 256, kG1L_A, kG1L_B, 1, kBK8, 1>;
+using Gemm2PairF8 = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK8, 1>;
+#define GEMM1_SMALL_F8 grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kSwiGLU, 2, kBK8, 1>
+#define GEMM1_LARGE_F8 grouped_gemm_kernel<2, 256, kG1L_A, kG1L_B, kSwiGLU, 1, kBK8, 1>
+#define GEMM2_PAIR_F8 grouped_gemm_kernel<2, 128, kG2P_A, kG2P_B, kDownPair, 2, kBK8, 1>
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -783,6 +831,19 @@ bool make_gemm_maps(GemmMaps* g, const void* a0, const void* a1, uint64_t weight
            make_map(&g->b64, b, n_rows, K, 64, kBK) && make_map(&g->b128, b, n_rows, K, 128, kBK);
 }
 
+// FP8 (one byte per element) maps: 128-element boxes with the 128B swizzle.
+bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    return encode_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, K, rows, K, kBK8, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool make_gemm_maps_u8(GemmMaps* g, const void* a0, const void* a1, uint64_t weight_rows,
+                       const void* b, uint64_t n_rows, uint64_t K) {
+    return make_map_u8(&g->a0, a0, weight_rows, K, BM) &&
+           make_map_u8(&g->a1, a1 ? a1 : a0, weight_rows, K, BM) &&
+           make_map_u8(&g->b16, b, n_rows, K, 16) && make_map_u8(&g->b32, b, n_rows, K, 32) &&
+           make_map_u8(&g->b64, b, n_rows, K, 64) && make_map_u8(&g->b128, b, n_rows, K, 128);
+}
+
 std::mutex g_attr_mu;
 bool g_attr_done[64];
 
@@ -796,6 +857,9 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_LARGE, a, Gemm2Large::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_PAIR, a, Gemm2Pair::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM_FUSED, a, Gemm1Small::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_SMALL_F8, a, Gemm1SmallF8::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_LARGE_F8, a, Gemm1LargeF8::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_PAIR_F8, a, Gemm2PairF8::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) g_attr_done[device] = true;
     return cudaSuccess;
@@ -906,6 +970,51 @@ int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* row_to_token, i
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, GEMM_FUSED, m1, m2, a, f);
     return e == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
+}
+
+int launch_gemm_gateup_fp8(const uint8_t* xq, const float* sx, const int32_t* row_to_token,
+                           int src_rows, const int32_t* offsets, int groups, int n_rows, int H,
+                           int I, const uint8_t* wg, const float* sg, const uint8_t* wu,
+                           const float* su, int activation, uint16_t* act, const DevCtx& ctx,
+                           cudaStream_t s) {
+    if (n_rows == 0) return GBMOE_OK;
+    GemmMaps m;
+    if (!make_gemm_maps_u8(&m, wg, wu, static_cast<uint64_t>(groups) * I, xq,
+                           row_to_token ? src_rows : n_rows, H))
+        return GBMOE_ERR_CUDA;
+    if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
+    GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
+               row_to_token, row_to_token ? xq : nullptr, src_rows, activation};
+    a.tok_scale = sx;
+    a.w_scale0 = sg;
+    a.w_scale1 = su;
+    const FusedArgs none{0, 0, nullptr, nullptr};
+    if (n_rows >= kLargeGateUpRows * groups) {
+        const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
+        GEMM1_LARGE_F8<<<grid, NUM_THREADS, Gemm1LargeF8::SMEM_BYTES, s>>>(m, m, a, none);
+    } else {
+        const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
+        GEMM1_SMALL_F8<<<grid, NUM_THREADS, Gemm1SmallF8::SMEM_BYTES, s>>>(m, m, a, none);
+    }
+    return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
+}
+
+int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offsets, int groups,
+                         int n_rows, int H, int I, const uint8_t* wd, const float* sd, float* y,
+                         const DevCtx& ctx, cudaStream_t s) {
+    if (n_rows == 0) return GBMOE_OK;
+    if (H % 256) return GBMOE_ERR_UNSUPPORTED;
+    GemmMaps m;
+    if (!make_gemm_maps_u8(&m, wd, nullptr, static_cast<uint64_t>(groups) * H, aq, n_rows, I))
+        return GBMOE_ERR_CUDA;
+    if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
+    GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
+    a.tok_scale = sa;
+    a.w_scale0 = sd;
+    const FusedArgs none{0, 0, nullptr, nullptr};
+    const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
+    GEMM2_PAIR_F8<<<grid, NUM_THREADS, Gemm2PairF8::SMEM_BYTES, s>>>(m, m, a, none);
+    return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 
 }  // namespace gbmoe

@@ -81,6 +81,22 @@ int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* row_to_token, i
                           int activation, uint16_t* act, float* y, int* ready,
                           const DevCtx& ctx, cudaStream_t s);
 
+// FP8 E4M3 grouped GEMMs (two launches; one fp32 scale per token / routed
+// row and per weight row): act = bf16(f((xq.wg^T) sx sg, (xq.wu^T) sx su)),
+// y = (aq.wd^T) sa sd.  H % 256 == 0 for the down GEMM.
+int launch_gemm_gateup_fp8(const uint8_t* xq, const float* sx, const int32_t* row_to_token,
+                           int src_rows, const int32_t* offsets, int groups, int n_rows, int H,
+                           int I, const uint8_t* wg, const float* sg, const uint8_t* wu,
+                           const float* su, int activation, uint16_t* act, const DevCtx& ctx,
+                           cudaStream_t s);
+int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offsets, int groups,
+                         int n_rows, int H, int I, const uint8_t* wd, const float* sd, float* y,
+                         const DevCtx& ctx, cudaStream_t s);
+
+// --- FP8 row quantization (quant.cu) ---
+cudaError_t launch_quantize_rows(const uint16_t* x, int64_t n, int K, uint8_t* q, float* s,
+                                 const DevCtx& ctx, cudaStream_t st);
+
 // --- latent-MoE tail (tail.cu) ---
 size_t latent_tail_ws_bytes(int T, int L, int Hm);
 int launch_latent_tail(const uint16_t* latent, int T, int L, const uint16_t* norm_w, float eps,
