@@ -118,6 +118,17 @@ typedef struct gbmoe_layer {
     const uint16_t* w_up_shared;  /* [I_shared, H] bf16 or NULL */
     const uint16_t* w_down_shared;/* [H, I_shared] bf16 or NULL */
     int activation;               /* GBMOE_ACT_*, of the routed and the shared experts */
+    /* FP8 routed experts (W8A8FP, see moe_gemm_gateup_act_fp8): when w_gate_q
+     * is non-NULL the routed expert MLP runs on these E4M3 codes and per-row
+     * scales (hidden states and activations are quantized per row on the fly)
+     * and w_gate / w_up / w_down may be NULL; H % 256 == 0.  The shared expert
+     * stays bf16. */
+    const uint8_t* w_gate_q;      /* [E_phys, I, H] E4M3 codes */
+    const float* s_gate;          /* [E_phys, I] */
+    const uint8_t* w_up_q;        /* [E_phys, I, H] */
+    const float* s_up;            /* [E_phys, I] */
+    const uint8_t* w_down_q;      /* [E_phys, H, I] */
+    const float* s_down;          /* [E_phys, H] */
 } gbmoe_layer;
 
 /* Text for a status code (static storage). */

@@ -23,7 +23,7 @@ from ._lib import ACTIVATION, ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
 __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_permute",
            "moe_gemm_gateup_act", "moe_gemm_gateup_act_rows", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
            "moe_combine", "moe_quantize_fp8_rows",
-           "moe_gemm_gateup_act_fp8", "moe_gemm_down_fp8", "moe_latent_tail", "MoELayer", "moe_forward",
+           "moe_gemm_gateup_act_fp8", "moe_gemm_down_fp8", "quantize_experts_fp8", "moe_latent_tail", "MoELayer", "moe_forward",
            "moe_forward_host", "check_device_status", "library"]
 
 
@@ -262,6 +262,14 @@ def moe_gemm_down_fp8(aq, sa, offsets, wdq, sd, y=None, stream=None):
     return y
 
 
+def quantize_experts_fp8(w, stream=None):
+    """bf16 expert weights [E, R, K] -> (E4M3 codes uint8 [E, R, K], fp32 per-row
+    scales [E, R]) with moe_quantize_fp8_rows."""
+    E, R, K = w.shape
+    q, sc = moe_quantize_fp8_rows(w.reshape(E * R, K), stream=stream)
+    return q.reshape(E, R, K), sc.reshape(E, R)
+
+
 def moe_latent_tail(latent, up_proj, norm_w=None, eps=1e-6, shared=None, out=None, ws=None,
                     stream=None):
     """out = bf16(rmsnorm(latent) . up_proj^T + shared): the latent-MoE tail on
@@ -293,20 +301,25 @@ class MoELayer:
 
     def __init__(self, cfg: RouteCfg, w_router, w_gate, w_up, w_down, router_bias=None,
                  corr_bias=None, tid2eid=None, log2phy=None, replica_cnt=None, shared=None,
-                 activation="swiglu"):
+                 activation="swiglu", fp8=None):
+        """fp8 = (w_gate_q, s_gate, w_up_q, s_up, w_down_q, s_down): FP8 routed
+        experts (E4M3 codes uint8 [E_phys, I, H] / [E_phys, H, I] and fp32
+        per-row scales, e.g. from quantize_experts_fp8); the bf16 w_gate / w_up /
+        w_down may then be None."""
         self.cfg = cfg
         self._keep = [w_router, w_gate, w_up, w_down, router_bias, corr_bias, tid2eid, log2phy,
-                      replica_cnt] + list(shared or [])
-        P, I, H = w_gate.shape
+                      replica_cnt] + list(shared or []) + list(fp8 or [])
+        ref = w_gate if w_gate is not None else fp8[0]
+        P, I, H = ref.shape
         Is = 0 if shared is None else shared[0].shape[0]
         self.H, self.I, self.I_shared = H, I, Is
-        self.device = w_gate.device
+        self.device = ref.device
         s = shared or (None, None, None)
         self.c = Layer(cfg, H, I, Is, _ptr(w_router), _ptr(router_bias), _ptr(corr_bias),
                        _ptr(tid2eid), 0 if tid2eid is None else tid2eid.shape[0], _ptr(log2phy),
                        _ptr(replica_cnt), 1 if log2phy is None else log2phy.shape[1],
                        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s[0]), _ptr(s[1]),
-                       _ptr(s[2]), _act(activation))
+                       _ptr(s[2]), _act(activation), *[_ptr(a) for a in (fp8 or [None] * 6)])
         self._ws = None
 
     def workspace_size(self, T_max: int, host: bool = False) -> int:

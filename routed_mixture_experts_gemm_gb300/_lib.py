@@ -31,7 +31,8 @@ class Layer(ctypes.Structure):
                 ("tid2eid", _vp), ("tid2eid_rows", _i64), ("log2phy", _vp),
                 ("replica_cnt", _vp), ("R_max", _i), ("w_gate", _vp), ("w_up", _vp),
                 ("w_down", _vp), ("w_gate_shared", _vp), ("w_up_shared", _vp),
-                ("w_down_shared", _vp), ("activation", _i)]
+                ("w_down_shared", _vp), ("activation", _i), ("w_gate_q", _vp), ("s_gate", _vp),
+                ("w_up_q", _vp), ("s_up", _vp), ("w_down_q", _vp), ("s_down", _vp)]
 
 
 _P = ctypes.POINTER

@@ -71,6 +71,8 @@ struct FwdWs {
     void* perm;
     uint16_t *act, *act_s;
     float *y, *ys;
+    uint8_t *xq, *aq;  // FP8 layers: hidden-state and activation codes
+    float *sx, *sa;    // and their per-row scales
     size_t bytes;
 };
 
@@ -93,6 +95,11 @@ FwdWs layout_fwd(const gbmoe_layer* L, int T, void* ws) {
     f.y = w.take<float>(N * L->H);
     f.act_s = w.take<uint16_t>(static_cast<size_t>(T) * L->I_shared);
     f.ys = w.take<float>(L->I_shared ? static_cast<size_t>(T) * L->H : 0);
+    const bool fp8 = L->w_gate_q != nullptr;
+    f.xq = w.take<uint8_t>(fp8 ? static_cast<size_t>(T) * L->H : 0);
+    f.sx = w.take<float>(fp8 ? static_cast<size_t>(T) : 0);
+    f.aq = w.take<uint8_t>(fp8 ? N * L->I : 0);
+    f.sa = w.take<float>(fp8 ? N : 0);
     f.bytes = w.off;
     return f;
 }
@@ -104,9 +111,18 @@ int check_layer(const gbmoe_layer* L) {
     const gbmoe_route_cfg& c = L->route;
     if (L->H <= 0 || L->I <= 0 || L->I_shared < 0) return GBMOE_ERR_INVALID_ARG;
     if (L->H % 128 || L->I % 128 || L->I_shared % 128) return GBMOE_ERR_UNSUPPORTED;
-    if (!L->w_router || !L->w_gate || !L->w_up || !L->w_down) return GBMOE_ERR_INVALID_ARG;
-    if (!aligned16(L->w_gate) || !aligned16(L->w_up) || !aligned16(L->w_down))
-        return GBMOE_ERR_INVALID_ARG;
+    if (!L->w_router) return GBMOE_ERR_INVALID_ARG;
+    if (L->w_gate_q) {  // FP8 routed experts
+        if (!L->w_up_q || !L->w_down_q || !L->s_gate || !L->s_up || !L->s_down)
+            return GBMOE_ERR_INVALID_ARG;
+        if (!aligned16(L->w_gate_q) || !aligned16(L->w_up_q) || !aligned16(L->w_down_q))
+            return GBMOE_ERR_INVALID_ARG;
+        if (L->H % 256) return GBMOE_ERR_UNSUPPORTED;
+    } else {
+        if (!L->w_gate || !L->w_up || !L->w_down) return GBMOE_ERR_INVALID_ARG;
+        if (!aligned16(L->w_gate) || !aligned16(L->w_up) || !aligned16(L->w_down))
+            return GBMOE_ERR_INVALID_ARG;
+    }
     if (c.use_hash && (!L->tid2eid || L->tid2eid_rows <= 0 || L->corr_bias))
         return GBMOE_ERR_INVALID_ARG;
     if (L->log2phy && (!L->replica_cnt || L->R_max < 1)) return GBMOE_ERR_INVALID_ARG;
@@ -475,7 +491,20 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
     if (st) return st;
     // 3-4. grouped gate/up + SwiGLU, grouped down ("Stage 4": unified_apply_mlp);
     // one fused launch for small groups
-    if (gemm_fused_eligible(c.E_phys, N, L->H)) {
+    if (L->w_gate_q) {
+        // FP8 routed experts: hidden states and activations quantized per row
+        st = status_from(launch_quantize_rows(x, T, L->H, f.xq, f.sx, *ctx, s));
+        if (st) return st;
+        st = launch_gemm_gateup_fp8(f.xq, f.sx, f.row_to_token, T, f.offsets, c.E_phys, N, L->H,
+                                    L->I, L->w_gate_q, L->s_gate, L->w_up_q, L->s_up,
+                                    L->activation, f.act, *ctx, s);
+        if (st) return st;
+        st = status_from(launch_quantize_rows(f.act, N, L->I, f.aq, f.sa, *ctx, s));
+        if (st) return st;
+        st = launch_gemm_down_fp8(f.aq, f.sa, f.offsets, c.E_phys, N, L->H, L->I, L->w_down_q,
+                                  L->s_down, f.y, *ctx, s);
+        if (st) return st;
+    } else if (gemm_fused_eligible(c.E_phys, N, L->H)) {
         st = launch_gemm_mlp_fused(x, f.row_to_token, T, f.offsets, c.E_phys, N, L->H, L->I,
                                    L->w_gate, L->w_up, L->w_down, L->activation, f.act, f.y,
                                    f.ready, *ctx, s);

@@ -102,3 +102,52 @@ def test_fp8_gemms(gb, shape, act):
         ref_y = a @ wdd.T
         bound = np.abs(a) @ np.abs(wdd).T
         assert np.all(np.abs(y_h[r0:r1] - ref_y) <= 2.0 ** -12 * bound + 1e-30)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mini_prefill", "mini_hash", "mini_skew"])
+def test_fp8_forward_end_to_end(gb, name):
+    """moe_forward with FP8 routed experts against the oracle pipeline: the
+    same routing and permutation (bit-exact), the weight codes bit-exact, the
+    oracle's FP8 MLP on its own codes of x and of the weights, the shared
+    expert in bf16, the fixed-order combine."""
+    from synth.device import device_case
+    cfg = synth.MINI[name]
+    case = device_case(cfg, DEV, host_weights=True)
+    d = case.dev
+    q = [gb.quantize_experts_fp8(d[k]) for k in ("w_gate", "w_up", "w_down")]
+    layer = gb.MoELayer(case.layer.cfg, d["w_router"], None, None, None,
+                        router_bias=d["router_bias"], corr_bias=d["corr_bias"],
+                        tid2eid=d["tid2eid"], log2phy=d["log2phy"],
+                        replica_cnt=d["replica_cnt"], shared=d["shared"],
+                        fp8=[a for pair in q for a in pair])
+    ids_p = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    out = gb.moe_forward(layer, case.x, input_ids=case.input_ids, ids_phys=ids_p)
+    assert gb.check_device_status() == 0
+    ref = oracle.run_config(cfg, inputs=case.inputs, weights=case.weights_host)
+    assert np.array_equal(_np(ids_p), ref["ids_phys"])
+    qo = []
+    for (wq, ws), wh in zip(q, case.weights_host):
+        P, R, K = wh.shape
+        cq, cs = oracle.quantize_rows(wh.reshape(P * R, K))
+        assert np.array_equal(_np(wq).reshape(P * R, K), cq)
+        assert np.array_equal(_np(ws).reshape(-1).view(np.uint32), cs.view(np.uint32))
+        qo += [cq.reshape(P, R, K), cs.reshape(P, R)]
+    xq, sx = oracle.quantize_rows(case.inputs["x"])
+    _, y = oracle.ffn_grouped_fp8(xq, sx, ref["row_to_token"], ref["offsets"], *qo, nthreads=8)
+    out_ref = oracle.combine(y, ref["flat_to_row"], ref["weights"], ref.get("ys"))
+    assert_within_tol(_bf(out), synth.bf16_to_f32(out_ref), f"fp8 forward {name}")
+    # run-to-run determinism (bitwise)
+    out2 = gb.moe_forward(layer, case.x, input_ids=case.input_ids)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_fp8_forward_rejects_unaligned_hidden(gb):
+    from synth.device import device_case
+    case = device_case(synth.MINI["mini_decode"], DEV, host_weights=True)   # H = 384
+    d = case.dev
+    q = [gb.quantize_experts_fp8(d[k]) for k in ("w_gate", "w_up", "w_down")]
+    layer = gb.MoELayer(case.layer.cfg, d["w_router"], None, None, None,
+                        router_bias=d["router_bias"], corr_bias=d["corr_bias"],
+                        fp8=[a for pair in q for a in pair])
+    with pytest.raises(gb.GbmoeError):
+        gb.moe_forward(layer, case.x)
