@@ -131,6 +131,17 @@ def _L():
             lib.oracle_ffn_grouped_fp8.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp, vp, vp, vp,
                                                    vp, i, vp, vp, i]
             lib.oracle_ffn_grouped_fp8.restype = None
+            lib.orc_f32_to_e2m1.argtypes = [f]
+            lib.orc_f32_to_e2m1.restype = ctypes.c_uint8
+            lib.orc_e2m1_to_f32.argtypes = [ctypes.c_uint8]
+            lib.orc_e2m1_to_f32.restype = f
+            lib.orc_mx_block_exp.argtypes = [f, i]
+            lib.orc_mx_block_exp.restype = i
+            lib.oracle_mx_quantize_rows.argtypes = [vp, i64, i, i, vp, vp]
+            lib.oracle_mx_quantize_rows.restype = None
+            lib.oracle_ffn_grouped_mx.argtypes = [vp, vp, vp, vp, i, i, i, i, vp, vp, vp, vp, vp,
+                                                  vp, i, vp, vp, vp, vp, i]
+            lib.oracle_ffn_grouped_mx.restype = None
             lib.oracle_rmsnorm_row.argtypes = [vp, i, vp, f, vp]
             lib.oracle_rmsnorm_row.restype = None
             lib.oracle_latent_tail.argtypes = [vp, i, i, vp, f, vp, i, vp, vp, i]
@@ -397,3 +408,55 @@ def ffn_grouped_fp8(xq, sx, row_to_token, offsets, wg, sg, wu, su, wd, sd, nthre
                                 _p(_c(sd, np.float32)), _act(activation), _p(act), _p(y),
                                 nthreads or default_threads())
     return act, y
+
+
+# --- MX block-scaled experts (Stage 4 quantized paths, MXFP and W4A8; reading R18) ---
+MX_FORMATS = {"e4m3": 0, "e2m1": 1}
+MX_BLOCK = 32
+
+
+def f32_to_e2m1(x: float) -> int:
+    """FP4 E2M1 code (sign bit 3) of an fp32 value: nearest, ties to even, saturate to +-6."""
+    return int(_L().orc_f32_to_e2m1(float(x)))
+
+
+def e2m1_to_f32(code: int) -> float:
+    return float(_L().orc_e2m1_to_f32(int(code)))
+
+
+def mx_block_exp(amax: float, fmt: str) -> int:
+    """Shared exponent e of an MX block (scale 2^e) with largest magnitude amax."""
+    return int(_L().orc_mx_block_exp(float(amax), MX_FORMATS[fmt]))
+
+
+def mx_quantize_rows(x_bits, fmt="e4m3"):
+    """bf16 rows [n, K] -> (codes uint8 [n, K] for E4M3 or [n, K/2] packed E2M1,
+    UE8M0 block-scale bytes uint8 [n, K/32])."""
+    x = _c(x_bits, np.uint16)
+    n, K = x.shape
+    q = np.empty((n, K // 2 if fmt == "e2m1" else K), dtype=np.uint8)
+    sc = np.empty((n, K // MX_BLOCK), dtype=np.uint8)
+    _L().oracle_mx_quantize_rows(_p(x), n, K, MX_FORMATS[fmt], _p(q), _p(sc))
+    return q, sc
+
+
+def ffn_grouped_mx(xq, xs, row_to_token, offsets, wg, sg, wu, su, wd, sd, wfmt="e4m3",
+                   nthreads=None, activation="swiglu"):
+    """MX grouped expert MLP (reading R18): x as MX E4M3 codes [T, H] + scales
+    [T, H/32]; weights as MX codes in format wfmt with their block scales.
+    Returns act bf16 bits [N, I], its MX E4M3 codes [N, I] and scales [N, I/32],
+    and y fp32 [N, H]."""
+    xq = _c(xq, np.uint8)
+    P, I = wg.shape[0], wg.shape[1]
+    H = xq.shape[1]
+    N = int(offsets[P])
+    act = np.empty((N, I), dtype=np.uint16)
+    aq = np.empty((N, I), dtype=np.uint8)
+    as_ = np.empty((N, I // MX_BLOCK), dtype=np.uint8)
+    y = np.empty((N, H), dtype=np.float32)
+    u8 = lambda a: _p(_c(a, np.uint8))  # noqa: E731
+    _L().oracle_ffn_grouped_mx(_p(xq), u8(xs), _p(_c(row_to_token, np.int32)),
+                               _p(_c(offsets, np.int32)), P, H, I, MX_FORMATS[wfmt], u8(wg),
+                               u8(sg), u8(wu), u8(su), u8(wd), u8(sd), _act(activation),
+                               _p(act), _p(aq), _p(as_), _p(y), nthreads or default_threads())
+    return act, aq, as_, y

@@ -52,6 +52,10 @@
  *   R17 FP8 experts (W8A8FP): OCP E4M3 codes with one fp32 scale per row
  *      (weights per output channel, activations per token / routed row); see
  *      orc_f32_to_e4m3 and orc_ffn_row_fp8.
+ *   R18 MX block-scaled experts (MXFP8 = W8A8 with E4M3 elements, and W4A8
+ *      read as E2M1 weights with E4M3 activations): OCP Microscaling blocks
+ *      of 32 consecutive elements along the reduction axis, one power-of-two
+ *      scale per block; see orc_mx_block_exp and orc_ffn_row_mx.
  *   R16 latent-MoE tail with one rank (NVIDIA LatentMoERunner page, tier 1):
  *      out = bf16(rmsnorm(latent) . up_proj^T + shared); see oracle_latent_tail.
  *   R15 activation branches (named, not defined, by the page): SwiGLU,
@@ -736,5 +740,183 @@ void oracle_ffn_grouped_fp8(const uint8_t* xq, const float* sx, const int32_t* r
     orc_ffn8_ctx c = {xq, sx, wg, wu, wd, sg, su, sd, row_to_token, row_expert, H, I, act_kind,
                       act, y};
     orc_parallel_for(N, nthreads, orc_ffn8_task, &c);
+    free(row_expert);
+}
+
+/* ------------------------------------------------------ MX block scales */
+/*
+ * R18: MX experts ("Stage 4": quantized paths include MXFP variants and W4A8;
+ * the page gives no formats).  Read as the OCP Microscaling (MX) format:
+ * every row is cut into blocks of 32 consecutive elements along the
+ * reduction axis (H for x, W_gate, W_up; I for the activations and W_down);
+ * a block shares one scale X = 2^e stored as an unsigned exponent byte
+ * (UE8M0, byte = e + 127); e = floor(log2(amax)) - emax, emax being the
+ * exponent of the element format's largest binade (8 for E4M3, 2 for E2M1),
+ * clamped to [-127, 127]; an all-zero block takes byte 127.  Each element is
+ * v / X rounded to nearest even in the element format, saturating to its
+ * largest magnitude (448, 6).  E2M1 (FP4): sign, 2 exponent bits (bias 1),
+ * 1 mantissa bit, magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; two codes per byte,
+ * the even element in the low nibble.  MXFP8 = E4M3 weights and
+ * activations; W4A8 = E2M1 weights and E4M3 activations.
+ */
+#define ORC_MX_BLOCK 32
+#define ORC_FMT_E4M3 0
+#define ORC_FMT_E2M1 1
+
+static const double orc_e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* fp32 -> E2M1 code: nearest representable magnitude, ties to the even code
+ * (mantissa bit 0), saturating to 6. */
+uint8_t orc_f32_to_e2m1(float xf) {
+    const double x = (double)xf;
+    const uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 0x8 : 0x0;
+    const double a = fabs(x);
+    if (!(a < 6.0)) return (uint8_t)(sign | 7);     /* also NaN: no NaN code */
+    int k = 0;
+    while (k < 7 && orc_e2m1_mag[k + 1] <= a) ++k;   /* mag[k] <= a < mag[k+1] */
+    if (a > orc_e2m1_mag[k]) {
+        const double mid = 0.5 * (orc_e2m1_mag[k] + orc_e2m1_mag[k + 1]);
+        if (a > mid || (a == mid && (k & 1))) ++k;
+    }
+    return (uint8_t)(sign | k);
+}
+
+float orc_e2m1_to_f32(uint8_t c) {
+    const double v = orc_e2m1_mag[c & 7];
+    return (float)((c & 8) ? -v : v);
+}
+
+/* the block exponent e of a block with largest magnitude amax */
+int orc_mx_block_exp(float amax, int fmt) {
+    if (!(amax > 0.0f)) return 0;
+    int e2;
+    frexp((double)amax, &e2);                        /* amax = f 2^e2, 0.5 <= f < 1 */
+    int e = (e2 - 1) - (fmt == ORC_FMT_E2M1 ? 2 : 8);
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* element k of an MX row as a double: codes (bytes, or packed nibbles) and
+ * block scale bytes */
+static double orc_mx_value(const uint8_t* q, const uint8_t* sc, int k, int fmt) {
+    const double x = orc_ldexp(1.0, (int)sc[k / ORC_MX_BLOCK] - 127);
+    if (fmt == ORC_FMT_E2M1) return orc_e2m1_to_f32((uint8_t)((q[k / 2] >> (4 * (k & 1))) & 15)) * x;
+    return orc_e4m3_to_f32(q[k]) * x;
+}
+
+/* one row of K values (bf16 bits, or fp32 when xf != NULL) -> MX codes + block scales */
+void oracle_mx_quantize_row(const uint16_t* xb, const float* xf, int K, int fmt, uint8_t* q,
+                            uint8_t* sc) {
+    if (fmt == ORC_FMT_E2M1) memset(q, 0, (size_t)K / 2);
+    for (int b = 0; b < K / ORC_MX_BLOCK; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < ORC_MX_BLOCK; ++i) {
+            const int k = b * ORC_MX_BLOCK + i;
+            const float v = fabsf(xf ? xf[k] : bf16_to_f32(xb[k]));
+            if (v > amax) amax = v;
+        }
+        const int e = orc_mx_block_exp(amax, fmt);
+        sc[b] = (uint8_t)(e + 127);
+        for (int i = 0; i < ORC_MX_BLOCK; ++i) {
+            const int k = b * ORC_MX_BLOCK + i;
+            const double v = (double)(xf ? xf[k] : bf16_to_f32(xb[k]));
+            const float r = (float)orc_ldexp(v, -e);     /* exact: a power-of-two scaling */
+            if (fmt == ORC_FMT_E2M1)
+                q[k / 2] |= (uint8_t)(orc_f32_to_e2m1(r) << (4 * (k & 1)));
+            else
+                q[k] = orc_f32_to_e4m3(r);
+        }
+    }
+}
+
+/* rows [n, K] bf16 -> codes [n, K] (E4M3) or [n, K/2] (E2M1) + scales [n, K/32] */
+void oracle_mx_quantize_rows(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* q,
+                             uint8_t* sc) {
+    const size_t qrow = fmt == ORC_FMT_E2M1 ? (size_t)K / 2 : (size_t)K;
+    for (int64_t r = 0; r < n; ++r)
+        oracle_mx_quantize_row(x + r * K, NULL, K, fmt, q + r * qrow, sc + r * (K / ORC_MX_BLOCK));
+}
+
+/*
+ * One routed row through one MX expert: x codes (E4M3) [H] with block scales
+ * [H/32]; W_gate / W_up [I, H] and W_down [H, I] in format wfmt with their
+ * block scales.  g = sum_h x_h w_h over the dequantized values (each
+ * product exact in double), rounded once to fp32; act = bf16(f(g, u)) (R15);
+ * the activation row is quantized to MX E4M3 (aq, as) and y = sum_i a_i d_i
+ * over the dequantized values, rounded once to fp32.
+ */
+void orc_ffn_row_mx(const uint8_t* xq, const uint8_t* xs, const uint8_t* wgq, const uint8_t* sg,
+                    const uint8_t* wuq, const uint8_t* su, const uint8_t* wdq, const uint8_t* sd,
+                    int wfmt, int H, int I, int act, uint16_t* act_out, uint8_t* aq,
+                    uint8_t* as, float* y_out) {
+    const size_t wrow_h = wfmt == ORC_FMT_E2M1 ? (size_t)H / 2 : (size_t)H;
+    const size_t wrow_i = wfmt == ORC_FMT_E2M1 ? (size_t)I / 2 : (size_t)I;
+    double* xv = (double*)malloc(sizeof(double) * (size_t)H);
+    float* actf = (float*)malloc(sizeof(float) * (size_t)I);
+    if (!xv || !actf) { free(xv); free(actf); return; }
+    for (int h = 0; h < H; ++h) xv[h] = orc_mx_value(xq, xs, h, ORC_FMT_E4M3);
+    for (int i = 0; i < I; ++i) {
+        const uint8_t *rg = wgq + (size_t)i * wrow_h, *ru = wuq + (size_t)i * wrow_h;
+        const uint8_t *rsg = sg + (size_t)i * (H / ORC_MX_BLOCK), *rsu = su + (size_t)i * (H / ORC_MX_BLOCK);
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            g += xv[h] * orc_mx_value(rg, rsg, h, wfmt);
+            u += xv[h] * orc_mx_value(ru, rsu, h, wfmt);
+        }
+        act_out[i] = f32_to_bf16((float)orc_act_value(act, (float)g, (float)u));
+        actf[i] = bf16_to_f32(act_out[i]);
+    }
+    oracle_mx_quantize_row(NULL, actf, I, ORC_FMT_E4M3, aq, as);
+    for (int h = 0; h < H; ++h) {
+        const uint8_t* rd = wdq + (size_t)h * wrow_i;
+        const uint8_t* rsd = sd + (size_t)h * (I / ORC_MX_BLOCK);
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i)
+            acc += orc_mx_value(aq, as, i, ORC_FMT_E4M3) * orc_mx_value(rd, rsd, i, wfmt);
+        y_out[h] = (float)acc;
+    }
+    free(xv);
+    free(actf);
+}
+
+typedef struct {
+    const uint8_t *xq, *xs, *wg, *sg, *wu, *su, *wd, *sd;
+    const int32_t *row_to_token, *row_expert;
+    int wfmt, H, I, act_kind;
+    uint16_t* act;
+    uint8_t *aq, *as;
+    float* y;
+} orc_ffnmx_ctx;
+
+static void orc_ffnmx_task(void* c_, int64_t r) {
+    orc_ffnmx_ctx* c = (orc_ffnmx_ctx*)c_;
+    const int64_t t = c->row_to_token[r];
+    const int64_t p = c->row_expert[r];
+    const int H = c->H, I = c->I;
+    const size_t wq = (size_t)H * I / (c->wfmt == ORC_FMT_E2M1 ? 2 : 1);
+    const size_t ws = (size_t)H * I / ORC_MX_BLOCK;
+    orc_ffn_row_mx(c->xq + (size_t)t * H, c->xs + (size_t)t * (H / ORC_MX_BLOCK), c->wg + p * wq,
+                   c->sg + p * ws, c->wu + p * wq, c->su + p * ws, c->wd + p * wq, c->sd + p * ws,
+                   c->wfmt, H, I, c->act_kind, c->act + (size_t)r * I, c->aq + (size_t)r * I,
+                   c->as + (size_t)r * (I / ORC_MX_BLOCK), c->y + (size_t)r * H);
+}
+
+/* Grouped MX MLP over the permuted rows: x codes [T, H] E4M3 + scales
+ * [T, H/32]; weights in format wfmt: codes [P, I, H(/2)] / [P, H, I(/2)],
+ * scales [P, I, H/32] / [P, H, I/32].  Outputs act bf16 [N, I], its MX E4M3
+ * codes [N, I] and scales [N, I/32], and y fp32 [N, H]. */
+void oracle_ffn_grouped_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* row_to_token,
+                           const int32_t* offsets, int P, int H, int I, int wfmt,
+                           const uint8_t* wg, const uint8_t* sg, const uint8_t* wu,
+                           const uint8_t* su, const uint8_t* wd, const uint8_t* sd, int act_kind,
+                           uint16_t* act, uint8_t* aq, uint8_t* as, float* y, int nthreads) {
+    int64_t N = offsets[P];
+    int32_t* row_expert = (int32_t*)malloc(sizeof(int32_t) * (N > 0 ? N : 1));
+    for (int p = 0; p < P; ++p)
+        for (int32_t r = offsets[p]; r < offsets[p + 1]; ++r) row_expert[r] = p;
+    orc_ffnmx_ctx c = {xq, xs, wg, sg, wu, su, wd, sd, row_to_token, row_expert, wfmt, H, I,
+                       act_kind, act, aq, as, y};
+    orc_parallel_for(N, nthreads, orc_ffnmx_task, &c);
     free(row_expert);
 }
