@@ -129,6 +129,19 @@ typedef struct gbmoe_layer {
     const float* s_up;            /* [E_phys, I] */
     const uint8_t* w_down_q;      /* [E_phys, H, I] */
     const float* s_down;          /* [E_phys, H] */
+    /* MX block-scaled routed experts (MXFP8 / W4A8, see moe_gemm_gateup_act_mx):
+     * when w_gate_mx is non-NULL (and w_gate_q is NULL) the routed expert MLP
+     * runs on these codes in format mx_format (GBMOE_MX_E4M3 or
+     * GBMOE_MX_E2M1) with UE8M0 scale bytes per 32 elements along K; hidden
+     * states and activations are MX E4M3 (quantized on the fly).  H % 256 ==
+     * 0.  The shared expert stays bf16. */
+    int mx_format;
+    const uint8_t* w_gate_mx;     /* [E_phys, I, H] (E4M3) or [E_phys, I, H/2] (E2M1) */
+    const uint8_t* sf_gate;       /* [E_phys, I, H/32] */
+    const uint8_t* w_up_mx;       /* as w_gate_mx */
+    const uint8_t* sf_up;         /* [E_phys, I, H/32] */
+    const uint8_t* w_down_mx;     /* [E_phys, H, I] (E4M3) or [E_phys, H, I/2] (E2M1) */
+    const uint8_t* sf_down;       /* [E_phys, H, I/32] */
 } gbmoe_layer;
 
 /* Text for a status code (static storage). */
@@ -355,6 +368,55 @@ int moe_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offsets
  */
 int moe_quantize_fp8_rows(const uint16_t* x, int64_t n, int K, uint8_t* q, float* scales,
                           gbmoe_stream_t stream);
+
+/*
+ * MX element formats (OCP Microscaling): E4M3 (one byte per element) or E2M1
+ * (FP4: sign, 2 exponent bits with bias 1, 1 mantissa bit; magnitudes 0, 0.5,
+ * 1, 1.5, 2, 3, 4, 6; two per byte, the even element in the low nibble).
+ */
+enum { GBMOE_MX_E4M3 = 0, GBMOE_MX_E2M1 = 1 };
+
+/*
+ * moe_quantize_mx_rows — MX block quantization of bf16 rows (reading of the
+ * "Stage 4" quantized paths MXFP / W4A8): every row is cut into blocks of 32
+ * consecutive elements; block b of row r gets the scale 2^e,
+ *   e = floor(log2(amax of the block)) - emax  (emax = 8 for E4M3, 2 for E2M1),
+ *   clamped to [-127, 127] (e = 0 for an all-zero block), stored as the byte
+ *   scales[r, b] = e + 127 (UE8M0), and each element x becomes the code of
+ *   x * 2^-e rounded to nearest even with saturation (448 / 6).
+ *   x [n, K] bf16, 16-byte aligned, K a multiple of 32 (else UNSUPPORTED);
+ *   q [n, K] (E4M3) or [n, K/2] (E2M1) uint8, 16-byte aligned; scales
+ *   [n, K/32] uint8.  fmt: GBMOE_MX_E4M3 or GBMOE_MX_E2M1.
+ */
+int moe_quantize_mx_rows(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* q,
+                         uint8_t* scales, gbmoe_stream_t stream);
+
+/*
+ * moe_gemm_gateup_act_mx / moe_gemm_down_mx — the grouped GEMMs with MX
+ * block-scaled operands on the tensor cores (tcgen05 kind::mxf8f6f4 with
+ * block scales): weights in format w_fmt (E4M3: MXFP8; E2M1: W4A8), tokens
+ * and activations in MX E4M3.  With dequantized values (code * 2^e of its
+ * block):
+ *   g = sum_h x[t,h] wg[p,i,h], u likewise (fp32 accumulation),
+ *   act = bf16(f(g, u)) quantized to MX E4M3 along I: act_q [N, I] codes and
+ *   act_s [N, I/32] scale bytes, the same definition as moe_quantize_mx_rows
+ *   (the quantization is fused into the GEMM's epilogue);
+ *   y[r, h] = sum_i a[r,i] wd[p,h,i]  (fp32).
+ *   xq [T or N, H] codes + xs [T or N, H/32] (t = row_to_token[r], or r with
+ *   row_to_token NULL); wgq / wuq [E_phys, I, H or H/2] + sg / su
+ *   [E_phys, I, H/32]; aq [N, I] + as [N, I/32]; wdq [E_phys, H, I or I/2] +
+ *   sd [E_phys, H, I/32].  H % 256 == 0, I % 128 == 0 (else UNSUPPORTED);
+ *   code arrays 16-byte aligned (E2M1 weights 32-byte aligned), scale arrays
+ *   4-byte aligned.
+ */
+int moe_gemm_gateup_act_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* row_to_token,
+                           int T, const int32_t* offsets, int E_phys, int N, int H, int I,
+                           int w_fmt, const uint8_t* wgq, const uint8_t* sg, const uint8_t* wuq,
+                           const uint8_t* su, int activation, uint8_t* act_q, uint8_t* act_s,
+                           gbmoe_stream_t stream);
+int moe_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* offsets, int E_phys,
+                     int N, int H, int I, int w_fmt, const uint8_t* wdq, const uint8_t* sd,
+                     float* y, gbmoe_stream_t stream);
 
 /*
  * moe_latent_tail — the post-MoE tail of a latent MoE on one GPU (the NVIDIA

@@ -18,12 +18,14 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import ACTIVATION, ACT_SWIGLU, GROUP, SCORE, Layer, RouteCfg
+from ._lib import ACTIVATION, ACT_SWIGLU, GROUP, MX_FORMAT, SCORE, Layer, RouteCfg
 
 __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_permute",
            "moe_gemm_gateup_act", "moe_gemm_gateup_act_rows", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
            "moe_combine", "moe_quantize_fp8_rows",
-           "moe_gemm_gateup_act_fp8", "moe_gemm_down_fp8", "quantize_experts_fp8", "moe_latent_tail", "MoELayer", "moe_forward",
+           "moe_gemm_gateup_act_fp8", "moe_gemm_down_fp8", "quantize_experts_fp8",
+           "moe_quantize_mx_rows", "moe_gemm_gateup_act_mx", "moe_gemm_down_mx",
+           "quantize_experts_mx", "moe_latent_tail", "MoELayer", "moe_forward",
            "moe_forward_host", "check_device_status", "library"]
 
 
@@ -270,6 +272,71 @@ def quantize_experts_fp8(w, stream=None):
     return q.reshape(E, R, K), sc.reshape(E, R)
 
 
+def _mx(fmt) -> int:
+    return MX_FORMAT[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def moe_quantize_mx_rows(x, fmt="e4m3", q=None, scales=None, stream=None):
+    """bf16 rows [n, K] -> MX codes (uint8 [n, K] for E4M3, [n, K/2] packed E2M1)
+    and UE8M0 block-scale bytes uint8 [n, K/32] (blocks of 32 along K)."""
+    lib = _lib.load()
+    n, K = x.shape
+    f = _mx(fmt)
+    if q is None:
+        q = torch.empty((n, K // 2 if f == MX_FORMAT["e2m1"] else K), dtype=torch.uint8,
+                        device=x.device)
+    if scales is None:
+        scales = torch.empty((n, K // 32), dtype=torch.uint8, device=x.device)
+    _check(lib.moe_quantize_mx_rows(_ptr(x), n, K, f, _ptr(q), _ptr(scales), _stream(stream)),
+           "moe_quantize_mx_rows")
+    return q, scales
+
+
+def quantize_experts_mx(w, fmt="e4m3", stream=None):
+    """bf16 expert weights [E, R, K] -> (MX codes [E, R, K or K/2], scale bytes
+    [E, R, K/32]) with moe_quantize_mx_rows."""
+    E, R, K = w.shape
+    q, sc = moe_quantize_mx_rows(w.reshape(E * R, K), fmt, stream=stream)
+    return q.reshape(E, R, -1), sc.reshape(E, R, K // 32)
+
+
+def moe_gemm_gateup_act_mx(xq, xs, offsets, wgq, sg, wuq, su, w_fmt="e4m3", row_to_token=None,
+                           act_q=None, act_s=None, activation="swiglu", stream=None):
+    """MX gate/up GEMM: act = bf16(f(x wg^T, x wu^T)) over the dequantized MX
+    operands, returned quantized to MX E4M3: (codes uint8 [N, I], scale bytes
+    [N, I/32]).  xq [T, H] codes + xs [T, H/32] gathered through row_to_token
+    [N] (or the N permuted rows); weights in format w_fmt."""
+    lib = _lib.load()
+    P, I = wgq.shape[0], wgq.shape[1]
+    H = xq.shape[1]
+    if row_to_token is None:
+        N, T = xq.shape[0], 0
+    else:
+        N, T = row_to_token.shape[0], xq.shape[0]
+    if act_q is None:
+        act_q = torch.empty((N, I), dtype=torch.uint8, device=xq.device)
+    if act_s is None:
+        act_s = torch.empty((N, I // 32), dtype=torch.uint8, device=xq.device)
+    _check(lib.moe_gemm_gateup_act_mx(_ptr(xq), _ptr(xs), _ptr(row_to_token), T, _ptr(offsets),
+                                      P, N, H, I, _mx(w_fmt), _ptr(wgq), _ptr(sg), _ptr(wuq),
+                                      _ptr(su), _act(activation), _ptr(act_q), _ptr(act_s),
+                                      _stream(stream)), "moe_gemm_gateup_act_mx")
+    return act_q, act_s
+
+
+def moe_gemm_down_mx(aq, as_, offsets, wdq, sd, w_fmt="e4m3", y=None, stream=None):
+    """MX down GEMM: y = a . wd^T over the dequantized MX operands, fp32 [N, H]."""
+    lib = _lib.load()
+    N, I = aq.shape
+    P, H = wdq.shape[0], wdq.shape[1]
+    if y is None:
+        y = torch.empty((N, H), dtype=torch.float32, device=aq.device)
+    _check(lib.moe_gemm_down_mx(_ptr(aq), _ptr(as_), _ptr(offsets), P, N, H, I, _mx(w_fmt),
+                                _ptr(wdq), _ptr(sd), _ptr(y), _stream(stream)),
+           "moe_gemm_down_mx")
+    return y
+
+
 def moe_latent_tail(latent, up_proj, norm_w=None, eps=1e-6, shared=None, out=None, ws=None,
                     stream=None):
     """out = bf16(rmsnorm(latent) . up_proj^T + shared): the latent-MoE tail on
@@ -301,16 +368,23 @@ class MoELayer:
 
     def __init__(self, cfg: RouteCfg, w_router, w_gate, w_up, w_down, router_bias=None,
                  corr_bias=None, tid2eid=None, log2phy=None, replica_cnt=None, shared=None,
-                 activation="swiglu", fp8=None):
+                 activation="swiglu", fp8=None, mx=None):
         """fp8 = (w_gate_q, s_gate, w_up_q, s_up, w_down_q, s_down): FP8 routed
         experts (E4M3 codes uint8 [E_phys, I, H] / [E_phys, H, I] and fp32
         per-row scales, e.g. from quantize_experts_fp8); the bf16 w_gate / w_up /
-        w_down may then be None."""
+        w_down may then be None.
+        mx = (fmt, w_gate_mx, sf_gate, w_up_mx, sf_up, w_down_mx, sf_down): MX
+        block-scaled routed experts ("e4m3" or "e2m1" codes and UE8M0 scale
+        bytes per 32 elements along K, e.g. from quantize_experts_mx)."""
         self.cfg = cfg
         self._keep = [w_router, w_gate, w_up, w_down, router_bias, corr_bias, tid2eid, log2phy,
-                      replica_cnt] + list(shared or []) + list(fp8 or [])
-        ref = w_gate if w_gate is not None else fp8[0]
-        P, I, H = ref.shape
+                      replica_cnt] + list(shared or []) + list(fp8 or []) + list(mx or [])[1:]
+        if w_gate is not None:
+            (P, I, H), ref = w_gate.shape, w_gate
+        elif fp8 is not None:
+            (P, I, H), ref = fp8[0].shape, fp8[0]
+        else:  # MX: H from the scale bytes (the codes of E2M1 hold H/2 bytes)
+            (P, I), H, ref = mx[1].shape[:2], mx[2].shape[2] * 32, mx[1]
         Is = 0 if shared is None else shared[0].shape[0]
         self.H, self.I, self.I_shared = H, I, Is
         self.device = ref.device
@@ -319,7 +393,8 @@ class MoELayer:
                        _ptr(tid2eid), 0 if tid2eid is None else tid2eid.shape[0], _ptr(log2phy),
                        _ptr(replica_cnt), 1 if log2phy is None else log2phy.shape[1],
                        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(s[0]), _ptr(s[1]),
-                       _ptr(s[2]), _act(activation), *[_ptr(a) for a in (fp8 or [None] * 6)])
+                       _ptr(s[2]), _act(activation), *[_ptr(a) for a in (fp8 or [None] * 6)],
+                       _mx(mx[0]) if mx else 0, *[_ptr(a) for a in (mx[1:] if mx else [None] * 6)])
         self._ws = None
 
     def workspace_size(self, T_max: int, host: bool = False) -> int:

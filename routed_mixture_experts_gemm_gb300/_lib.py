@@ -14,6 +14,7 @@ SCORE = {"softmax": 0, "sigmoid": 1, "sqrtsoftplus": 2}
 GROUP = {"max": 0, "top2sum": 1}
 ACT_SWIGLU = 0
 ACTIVATION = {"swiglu": 0, "swiglu_oai": 1, "geglu": 2, "geglu_tanh": 3}
+MX_FORMAT = {"e4m3": 0, "e2m1": 1}
 
 # every function the header declares, with (restype, argtypes)
 _vp, _i, _i64, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -32,7 +33,9 @@ class Layer(ctypes.Structure):
                 ("replica_cnt", _vp), ("R_max", _i), ("w_gate", _vp), ("w_up", _vp),
                 ("w_down", _vp), ("w_gate_shared", _vp), ("w_up_shared", _vp),
                 ("w_down_shared", _vp), ("activation", _i), ("w_gate_q", _vp), ("s_gate", _vp),
-                ("w_up_q", _vp), ("s_up", _vp), ("w_down_q", _vp), ("s_down", _vp)]
+                ("w_up_q", _vp), ("s_up", _vp), ("w_down_q", _vp), ("s_down", _vp),
+                ("mx_format", _i), ("w_gate_mx", _vp), ("sf_gate", _vp), ("w_up_mx", _vp),
+                ("sf_up", _vp), ("w_down_mx", _vp), ("sf_down", _vp)]
 
 
 _P = ctypes.POINTER
@@ -59,6 +62,10 @@ SIGNATURES = {
     "moe_gemm_gateup_act_fp8": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                                      _i, _vp, _vp]),
     "moe_gemm_down_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "moe_quantize_mx_rows": (_i, [_vp, _i64, _i, _i, _vp, _vp, _vp]),
+    "moe_gemm_gateup_act_mx": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
+                                    _vp, _i, _vp, _vp, _vp]),
+    "moe_gemm_down_mx": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "gbmoe_latent_tail_workspace_size": (_sz, [_i, _i, _i]),
     "moe_latent_tail": (_i, [_vp, _i, _i, _vp, ctypes.c_float, _vp, _i, _vp, _vp, _vp, _sz,
                              _vp]),

@@ -30,6 +30,11 @@ constexpr int kMaxGroups = 32;
 bool valid_activation(int a) { return a >= GBMOE_ACT_SWIGLU && a <= GBMOE_ACT_GEGLU_TANH; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+// E2M1 weights are read by 32-byte-aligned tensor copies
+inline bool mx_weights_aligned(int fmt, const void* p) {
+    return (reinterpret_cast<uintptr_t>(p) & (fmt == GBMOE_MX_E2M1 ? 31u : 15u)) == 0;
+}
 inline size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 int status_from(cudaError_t e) { return e == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA; }
@@ -71,8 +76,9 @@ struct FwdWs {
     void* perm;
     uint16_t *act, *act_s;
     float *y, *ys;
-    uint8_t *xq, *aq;  // FP8 layers: hidden-state and activation codes
-    float *sx, *sa;    // and their per-row scales
+    uint8_t *xq, *aq;  // FP8 / MX layers: hidden-state and activation codes
+    float *sx, *sa;    // and their per-row scales (FP8)
+    uint8_t *xs, *as;  // or block-scale bytes (MX)
     size_t bytes;
 };
 
@@ -96,10 +102,13 @@ FwdWs layout_fwd(const gbmoe_layer* L, int T, void* ws) {
     f.act_s = w.take<uint16_t>(static_cast<size_t>(T) * L->I_shared);
     f.ys = w.take<float>(L->I_shared ? static_cast<size_t>(T) * L->H : 0);
     const bool fp8 = L->w_gate_q != nullptr;
-    f.xq = w.take<uint8_t>(fp8 ? static_cast<size_t>(T) * L->H : 0);
+    const bool mx = !fp8 && L->w_gate_mx != nullptr;
+    f.xq = w.take<uint8_t>(fp8 || mx ? static_cast<size_t>(T) * L->H : 0);
     f.sx = w.take<float>(fp8 ? static_cast<size_t>(T) : 0);
-    f.aq = w.take<uint8_t>(fp8 ? N * L->I : 0);
+    f.aq = w.take<uint8_t>(fp8 || mx ? N * L->I : 0);
     f.sa = w.take<float>(fp8 ? N : 0);
+    f.xs = w.take<uint8_t>(mx ? static_cast<size_t>(T) * (L->H / 32) : 0);
+    f.as = w.take<uint8_t>(mx ? N * (L->I / 32) : 0);
     f.bytes = w.off;
     return f;
 }
@@ -116,6 +125,17 @@ int check_layer(const gbmoe_layer* L) {
         if (!L->w_up_q || !L->w_down_q || !L->s_gate || !L->s_up || !L->s_down)
             return GBMOE_ERR_INVALID_ARG;
         if (!aligned16(L->w_gate_q) || !aligned16(L->w_up_q) || !aligned16(L->w_down_q))
+            return GBMOE_ERR_INVALID_ARG;
+        if (L->H % 256) return GBMOE_ERR_UNSUPPORTED;
+    } else if (L->w_gate_mx) {  // MX block-scaled routed experts
+        if (!L->w_up_mx || !L->w_down_mx || !L->sf_gate || !L->sf_up || !L->sf_down)
+            return GBMOE_ERR_INVALID_ARG;
+        if (L->mx_format != GBMOE_MX_E4M3 && L->mx_format != GBMOE_MX_E2M1)
+            return GBMOE_ERR_UNSUPPORTED;
+        if (!mx_weights_aligned(L->mx_format, L->w_gate_mx) ||
+            !mx_weights_aligned(L->mx_format, L->w_up_mx) ||
+            !mx_weights_aligned(L->mx_format, L->w_down_mx) || !aligned4(L->sf_gate) ||
+            !aligned4(L->sf_up) || !aligned4(L->sf_down))
             return GBMOE_ERR_INVALID_ARG;
         if (L->H % 256) return GBMOE_ERR_UNSUPPORTED;
     } else {
@@ -425,6 +445,63 @@ int moe_quantize_fp8_rows(const uint16_t* x, int64_t n, int K, uint8_t* q, float
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_quantize_mx_rows(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* q,
+                         uint8_t* scales, gbmoe_stream_t stream) {
+    if (n < 0 || K <= 0) return GBMOE_ERR_INVALID_ARG;
+    if (fmt != GBMOE_MX_E4M3 && fmt != GBMOE_MX_E2M1) return GBMOE_ERR_UNSUPPORTED;
+    if (K % 32) return GBMOE_ERR_UNSUPPORTED;
+    if (n == 0) return GBMOE_OK;
+    if (!x || !q || !scales || !aligned16(x) || !aligned16(q)) return GBMOE_ERR_INVALID_ARG;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return status_from(launch_mx_quantize(x, n, K, fmt, q, scales, *ctx,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_gemm_gateup_act_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* row_to_token,
+                           int T, const int32_t* offsets, int E_phys, int N, int H, int I,
+                           int w_fmt, const uint8_t* wgq, const uint8_t* sg, const uint8_t* wuq,
+                           const uint8_t* su, int activation, uint8_t* act_q, uint8_t* act_s,
+                           gbmoe_stream_t stream) {
+    if (!valid_activation(activation)) return GBMOE_ERR_UNSUPPORTED;
+    if (w_fmt != GBMOE_MX_E4M3 && w_fmt != GBMOE_MX_E2M1) return GBMOE_ERR_UNSUPPORTED;
+    if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
+    if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
+    if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
+    if (H % 256 || I % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (N == 0) return GBMOE_OK;
+    if (row_to_token && T < 1) return GBMOE_ERR_INVALID_ARG;
+    if (!xq || !xs || !wgq || !sg || !wuq || !su || !act_q || !act_s)
+        return GBMOE_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !mx_weights_aligned(w_fmt, wgq) || !mx_weights_aligned(w_fmt, wuq) ||
+        !aligned4(xs) || !aligned4(sg) || !aligned4(su))
+        return GBMOE_ERR_INVALID_ARG;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return launch_gemm_gateup_mx(xq, xs, row_to_token, row_to_token ? T : N, offsets, E_phys, N,
+                                 H, I, w_fmt, wgq, sg, wuq, su, activation, act_q, act_s, *ctx,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* offsets, int E_phys,
+                     int N, int H, int I, int w_fmt, const uint8_t* wdq, const uint8_t* sd,
+                     float* y, gbmoe_stream_t stream) {
+    if (w_fmt != GBMOE_MX_E4M3 && w_fmt != GBMOE_MX_E2M1) return GBMOE_ERR_UNSUPPORTED;
+    if (N < 0 || H <= 0 || I <= 0 || E_phys < 1) return GBMOE_ERR_INVALID_ARG;
+    if (E_phys > gemm_max_groups()) return GBMOE_ERR_UNSUPPORTED;
+    if (!offsets && E_phys != 1) return GBMOE_ERR_INVALID_ARG;
+    if (H % 256 || I % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (N == 0) return GBMOE_OK;
+    if (!aq || !as || !wdq || !sd || !y) return GBMOE_ERR_INVALID_ARG;
+    if (!aligned16(aq) || !mx_weights_aligned(w_fmt, wdq) || !aligned4(as) || !aligned4(sd) ||
+        !aligned16(y))
+        return GBMOE_ERR_INVALID_ARG;
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return launch_gemm_down_mx(aq, as, offsets, E_phys, N, H, I, w_fmt, wdq, sd, y, *ctx,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t gbmoe_latent_tail_workspace_size(int T, int L, int Hm) {
     if (T < 0 || L <= 0 || Hm <= 0) return 0;
     return latent_tail_ws_bytes(T, L, Hm);
@@ -503,6 +580,18 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
         if (st) return st;
         st = launch_gemm_down_fp8(f.aq, f.sa, f.offsets, c.E_phys, N, L->H, L->I, L->w_down_q,
                                   L->s_down, f.y, *ctx, s);
+        if (st) return st;
+    } else if (L->w_gate_mx) {
+        // MX routed experts: hidden states quantized per 32-element block; the
+        // gate/up GEMM writes the activation already quantized
+        st = status_from(launch_mx_quantize(x, T, L->H, GBMOE_MX_E4M3, f.xq, f.xs, *ctx, s));
+        if (st) return st;
+        st = launch_gemm_gateup_mx(f.xq, f.xs, f.row_to_token, T, f.offsets, c.E_phys, N, L->H,
+                                   L->I, L->mx_format, L->w_gate_mx, L->sf_gate, L->w_up_mx,
+                                   L->sf_up, L->activation, f.aq, f.as, *ctx, s);
+        if (st) return st;
+        st = launch_gemm_down_mx(f.aq, f.as, f.offsets, c.E_phys, N, L->H, L->I, L->mx_format,
+                                 L->w_down_mx, L->sf_down, f.y, *ctx, s);
         if (st) return st;
     } else if (gemm_fused_eligible(c.E_phys, N, L->H)) {
         st = launch_gemm_mlp_fused(x, f.row_to_token, T, f.offsets, c.E_phys, N, L->H, L->I,

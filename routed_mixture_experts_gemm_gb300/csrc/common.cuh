@@ -169,6 +169,22 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= (A . B^T) with per-32-element block scales (kind::mxf8f6f4
+// block_scale, one UE8M0 scale per 32 K-elements of every A row and B row):
+// A and B in E4M3 or E2M1 (one byte per element in shared memory), 32
+// K-elements per instruction, fp32 accumulate.  sfa / sfb are the TMEM
+// addresses of the scale columns; the byte of each 32-bit column used by this
+// instruction is selected in the instruction descriptor.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+}
 // Arrive once on `bar` when all previously issued tcgen05 ops of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile(
@@ -188,6 +204,23 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 }
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// 32 TMEM lanes x 4 / 8 consecutive 32-bit columns from registers; thread i
+// of the warp writes lane (base+i).
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major bf16 tile stored as rows of
@@ -217,6 +250,36 @@ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
 __device__ __forceinline__ uint32_t idesc_e4m3_f32(int M, int N) {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// two fp32 values -> two OCP FP8 E4M3 codes (round to nearest even,
+// saturating to +-448), the first in the low byte
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// MX element formats (argument values of the C ABI)
+constexpr int kMxE4M3 = 0, kMxE2M1 = 1;
+// Shared exponent of an MX block with largest magnitude amax >= 0:
+// floor(log2(amax)) - emax clamped to [-127, 127] (0 for an all-zero block),
+// floor(log2) read from the fp32 bits (subnormals by their leading one).
+__device__ __forceinline__ int mx_block_exp(float amax, int emax) {
+    const uint32_t b = __float_as_uint(amax);
+    if (b == 0u) return 0;
+    const int be = static_cast<int>(b >> 23);
+    const int l = be ? be - 127 : (31 - __clz(static_cast<int>(b))) - 149;
+    return min(127, max(-127, l - emax));
+}
+// Instruction descriptor, kind::mxf8f6f4 with block scales: A type a_fmt, B
+// type b_fmt (0 = E4M3, 5 = E2M1), both K-major, UE8M0 scales (bit 23);
+// bits 4-5 and 29-30 select the byte of the B and A scale columns (the
+// 32-element K block within a group of four).
+__device__ __forceinline__ uint32_t idesc_mx(int M, int N, uint32_t a_fmt, uint32_t b_fmt,
+                                             uint32_t sf_byte) {
+    return (sf_byte << 4) | (a_fmt << 7) | (b_fmt << 10) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | (sf_byte << 29);
 }
 
 }  // namespace gbmoe

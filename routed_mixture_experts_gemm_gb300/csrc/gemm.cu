@@ -82,14 +82,24 @@ constexpr int kSwiGLU = 0, kDown = 1, kDownPair = 2, kFused = 3;
 // Shared memory: a ring of SA weight stages (NUM_A boxes of 128 rows x BK)
 // and a ring of SB token stages (up to BN rows x BK); EB bytes per element
 // (2: bf16, 1: FP8 E4M3), a stage row is BK * EB = 128 (or 64) bytes.
-template <int NUM_A, int BN, int SA, int SB, int ACC_BUFS, int BK, int EB = 2>
+//
+// MX block scales (MXS = 1): TMEM holds, after the accumulators, one group
+// of scale columns per token stage: 4 columns per A operand and BN/32 for the
+// token rows.  Column j of a group holds, in lane r of every lane quarter,
+// the four scale bytes (the stage's four 32-element K blocks, byte b = block
+// b) of row 32j + r of that operand.
+template <int NUM_A, int BN, int SA, int SB, int ACC_BUFS, int BK, int EB = 2, int MXS = 0>
 struct Layout {
     static constexpr int ROW_BYTES = BK * EB;
     static constexpr int A_BYTES = BM * ROW_BYTES;
     static constexpr int A_STAGE = NUM_A * A_BYTES;
     static constexpr int B_BYTES = BN * ROW_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
-    static constexpr int TMEM_COLS = ACC_BUFS * ACC_COLS;
+    static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
+    static constexpr int SFB_COLS = BN / 32;
+    static constexpr int SF_STAGE_COLS = NUM_A * 4 + SFB_COLS;
+    static constexpr int TMEM_USED = SF_BASE + (MXS ? SB * SF_STAGE_COLS : 0);
+    static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static constexpr int TABLE_INTS = MAX_GROUPS + 4;
     static constexpr int OFF_B = SA * A_STAGE;
     static constexpr int OFF_TBS = OFF_B + SB * B_BYTES;      // prefix of token blocks
@@ -101,7 +111,8 @@ struct Layout {
     static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
     static constexpr int END = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
-    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of 2");
+    static_assert(TMEM_USED <= 512 && (MXS || TMEM_USED == TMEM_COLS), "TMEM columns");
+    static_assert(!MXS || (EB == 1 && BK == 128), "MX stages hold four 32-element K blocks");
     static_assert(A_STAGE % 1024 == 0 && B_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(ROW_BYTES == 128 || (EB == 2 && ROW_BYTES == 64),
                   "stage K is one 128- or 64-byte swizzled row");
@@ -136,6 +147,17 @@ struct GemmArgs {
     const float* tok_scale;
     const float* w_scale0;
     const float* w_scale1;
+    // MX block scales (UE8M0 bytes, one per 32 K-elements of a row; null
+    // otherwise): of the token operand [rows, K/32] (rows of gather_src, or of
+    // the operand), of the weights (w_sf0: gate / down, w_sf1: up), and of the
+    // activation the gate/up epilogue writes quantized (out_sf [n_rows, R/32];
+    // out then holds its E4M3 codes [n_rows, R]); a_fmt: the weights' type
+    // code in the instruction descriptor (0 E4M3, 5 E2M1)
+    const uint8_t* tok_sf;
+    const uint8_t* w_sf0;
+    const uint8_t* w_sf1;
+    uint8_t* out_sf;
+    uint32_t a_fmt;
 };
 
 // The second GEMM of the fused mode (paired down tiles) and the per-group
@@ -264,7 +286,8 @@ __device__ __forceinline__ float gated_act(int act, float g, float u) {
     }
 }
 
-template <int NUM_A, int BN, int SA, int SB, int MODE, int ACC_BUFS, int BK, int EB = 2>
+template <int NUM_A, int BN, int SA, int SB, int MODE, int ACC_BUFS, int BK, int EB = 2,
+          int MXS = 0>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__ GemmMaps m2,
                     const GemmArgs args, const FusedArgs fz) {
@@ -272,7 +295,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     constexpr int MODE1 = FUSED ? kSwiGLU : MODE;  // mode of the first GEMM's tiles
     static_assert(MODE1 != kDown || NUM_A == 1, "down tiles have one A operand");
     static_assert(MODE1 == kDown || NUM_A == 2, "gate/up and paired tiles have two");
-    using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK, EB>;
+    using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK, EB, MXS>;
     static_assert(EB == 2 || !FUSED, "the FP8 path runs its GEMMs as two launches");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -402,6 +425,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const int KB = (second ? fz.K : args.K) / BK;
             const int a_row = tl.p * R + tl.rblk * (mode == kDownPair ? 2 * BM : BM);
             const uint64_t pol_w = token_blocks(gcnt[tl.p], BN) > 1 ? pol_shared : pol_once;
+            // an E2M1 box lands as one byte per element (16 codes in the first
+            // 8 bytes of every 16) but completes with its packed size
+            const uint32_t a_tx = (MXS && args.a_fmt == 5u) ? L::A_BYTES / 2 : L::A_BYTES;
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait_bounded(aempty + stage, phase ^ 1u, abort_flag, args.status,
@@ -409,7 +435,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(afull + stage, NUM_A * L::A_BYTES);
+                mbar_arrive_expect_tx(afull + stage, NUM_A * a_tx);
                 uint8_t* sA = smem + stage * L::A_STAGE;
                 tma_load_2d(sA, &m.a0, afull + stage, kb * BK, a_row, pol_w);
                 if (mode == kSwiGLU)
@@ -449,7 +475,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         static_assert(BN % RSTEP == 0, "loader rows");
         const uint64_t pol_x = l2_policy_evict_last();
         // without gathered rows the lead thread alone streams the B ring
-        const bool solo = args.gather_rows == nullptr;
+        // (with MX block scales every loader warp writes the scale columns of
+        // its TMEM lane quarter)
+        const bool solo = args.gather_rows == nullptr && !MXS;
+        const uint32_t sf_lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const int kq = args.K / 32;     // scale bytes per row
         auto all_agree = [&](bool v) { return solo ? v : loader_bar_all(v); };
         int stage = 0;
         uint32_t phase = 0;
@@ -460,7 +490,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             bool second;
             Tile tl;
             job(tau, second, tl);
-            const bool gather = !second && !solo && L::ROW_BYTES == 128;
+            const bool gather = !second && args.gather_rows != nullptr && L::ROW_BYTES == 128;
             if (FUSED && second) {
                 // publish a pending gathered stage before waiting: the MMA
                 // needs it to finish the very gate/up tiles waited for
@@ -514,7 +544,48 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     }
                 }
             }
+            // MX: the scale rows of this lane (row 32j + lane of each operand)
+            int64_t sfa_row[NUM_A], sfb_row[L::SFB_COLS];
+            if (MXS) {
+                const int a_row = tl.p * args.R + tl.rblk * WROWS1;
+#pragma unroll
+                for (int a = 0; a < NUM_A; ++a)
+                    sfa_row[a] = a_row + (MODE1 == kDownPair ? a * BM : 0) + lane;
+#pragma unroll
+                for (int j = 0; j < L::SFB_COLS; ++j) {
+                    const int n = 32 * j + lane;
+                    sfb_row[j] = -1;
+                    if (n < tl.n_valid) {
+                        int t = tl.row0 + n;
+                        if (args.gather_rows) {
+                            t = args.gather_rows[t];
+                            if (t < 0 || t >= args.src_rows) {
+                                record_error(args.status, GBMOE_ERR_DEVICE);
+                                t = 0;
+                            }
+                        }
+                        sfb_row[j] = t;
+                    }
+                }
+            }
             for (int kb = 0; kb < KB; ++kb) {
+                // MX: this stage's scale bytes (loaded before waiting for the slot)
+                uint32_t sfa[NUM_A][4], sfb[L::SFB_COLS];
+                if (MXS) {
+#pragma unroll
+                    for (int a = 0; a < NUM_A; ++a) {
+                        const uint8_t* w = (MODE1 == kSwiGLU && a == 1) ? args.w_sf1 : args.w_sf0;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            sfa[a][j] = __ldg(reinterpret_cast<const uint32_t*>(
+                                w + (sfa_row[a] + 32 * j) * kq + kb * 4));
+                    }
+#pragma unroll
+                    for (int j = 0; j < L::SFB_COLS; ++j)
+                        sfb[j] = sfb_row[j] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(
+                                                       args.tok_sf + sfb_row[j] * kq + kb * 4))
+                                                 : 0x7f7f7f7fu;
+                }
                 bool free_ok = true;
                 if (lead)
                     free_ok = mbar_wait_bounded(bempty + stage, phase ^ 1u, abort_flag,
@@ -522,6 +593,24 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 if (!all_agree(free_ok)) {
                     ok = false;
                     break;
+                }
+                if (MXS) {
+                    // write the scale columns of this slot (every lane quarter
+                    // holds the same copy) and order them before the slot is
+                    // published: through the loaders' barrier to the lead
+                    // thread's arrive (TMA rows), or to the next stage's
+                    // publishing barrier (gathered rows)
+                    const uint32_t t =
+                        tmem_base + L::SF_BASE + stage * L::SF_STAGE_COLS + sf_lane;
+#pragma unroll
+                    for (int a = 0; a < NUM_A; ++a) tmem_st_32x32b_x4(t + 4 * a, sfa[a]);
+                    if constexpr (L::SFB_COLS == 4)
+                        tmem_st_32x32b_x4(t + 4 * NUM_A, sfb);
+                    else
+                        tmem_st_32x32b_x8(t + 4 * NUM_A, sfb);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    if (!gather) loader_bar_all(true);
                 }
                 uint8_t* sB = smem + L::OFF_B + stage * L::B_BYTES;
                 if (gather) {
@@ -591,7 +680,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             job(tau, second, tl);
             const int KB = (second ? fz.K : args.K) / BK;
             const int n_mma = ((tl.n_valid + 15) / 16) * 16;
-            const uint32_t idesc = EB == 2 ? idesc_bf16_f32(BM, n_mma) : idesc_e4m3_f32(BM, n_mma);
+            const uint32_t idesc = MXS ? idesc_mx(BM, n_mma, args.a_fmt, 0u, 0u)
+                                 : EB == 2 ? idesc_bf16_f32(BM, n_mma) : idesc_e4m3_f32(BM, n_mma);
             if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, args.status,
                                    kWaitLimitNs))
                 break;
@@ -607,6 +697,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 tc_fence_after();
                 const uint32_t sA = smem_u32(smem + as * L::A_STAGE);
                 const uint32_t sB = smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
+                const uint32_t sf = tmem_base + L::SF_BASE + bs * L::SF_STAGE_COLS;
                 // one MMA covers 32 bytes of K (16 bf16 or 32 FP8 elements)
 #pragma unroll
                 for (int ks = 0; ks < L::ROW_BYTES / 32; ++ks) {
@@ -615,7 +706,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     for (int a = 0; a < NUM_A; ++a) {
                         const uint64_t adesc =
                             smem_desc_kmajor<L::ROW_BYTES / 2>(sA + a * L::A_BYTES + ks * 32);
-                        if (EB == 2)
+                        if (MXS)
+                            umma_mx(d0 + a * BN, adesc, bdesc,
+                                    idesc | (static_cast<uint32_t>(ks) << 4) |
+                                        (static_cast<uint32_t>(ks) << 29),
+                                    sf + 4 * a, sf + 4 * NUM_A, (kb > 0 || ks > 0) ? 1u : 0u);
+                        else if (EB == 2)
                             umma_bf16(d0 + a * BN, adesc, bdesc, idesc,
                                       (kb > 0 || ks > 0) ? 1u : 0u);
                         else
@@ -665,7 +761,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             tc_fence_after();
             const int mode = second ? kDownPair : MODE1;
             const bool swiglu = mode == kSwiGLU;
-            const int out_elem = swiglu ? 2 : 4;
+            const bool quant_out = MXS && swiglu;  // MX E4M3 activation codes + scales
+            const int out_elem = quant_out ? 1 : swiglu ? 2 : 4;
             const int R = second ? fz.R : args.R;
             uint8_t* outp = static_cast<uint8_t*>(second ? static_cast<void*>(fz.out) : args.out);
             const int wrows = mode == kDownPair ? 2 * BM : BM;
@@ -687,7 +784,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     gv[c] = __uint_as_float(g[c]);
                     uv[c] = swiglu ? __uint_as_float(u[c]) : 0.0f;
                 }
-                if (EB == 1) {
+                if (EB == 1 && !MXS) {
                     // FP8 operands: (acc * token scale) * weight-row scale
                     const size_t wrow = static_cast<size_t>(tl.p) * R + col;
                     const float sw0 = args.w_scale0[wrow];
@@ -725,6 +822,31 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 // outputs (128 B of fp32 / 64 B of bf16): coalesced stores
                 // straight from registers.
                 uint8_t* base = outp + (static_cast<size_t>(tl.row0 + c0) * R + col) * out_elem;
+                if (quant_out) {
+                    // the activation rounded to bf16, then quantized to MX E4M3:
+                    // the warp's 32 lanes are one 32-element block of each
+                    // token row (max over the warp, shared exponent, codes)
+                    const int blk = (tl.rblk * BM + q * 32) / 32;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float a = bf16_bits_to_f32(f32_to_bf16_bits(v[c]));
+                        float m = fabsf(a);
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1)
+                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        const int e = mx_block_exp(m, 8);
+                        const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+                        const uint32_t code = cvt_e4m3x2(__fmul_rn(a, inv), 0.0f) & 0xffu;
+                        const int row = tl.row0 + c0 + c;
+                        if (c < nr && row < args.n_rows) {
+                            base[c * row_bytes] = static_cast<uint8_t>(code);
+                            if (lane == 0)
+                                args.out_sf[static_cast<size_t>(row) * (R / 32) + blk] =
+                                    static_cast<uint8_t>(e + 127);
+                        }
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     if (c < nr && tl.row0 + c0 + c < args.n_rows) {
@@ -797,6 +919,12 @@ using Gemm2PairF8 = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK8, 1>;
 #define GEMM1_SMALL_F8 grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kSwiGLU, 2, kBK8, 1>
 #define GEMM1_LARGE_F8 grouped_gemm_kernel<2, 256, kG1L_A, kG1L_B, kSwiGLU, 1, kBK8, 1>
 #define GEMM2_PAIR_F8 grouped_gemm_kernel<2, 128, kG2P_A, kG2P_B, kDownPair, 2, kBK8, 1>
+// MX block scales: 128-token tiles with one accumulator buffer (the scale
+// columns of the four token stages take the rest of TMEM)
+constexpr int kMx_A = 4, kMx_B = 4;
+using GemmMx = Layout<2, 128, kMx_A, kMx_B, 1, kBK8, 1, 1>;
+#define GEMM1_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kSwiGLU, 1, kBK8, 1, 1>
+#define GEMM2_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kDownPair, 1, kBK8, 1, 1>
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -844,6 +972,23 @@ bool make_gemm_maps_u8(GemmMaps* g, const void* a0, const void* a1, uint64_t wei
            make_map_u8(&g->b64, b, n_rows, K, 64) && make_map_u8(&g->b128, b, n_rows, K, 128);
 }
 
+// MX weight maps: E4M3 codes as bytes, or E2M1 codes packed two per byte
+// expanded by the copy to one element per byte of shared memory (16 codes in
+// the first 8 bytes of every 16), the layout kind::mxf8f6f4 reads.
+bool make_map_w_mx(CUtensorMap* m, int fmt, const void* ptr, uint64_t rows, uint64_t K) {
+    if (fmt == kMxE2M1)
+        return encode_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, ptr, K, rows, K / 2, kBK8,
+                             BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    return make_map_u8(m, ptr, rows, K, BM);
+}
+bool make_gemm_maps_mx(GemmMaps* g, int fmt, const void* a0, const void* a1,
+                       uint64_t weight_rows, const void* b, uint64_t n_rows, uint64_t K) {
+    return make_map_w_mx(&g->a0, fmt, a0, weight_rows, K) &&
+           make_map_w_mx(&g->a1, fmt, a1 ? a1 : a0, weight_rows, K) &&
+           make_map_u8(&g->b16, b, n_rows, K, 16) && make_map_u8(&g->b32, b, n_rows, K, 32) &&
+           make_map_u8(&g->b64, b, n_rows, K, 64) && make_map_u8(&g->b128, b, n_rows, K, 128);
+}
+
 std::mutex g_attr_mu;
 bool g_attr_done[64];
 
@@ -860,6 +1005,8 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_SMALL_F8, a, Gemm1SmallF8::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_LARGE_F8, a, Gemm1LargeF8::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_PAIR_F8, a, Gemm2PairF8::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX, a, GemmMx::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX, a, GemmMx::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) g_attr_done[device] = true;
     return cudaSuccess;
@@ -1014,6 +1161,50 @@ int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offs
     const FusedArgs none{0, 0, nullptr, nullptr};
     const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
     GEMM2_PAIR_F8<<<grid, NUM_THREADS, Gemm2PairF8::SMEM_BYTES, s>>>(m, m, a, none);
+    return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
+}
+
+int launch_gemm_gateup_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* row_to_token,
+                          int src_rows, const int32_t* offsets, int groups, int n_rows, int H,
+                          int I, int w_fmt, const uint8_t* wg, const uint8_t* sg,
+                          const uint8_t* wu, const uint8_t* su, int activation, uint8_t* aq,
+                          uint8_t* as, const DevCtx& ctx, cudaStream_t s) {
+    if (n_rows == 0) return GBMOE_OK;
+    GemmMaps m;
+    if (!make_gemm_maps_mx(&m, w_fmt, wg, wu, static_cast<uint64_t>(groups) * I, xq,
+                           row_to_token ? src_rows : n_rows, H))
+        return GBMOE_ERR_CUDA;
+    if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
+    GemmArgs a{offsets, groups, n_rows, I, H, aq, ctx.status,
+               row_to_token, row_to_token ? xq : nullptr, src_rows, activation};
+    a.tok_sf = xs;
+    a.w_sf0 = sg;
+    a.w_sf1 = su;
+    a.out_sf = as;
+    a.a_fmt = w_fmt == kMxE2M1 ? 5u : 0u;
+    const FusedArgs none{0, 0, nullptr, nullptr};
+    const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
+    GEMM1_MX<<<grid, NUM_THREADS, GemmMx::SMEM_BYTES, s>>>(m, m, a, none);
+    return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
+}
+
+int launch_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* offsets, int groups,
+                        int n_rows, int H, int I, int w_fmt, const uint8_t* wd,
+                        const uint8_t* sd, float* y, const DevCtx& ctx, cudaStream_t s) {
+    if (n_rows == 0) return GBMOE_OK;
+    if (H % 256) return GBMOE_ERR_UNSUPPORTED;
+    GemmMaps m;
+    if (!make_gemm_maps_mx(&m, w_fmt, wd, nullptr, static_cast<uint64_t>(groups) * H, aq, n_rows,
+                           I))
+        return GBMOE_ERR_CUDA;
+    if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
+    GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
+    a.tok_sf = as;
+    a.w_sf0 = sd;
+    a.a_fmt = w_fmt == kMxE2M1 ? 5u : 0u;
+    const FusedArgs none{0, 0, nullptr, nullptr};
+    const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
+    GEMM2_MX<<<grid, NUM_THREADS, GemmMx::SMEM_BYTES, s>>>(m, m, a, none);
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 

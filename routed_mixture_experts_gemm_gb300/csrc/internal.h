@@ -93,9 +93,28 @@ int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offs
                          int n_rows, int H, int I, const uint8_t* wd, const float* sd, float* y,
                          const DevCtx& ctx, cudaStream_t s);
 
-// --- FP8 row quantization (quant.cu) ---
+// MX block-scaled grouped GEMMs (kind::mxf8f6f4 block_scale): tokens /
+// activations as MX E4M3 (codes [rows, K], scale bytes [rows, K/32]),
+// weights as MX E4M3 or E2M1 (w_fmt: kMxE4M3 / kMxE2M1; E2M1 codes packed two
+// per byte).  The gate/up GEMM writes the activation already quantized to MX
+// E4M3 (act codes [n_rows, I] + scales [n_rows, I/32]); the down GEMM writes
+// y fp32.  H % 256 == 0, I % 128 == 0.
+int launch_gemm_gateup_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* row_to_token,
+                          int src_rows, const int32_t* offsets, int groups, int n_rows, int H,
+                          int I, int w_fmt, const uint8_t* wg, const uint8_t* sg,
+                          const uint8_t* wu, const uint8_t* su, int activation, uint8_t* aq,
+                          uint8_t* as, const DevCtx& ctx, cudaStream_t s);
+int launch_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* offsets, int groups,
+                        int n_rows, int H, int I, int w_fmt, const uint8_t* wd,
+                        const uint8_t* sd, float* y, const DevCtx& ctx, cudaStream_t s);
+
+// --- FP8 row quantization and MX block quantization (quant.cu) ---
 cudaError_t launch_quantize_rows(const uint16_t* x, int64_t n, int K, uint8_t* q, float* s,
                                  const DevCtx& ctx, cudaStream_t st);
+// rows [n, K] bf16 (K % 32 == 0) -> codes (E4M3 [n, K] or E2M1 [n, K/2]) and
+// UE8M0 scale bytes [n, K/32]
+cudaError_t launch_mx_quantize(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* q,
+                               uint8_t* sc, const DevCtx& ctx, cudaStream_t st);
 
 // --- latent-MoE tail (tail.cu) ---
 size_t latent_tail_ws_bytes(int T, int L, int Hm);
