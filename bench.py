@@ -18,9 +18,11 @@ resident in HBM.  Prints ONE JSON line (rank 0):
             measured peak: HBM bytes of the touched experts for decode,
             tensor FLOPs for prefill
   cpu_baseline  the CPU oracle timed on this host on a bounded token sample
-  fp8       both workloads again with FP8 E4M3 routed experts (row-quantized
-            weights, tokens and activations): throughput, the FP8 GEMM stage
-            times and their roofline (--no-fp8 skips it)
+  quantized both workloads again with quantized routed experts: FP8 E4M3
+            with one scale per row, MXFP8 (E4M3, a power-of-two scale per 32
+            elements) and W4A8 (MX E2M1 weights, MX E4M3 activations):
+            throughput, the expert-stage kernel times and the gate/up GEMM's
+            roofline (--no-quant skips them)
 
 --impl reference times the CPU oracle itself (the only reference there is:
 the pages publish no implementation), on the same workload and metric.
@@ -276,59 +278,92 @@ class Workload:
         if st:
             raise RuntimeError(f"staged forward failed (status bits {st})")
 
-    def enable_fp8(self):
-        """E4M3 codes and per-row scales of the routed experts' weights (made on
-        the device by the row quantizer) and a layer that runs on them."""
-        c, d, T = self.case, self.case.dev, self.cfg.T
-        q = [self.gb.quantize_experts_fp8(d[k]) for k in ("w_gate", "w_up", "w_down")]
-        self.w8 = [a for pair in q for a in pair]
-        self.layer8 = self.gb.MoELayer(c.layer.cfg, d["w_router"], None, None, None,
-                                       router_bias=d["router_bias"], corr_bias=d["corr_bias"],
-                                       tid2eid=d["tid2eid"], log2phy=d["log2phy"],
-                                       replica_cnt=d["replica_cnt"], shared=d["shared"],
-                                       fp8=self.w8)
-        self.ws8 = self.layer8.workspace(T)
+    # ---- quantized routed experts: "fp8_row" (E4M3, one fp32 scale per row),
+    # "mxfp8" (MX E4M3 weights and activations), "w4a8" (MX E2M1 weights, MX
+    # E4M3 activations)
+    QUANT = ("fp8_row", "mxfp8", "w4a8")
+
+    def enable_quant(self, kind):
+        """Quantized copies of the routed experts' weights (made on the device
+        by the library's quantizers) and a layer that runs on them."""
+        c, d, T, cfg = self.case, self.case.dev, self.cfg.T, self.cfg
         e = lambda *s, dt: self.torch.empty(s, dtype=dt, device=c.x.device)  # noqa: E731
-        self.xq = e(T, self.cfg.H, dt=self.torch.uint8)
-        self.sx = e(T, dt=self.torch.float32)
-        self.aq = e(self.cfg.N, self.cfg.I, dt=self.torch.uint8)
-        self.sa = e(self.cfg.N, dt=self.torch.float32)
+        u8, f32 = self.torch.uint8, self.torch.float32
+        kw = dict(router_bias=d["router_bias"], corr_bias=d["corr_bias"], tid2eid=d["tid2eid"],
+                  log2phy=d["log2phy"], replica_cnt=d["replica_cnt"], shared=d["shared"])
+        self.qkind = kind
+        if kind == "fp8_row":
+            q = [self.gb.quantize_experts_fp8(d[k]) for k in ("w_gate", "w_up", "w_down")]
+            self.wq = [a for pair in q for a in pair]
+            self.layer_q = self.gb.MoELayer(c.layer.cfg, d["w_router"], None, None, None,
+                                            fp8=self.wq, **kw)
+            self.xs, self.as_ = e(T, dt=f32), e(cfg.N, dt=f32)
+        else:
+            self.wfmt = "e4m3" if kind == "mxfp8" else "e2m1"
+            q = [self.gb.quantize_experts_mx(d[k], self.wfmt) for k in ("w_gate", "w_up",
+                                                                          "w_down")]
+            self.wq = [a for pair in q for a in pair]
+            self.layer_q = self.gb.MoELayer(c.layer.cfg, d["w_router"], None, None, None,
+                                            mx=[self.wfmt] + self.wq, **kw)
+            self.xs, self.as_ = e(T, cfg.H // 32, dt=u8), e(cfg.N, cfg.I // 32, dt=u8)
+        self.ws_q = self.layer_q.workspace(T)
+        self.xq = e(T, cfg.H, dt=u8)
+        self.aq = e(cfg.N, cfg.I, dt=u8)
 
-    def forward_fp8(self):
+    def disable_quant(self):
+        for k in ("wq", "layer_q", "ws_q", "xq", "aq", "xs", "as_"):
+            setattr(self, k, None)
+
+    def forward_q(self):
         c = self.case
-        self.gb.moe_forward(self.layer8, c.x, input_ids=c.input_ids, out=self.out,
+        self.gb.moe_forward(self.layer_q, c.x, input_ids=c.input_ids, out=self.out,
                             ids_log=self.ids, ids_phys=self.idp, weights=self.w,
-                            counts=self.counts, ws=self.ws8, stream=self.stream)
+                            counts=self.counts, ws=self.ws_q, stream=self.stream)
 
-    def staged_fp8_experts(self, ev):
-        """The FP8 expert stage as separate C-ABI calls (the routing and the
-        permutation from the last staged() call): quantize x, gate/up GEMM,
-        quantize the activations, down GEMM."""
+    def staged_q_experts(self, ev):
+        """The quantized expert stage as separate C-ABI calls (the routing and
+        the permutation from the last staged() call).  fp8_row: quantize x,
+        gate/up, quantize act, down; MX: quantize x, gate/up with the
+        activation quantized in its epilogue, down."""
         L, cfg, c, s = self.lib, self.cfg, self.case, self.stream.cuda_stream
         p = lambda t: t.data_ptr()  # noqa: E731
         T, P, N, H, I = cfg.T, cfg.P, cfg.N, cfg.H, cfg.I
-        wg, sg, wu, su, wd, sd = self.w8
+        wg, sg, wu, su, wd, sd = self.wq
         ev[0].record(self.stream)
-        st = L.moe_quantize_fp8_rows(p(c.x), T, H, p(self.xq), p(self.sx), s)
-        ev[1].record(self.stream)
-        st |= L.moe_gemm_gateup_act_fp8(p(self.xq), p(self.sx), p(self.r2t), T, p(self.offsets),
-                                        P, N, H, I, p(wg), p(sg), p(wu), p(su), 0, p(self.act),
-                                        s)
-        ev[2].record(self.stream)
-        st |= L.moe_quantize_fp8_rows(p(self.act), N, I, p(self.aq), p(self.sa), s)
-        ev[3].record(self.stream)
-        st |= L.moe_gemm_down_fp8(p(self.aq), p(self.sa), p(self.offsets), P, N, H, I, p(wd),
-                                  p(sd), p(self.y), s)
+        if self.qkind == "fp8_row":
+            st = L.moe_quantize_fp8_rows(p(c.x), T, H, p(self.xq), p(self.xs), s)
+            ev[1].record(self.stream)
+            st |= L.moe_gemm_gateup_act_fp8(p(self.xq), p(self.xs), p(self.r2t), T,
+                                            p(self.offsets), P, N, H, I, p(wg), p(sg), p(wu),
+                                            p(su), 0, p(self.act), s)
+            ev[2].record(self.stream)
+            st |= L.moe_quantize_fp8_rows(p(self.act), N, I, p(self.aq), p(self.as_), s)
+            ev[3].record(self.stream)
+            st |= L.moe_gemm_down_fp8(p(self.aq), p(self.as_), p(self.offsets), P, N, H, I, p(wd),
+                                      p(sd), p(self.y), s)
+        else:
+            f = 0 if self.wfmt == "e4m3" else 1
+            st = L.moe_quantize_mx_rows(p(c.x), T, H, 0, p(self.xq), p(self.xs), s)
+            ev[1].record(self.stream)
+            st |= L.moe_gemm_gateup_act_mx(p(self.xq), p(self.xs), p(self.r2t), T,
+                                           p(self.offsets), P, N, H, I, f, p(wg), p(sg), p(wu),
+                                           p(su), 0, p(self.aq), p(self.as_), s)
+            ev[2].record(self.stream)
+            ev[3].record(self.stream)
+            st |= L.moe_gemm_down_mx(p(self.aq), p(self.as_), p(self.offsets), P, N, H, I, f,
+                                     p(wd), p(sd), p(self.y), s)
         ev[4].record(self.stream)
         if st:
-            raise RuntimeError(f"staged FP8 experts failed (status bits {st})")
+            raise RuntimeError(f"staged {self.qkind} experts failed (status bits {st})")
 
-    def launches_per_step_fp8(self):
-        # the bf16 step with the expert MLP as quantize x, gate/up, quantize
-        # act, down
+    def launches_per_step_q(self):
+        # the bf16 step with the expert MLP replaced: fp8_row 4 launches
+        # (quantize x, gate/up, quantize act, down), MX 3 (quantize x, gate/up
+        # with the quantized activation, down)
         cfg = self.cfg
         perm = 1 if (cfg.N <= 4096 and cfg.P <= 1024) else 3
-        return 2 + perm + 4 + (2 if cfg.shared_I else 0) + 1
+        mlp = 4 if self.qkind == "fp8_row" else 3
+        return 2 + perm + mlp + (2 if cfg.shared_I else 0) + 1
 
     def launches_per_step(self):
         cfg = self.cfg
@@ -392,70 +427,92 @@ def touched_bytes(cfg, counts, fused=False):
     return w + xa, touched
 
 
-def fp8_stage_times(wl, steps, torch):
-    names = ["quantize_x", "gemm_gateup_fp8", "quantize_act", "gemm_down_fp8"]
+def q_stage_times(wl, steps, torch):
+    names = ["quantize_x", "gemm_gateup", "quantize_act", "gemm_down"]
     wl.staged([torch.cuda.Event(enable_timing=True) for _ in range(7)])
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     for _ in range(3):
-        wl.staged_fp8_experts(evs[0])
+        wl.staged_q_experts(evs[0])
     torch.cuda.synchronize()
     for i in range(steps):
-        wl.staged_fp8_experts(evs[i])
+        wl.staged_q_experts(evs[i])
     torch.cuda.synchronize()
-    return {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
-            for j, n in enumerate(names)}
+    out = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)) / steps
+           for j, n in enumerate(names)}
+    if wl.qkind != "fp8_row":
+        del out["quantize_act"]  # fused into the gate/up epilogue
+    return out
 
 
-def fp8_bytes(cfg, counts):
-    """Algorithmic bytes of the FP8 gate/up and down GEMMs: E4M3 weight codes
-    of the experts with rows and their fp32 row scales; gate/up reads each
-    token's codes once (gathered, repeats hit L2) and writes the bf16
-    activations; down reads the activation codes and writes fp32 outputs."""
+def q_bytes(cfg, counts, kind):
+    """Algorithmic bytes of the quantized gate/up and down GEMMs: weight codes
+    of the experts with rows (1 byte per element, 1/2 for E2M1) and their
+    scales (fp32 per row, or one byte per 32 elements); gate/up reads each
+    token's codes and scales once (gathered, repeats hit L2) and writes the
+    activation (bf16, or MX E4M3 codes + scales); down reads the activation
+    codes and writes fp32 outputs."""
     touched = int((counts > 0).sum())
-    g = touched * 2 * cfg.I * (cfg.H + 4) + cfg.T * (cfg.H + 4) + cfg.N * cfg.I * 2
-    d = touched * cfg.H * (cfg.I + 4) + cfg.N * (cfg.I + 4) + cfg.N * cfg.H * 4
+    H, I, T, N = cfg.H, cfg.I, cfg.T, cfg.N
+    if kind == "fp8_row":
+        g = touched * 2 * I * (H + 4) + T * (H + 4) + N * I * 2
+        d = touched * H * (I + 4) + N * (I + 4) + N * H * 4
+    else:
+        wb = 1.0 if kind == "mxfp8" else 0.5
+        g = touched * 2 * I * (H * wb + H / 32) + T * (H + H / 32) + N * (I + I / 32)
+        d = touched * H * (I * wb + I / 32) + N * (I + I / 32) + N * H * 4
     return g, d
 
 
-def fp8_measure(wl, steps, warmup, torch, barrier, peaks, peak_src, world, bound, local):
-    """The same workload with FP8 E4M3 routed experts: whole-layer throughput
-    and the roofline of the FP8 gate/up GEMM."""
-    wl.enable_fp8()
-    wl.forward_fp8()
+def q_measure(wl, kind, steps, warmup, torch, barrier, peaks, peak_src, world, bound, local):
+    """The same workload with quantized routed experts: whole-layer throughput,
+    the expert-stage kernel times and the gate/up GEMM's roofline."""
+    wl.enable_quant(kind)
+    wl.forward_q()
     torch.cuda.synchronize()
-    est = time_device(wl.forward_fp8, 3, warmup, torch, barrier) / 3
+    est = time_device(wl.forward_q, 3, warmup, torch, barrier) / 3
     n = max(steps, int(1.0 / max(est, 1e-6)))
     with ClockSampler(local) as clk:
         clk.mark_start()
-        secs = time_device(wl.forward_fp8, n, 1, torch, barrier)
+        secs = time_device(wl.forward_q, n, 1, torch, barrier)
         clk.mark_end()
-    stg = fp8_stage_times(wl, min(steps, 20), torch)
+    stg = q_stage_times(wl, min(steps, 20), torch)
     cfg = wl.cfg
-    gb_, db_ = fp8_bytes(cfg, wl.counts.cpu().numpy())
-    g1 = stg["gemm_gateup_fp8"] / 1000.0
-    g2 = stg["gemm_down_fp8"] / 1000.0
+    gb_, db_ = q_bytes(cfg, wl.counts.cpu().numpy(), kind)
+    g1 = stg["gemm_gateup"] / 1000.0
+    g2 = stg["gemm_down"] / 1000.0
+    kname = {"fp8_row": "grouped_gemm FP8 gate/up + SwiGLU (tcgen05 kind::f8f6f4)",
+             "mxfp8": "grouped_gemm MXFP8 gate/up + SwiGLU + MX quantization "
+                      "(tcgen05 kind::mxf8f6f4 block_scale)",
+             "w4a8": "grouped_gemm E2M1 x E4M3 gate/up + SwiGLU + MX quantization "
+                     "(tcgen05 kind::mxf8f6f4 block_scale)"}[kind]
     if bound == "hbm":
         hbm = peaks["hbm_gbs"]
-        roof = {"kernel": "grouped_gemm FP8 gate/up + SwiGLU (tcgen05 kind::f8f6f4)",
-                "bound": "hbm", "achieved": gb_ / g1 / 1e9, "peak": hbm, "unit": "GB/s",
-                "frac": gb_ / g1 / 1e9 / hbm, "traffic": None, "algorithmic_bytes": gb_,
+        roof = {"kernel": kname, "bound": "hbm", "achieved": gb_ / g1 / 1e9, "peak": hbm,
+                "unit": "GB/s", "frac": gb_ / g1 / 1e9 / hbm, "traffic": None,
+                "algorithmic_bytes": gb_,
                 "down": {"achieved": db_ / g2 / 1e9, "frac": db_ / g2 / 1e9 / hbm,
                          "algorithmic_bytes": db_},
                 "peak_source": f"{peak_src} hbm_gbs"}
     else:
         # nominal fp8 / bf16 dense tensor ratio 2 on the measured bf16 peak
+        # (E2M1 x E4M3 runs at the fp8 rate)
         pk = 2.0 * peaks["bf16_tflops_sustained"]
         f1 = 2.0 * cfg.N * 2 * cfg.H * cfg.I
         f2 = 2.0 * cfg.N * cfg.H * cfg.I
-        roof = {"kernel": "grouped_gemm FP8 gate/up + SwiGLU (tcgen05 kind::f8f6f4)",
-                "bound": "tensor", "achieved": f1 / g1 / 1e12, "peak": pk, "unit": "TFLOP/s",
-                "frac": f1 / g1 / 1e12 / pk, "traffic": None,
+        roof = {"kernel": kname, "bound": "tensor", "achieved": f1 / g1 / 1e12, "peak": pk,
+                "unit": "TFLOP/s", "frac": f1 / g1 / 1e12 / pk, "traffic": None,
                 "down": {"achieved": f2 / g2 / 1e12, "frac": f2 / g2 / 1e12 / pk},
                 "peak_source": f"{peak_src} bf16_tflops_sustained x 2 (nominal fp8/bf16 ratio)"}
-    return {"workload": cfg.name, "T": cfg.T, "dtype": "e4m3 x e4m3 -> f32 (routed experts)",
-            "value": world * cfg.T * n / secs, "unit": UNIT, "ms_per_step": 1000.0 * secs / n,
-            "steps": n, "stages_ms": stg, "clocks": clk.summary(),
-            "roofline": roof}, wl.launches_per_step_fp8() * n
+    res = {"workload": cfg.name, "T": cfg.T,
+           "dtype": {"fp8_row": "e4m3 x e4m3 -> f32, fp32 row scales",
+                     "mxfp8": "e4m3 x e4m3 -> f32, UE8M0 scales per 32",
+                     "w4a8": "e2m1 x e4m3 -> f32, UE8M0 scales per 32"}[kind],
+           "value": world * cfg.T * n / secs, "unit": UNIT, "ms_per_step": 1000.0 * secs / n,
+           "steps": n, "stages_ms": stg, "clocks": clk.summary(), "roofline": roof}
+    launches = wl.launches_per_step_q() * n
+    wl.disable_quant()
+    torch.cuda.empty_cache()
+    return res, launches
 
 
 def e2e_time(wl, steps, warmup, torch):
@@ -561,8 +618,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-fp8", action="store_true",
-                    help="skip the FP8 E4M3 expert measurements")
+    ap.add_argument("--no-quant", action="store_true",
+                    help="skip the quantized-expert measurements (FP8 rows, MXFP8, W4A8)")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     cfg = workload(args.workload)
@@ -664,11 +721,13 @@ def main(argv=None):
         "gpu_launches": wl.launches_per_step() * args.steps,
         "clocks": clocks,
     }
-    if not args.no_fp8:
-        f8, n8 = fp8_measure(wl, args.steps, args.warmup, torch, barrier, peaks, peak_src,
-                             world, "hbm", local)
-        line["fp8"] = {cfg.name: f8}
-        line["gpu_launches"] += n8
+    if not args.no_quant:
+        line["quantized"] = {}
+        for kind in Workload.QUANT:
+            r, nl = q_measure(wl, kind, args.steps, args.warmup, torch, barrier, peaks, peak_src,
+                              world, "hbm", local)
+            line["quantized"].setdefault(kind, {})[cfg.name] = r
+            line["gpu_launches"] += nl
     del wl
     torch.cuda.empty_cache()
 
@@ -702,11 +761,12 @@ def main(argv=None):
                          "peak_source": f"{peak_src} bf16_tflops_sustained"},
         }
         line["gpu_launches"] += w2.launches_per_step() * steps2
-        if not args.no_fp8:
-            f8, n8 = fp8_measure(w2, min(args.steps, 20), args.warmup, torch, barrier, peaks,
-                                 peak_src, world, "tensor", local)
-            line.setdefault("fp8", {})[c2.name] = f8
-            line["gpu_launches"] += n8
+        if not args.no_quant:
+            for kind in Workload.QUANT:
+                r, nl = q_measure(w2, kind, min(args.steps, 20), args.warmup, torch, barrier,
+                                  peaks, peak_src, world, "tensor", local)
+                line.setdefault("quantized", {}).setdefault(kind, {})[c2.name] = r
+                line["gpu_launches"] += nl
         del w2
         torch.cuda.empty_cache()
 

@@ -406,8 +406,8 @@ int moe_quantize_mx_rows(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* 
  *   row_to_token NULL); wgq / wuq [E_phys, I, H or H/2] + sg / su
  *   [E_phys, I, H/32]; aq [N, I] + as [N, I/32]; wdq [E_phys, H, I or I/2] +
  *   sd [E_phys, H, I/32].  H % 256 == 0, I % 128 == 0 (else UNSUPPORTED);
- *   code arrays 16-byte aligned (E2M1 weights 32-byte aligned), scale arrays
- *   4-byte aligned.
+ *   code arrays 16-byte aligned (E2M1 weights 32-byte aligned); weight scale
+ *   arrays 16-byte aligned, token / activation scale arrays 4-byte aligned.
  */
 int moe_gemm_gateup_act_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* row_to_token,
                            int T, const int32_t* offsets, int E_phys, int N, int H, int I,

@@ -134,8 +134,8 @@ int check_layer(const gbmoe_layer* L) {
             return GBMOE_ERR_UNSUPPORTED;
         if (!mx_weights_aligned(L->mx_format, L->w_gate_mx) ||
             !mx_weights_aligned(L->mx_format, L->w_up_mx) ||
-            !mx_weights_aligned(L->mx_format, L->w_down_mx) || !aligned4(L->sf_gate) ||
-            !aligned4(L->sf_up) || !aligned4(L->sf_down))
+            !mx_weights_aligned(L->mx_format, L->w_down_mx) || !aligned16(L->sf_gate) ||
+            !aligned16(L->sf_up) || !aligned16(L->sf_down))
             return GBMOE_ERR_INVALID_ARG;
         if (L->H % 256) return GBMOE_ERR_UNSUPPORTED;
     } else {
@@ -474,7 +474,7 @@ int moe_gemm_gateup_act_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* 
     if (!xq || !xs || !wgq || !sg || !wuq || !su || !act_q || !act_s)
         return GBMOE_ERR_INVALID_ARG;
     if (!aligned16(xq) || !mx_weights_aligned(w_fmt, wgq) || !mx_weights_aligned(w_fmt, wuq) ||
-        !aligned4(xs) || !aligned4(sg) || !aligned4(su))
+        !aligned4(xs) || !aligned16(sg) || !aligned16(su))
         return GBMOE_ERR_INVALID_ARG;
     const DevCtx* ctx = device_ctx();
     if (!ctx) return GBMOE_ERR_CUDA;
@@ -493,7 +493,7 @@ int moe_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* offset
     if (H % 256 || I % 128) return GBMOE_ERR_UNSUPPORTED;
     if (N == 0) return GBMOE_OK;
     if (!aq || !as || !wdq || !sd || !y) return GBMOE_ERR_INVALID_ARG;
-    if (!aligned16(aq) || !mx_weights_aligned(w_fmt, wdq) || !aligned4(as) || !aligned4(sd) ||
+    if (!aligned16(aq) || !mx_weights_aligned(w_fmt, wdq) || !aligned4(as) || !aligned16(sd) ||
         !aligned16(y))
         return GBMOE_ERR_INVALID_ARG;
     const DevCtx* ctx = device_ctx();

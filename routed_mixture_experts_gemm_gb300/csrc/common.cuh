@@ -205,22 +205,22 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-// 32 TMEM lanes x 4 / 8 consecutive 32-bit columns from registers; thread i
-// of the warp writes lane (base+i).
-__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&r)[4]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+// Shared memory -> TMEM: 32 rows of 16 bytes (row r at byte 16 r of the
+// source) into lanes r of all four lane quarters, 4 consecutive 32-bit
+// columns.  Issued by one thread; ordered with its later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                  : "memory");
 }
-__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
-                     taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-                 "r"(r[7])
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+// Descriptor of a contiguous, unswizzled source of 16-byte rows (8-row core
+// matrices 128 bytes apart in either direction).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(128 >> 4) << 16;            // leading byte offset
+    d |= static_cast<uint64_t>(128 >> 4) << 32;            // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                   // descriptor version (tcgen05)
+    return d;                                              // swizzle mode 0: none
 }
 
 // Shared-memory matrix descriptor for a K-major bf16 tile stored as rows of

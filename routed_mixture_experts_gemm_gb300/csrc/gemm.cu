@@ -69,6 +69,7 @@ constexpr int MAX_GROUPS = 1024;
 constexpr int NUM_THREADS = 32 * (LOADER_WARP0 + LOADER_WARPS);
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr int kCopyLag = 2;      // token stages in flight on the cp.async path
 
 // Operand / epilogue modes of the kernel template.
 //   kSwiGLU:   A0 = W_gate rows, A1 = W_up rows of the same 128-row block;
@@ -109,10 +110,17 @@ struct Layout {
     static constexpr int OFF_BARS = OFF_SCAN + NUM_THREADS * 4 + 16;
     static constexpr int NUM_BARS = 2 * SA + 2 * SB + 4 + 1;
     static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
-    static constexpr int END = OFF_MISC + 16;
+    // MX: per token stage, the scale words of its TMEM columns as 512-byte
+    // chunks of 32 rows x 16 bytes (row r = the four columns of lane r): one
+    // chunk per A operand and one per 128 token rows
+    static constexpr int SF_CHUNKS = NUM_A + BN / 128;
+    static constexpr int OFF_SFS = (OFF_MISC + 16 + 127) / 128 * 128;
+    static constexpr int SFS_BYTES = MXS ? SB * SF_CHUNKS * 512 : 0;
+    static constexpr int END = OFF_SFS + SFS_BYTES;
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
     static_assert(TMEM_USED <= 512 && (MXS || TMEM_USED == TMEM_COLS), "TMEM columns");
     static_assert(!MXS || (EB == 1 && BK == 128), "MX stages hold four 32-element K blocks");
+    static_assert(!MXS || BN % 128 == 0, "token scale chunks of 128 rows");
     static_assert(A_STAGE % 1024 == 0 && B_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(ROW_BYTES == 128 || (EB == 2 && ROW_BYTES == 64),
                   "stage K is one 128- or 64-byte swizzled row");
@@ -251,14 +259,26 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64
                  "l"(src), "l"(pol)
                  : "memory");
 }
+// 4-byte copy; with valid == false the destination is zero-filled and the
+// source is not read
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_one() {  // all but the newest group landed
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
+template <int N>  // all but the newest N groups landed
+__device__ __forceinline__ void cp_async_wait_newest() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // The gated activations (the result is rounded to bf16, so the fast
@@ -327,8 +347,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             mbar_init(afull + s, 1);
             mbar_init(aempty + s, 1);
         }
+        // MX token stages loaded by TMA complete on two arrivals: the lead
+        // thread's (with the copies' bytes) and the published scale columns
+        const uint32_t bfull_count = (MXS && args.gather_rows == nullptr) ? 2u : 1u;
         for (int s = 0; s < SB; ++s) {
-            mbar_init(bfull + s, 1);
+            mbar_init(bfull + s, bfull_count);
             mbar_init(bempty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -415,10 +438,26 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         uint32_t phase = 0;
         uint32_t armed = 0;          // bit s: stage s has been armed at least once
         uint32_t armed_phase = 0;    // bit s: parity of its last armed phase
+        // MX: a tile's weight scale rows (one contiguous run per A operand)
+        // are prefetched into L2 a tile ahead: the token loaders read them in
+        // 4-byte pieces on their critical path
+        auto prefetch_sf = [&](int tau) {
+            if (!MXS || tau >= total) return;
+            bool sec;
+            Tile t;
+            job(tau, sec, t);
+            const size_t kq = static_cast<size_t>(args.K / 32);
+            const size_t row = static_cast<size_t>(t.p) * args.R + static_cast<size_t>(t.rblk) * WROWS1;
+            prefetch_l2_bulk(args.w_sf0 + row * kq, static_cast<uint32_t>(WROWS1 * kq));
+            if (MODE1 == kSwiGLU)
+                prefetch_l2_bulk(args.w_sf1 + row * kq, static_cast<uint32_t>(BM * kq));
+        };
+        prefetch_sf(blockIdx.x);
         for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
             bool second;
             Tile tl;
             job(tau, second, tl);
+            prefetch_sf(tau + gridDim.x);
             const GemmMaps& m = second ? m2 : m1;
             const int mode = second ? kDownPair : MODE1;
             const int R = second ? fz.R : args.R;
@@ -459,13 +498,15 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     } else if (warp >= LOADER_WARP0) {
         // B loaders: token rows, by TMA (lead thread) or gathered by cp.async
         // (every loader thread copies one fixed 16-byte column of every 16th
-        // row of the tile).  A gathered stage is published once the next one
-        // has been issued (two stages in flight) and every loader's copies of
-        // it have landed: each thread waits for its own older copies and
-        // fences them for the tensor cores' proxy, and the barrier orders all
-        // of that before the lead thread's arrive.  A stage is published
-        // before the lead thread waits for the next free slot, which needs
-        // only stages SB or more behind: no cycle.
+        // row of the tile).  A gathered stage is published once a newer one
+        // has been issued (two stages in flight) and every loader's
+        // copies of it have landed: each thread waits for its own older
+        // copies and fences them for the tensor cores' proxy, and the barrier
+        // orders all of that before the lead thread's arrive.  A stage is
+        // published before the lead thread waits for the slot SB stages
+        // later: no cycle.  MX block scales travel the same way (scale words
+        // staged by cp.async; with TMA rows the stage completes on the lead
+        // thread's arrive and the scales' publishing arrive).
         const int li = tid - 32 * LOADER_WARP0;
         const bool lead = li == 0;
         const int chunk = li & 7;       // 16-byte column of the 128-byte row
@@ -475,15 +516,28 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         static_assert(BN % RSTEP == 0, "loader rows");
         const uint64_t pol_x = l2_policy_evict_last();
         // without gathered rows the lead thread alone streams the B ring
-        // (with MX block scales every loader warp writes the scale columns of
-        // its TMEM lane quarter)
+        // (with MX block scales every loader thread also stages scale words)
         const bool solo = args.gather_rows == nullptr && !MXS;
-        const uint32_t sf_lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const int kq = args.K / 32;     // scale bytes per row
+        // MX: loader warp w stages scale column w of every 4-column group
+        // (rows 32 w + lane of each A operand; token rows 32 (w + 4 c) + lane)
+        const int wi = warp - LOADER_WARP0;
         auto all_agree = [&](bool v) { return solo ? v : loader_bar_all(v); };
         int stage = 0;
         uint32_t phase = 0;
-        int pend = -1;                  // gathered stage whose copies are not yet published
+        // staged (cp.async) stages in flight: up to LAG copy groups, the
+        // oldest published once a new one is issued; with LAG <= SB a stage
+        // is always published before the lead thread waits for a slot that
+        // needs it consumed
+        constexpr int LAG = SB < kCopyLag ? SB : kCopyLag;
+        int npend = 0, last = 0;        // unpublished staged stages: the npend up to `last`
+        auto publish_oldest = [&](bool go) {
+            const int old = (last - (npend - 1) + SB) % SB;
+            fence_proxy_async_shared();
+            const bool all = loader_bar_all(go);
+            if (lead && all) mbar_arrive(bfull + old);
+            --npend;
+        };
         uint32_t armed = 0, armed_phase = 0;  // TMA-armed stages (lead thread)
         bool ok = !solo || lead;
         for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
@@ -492,14 +546,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             job(tau, second, tl);
             const bool gather = !second && args.gather_rows != nullptr && L::ROW_BYTES == 128;
             if (FUSED && second) {
-                // publish a pending gathered stage before waiting: the MMA
-                // needs it to finish the very gate/up tiles waited for
-                if (pend >= 0) {
+                // publish the pending gathered stages before waiting: the MMA
+                // needs them to finish the very gate/up tiles waited for
+                if (npend > 0) {
                     cp_async_wait_all();
-                    fence_proxy_async_shared();
-                    ok = loader_bar_all(true);
-                    if (lead) mbar_arrive(bfull + pend);
-                    pend = -1;
+                    while (npend > 0) publish_oldest(true);
                 }
                 // all gate/up tiles of this group must have published their rows
                 bool got = true;
@@ -544,16 +595,16 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     }
                 }
             }
-            // MX: the scale rows of this lane (row 32j + lane of each operand)
-            int64_t sfa_row[NUM_A], sfb_row[L::SFB_COLS];
+            // MX: the scale rows this thread stages
+            int64_t sfa_row[NUM_A], sfb_row[BN / 128];
             if (MXS) {
                 const int a_row = tl.p * args.R + tl.rblk * WROWS1;
 #pragma unroll
                 for (int a = 0; a < NUM_A; ++a)
-                    sfa_row[a] = a_row + (MODE1 == kDownPair ? a * BM : 0) + lane;
+                    sfa_row[a] = a_row + (MODE1 == kDownPair ? a * BM : 0) + 32 * wi + lane;
 #pragma unroll
-                for (int j = 0; j < L::SFB_COLS; ++j) {
-                    const int n = 32 * j + lane;
+                for (int j = 0; j < BN / 128; ++j) {
+                    const int n = 32 * (wi + 4 * j) + lane;
                     sfb_row[j] = -1;
                     if (n < tl.n_valid) {
                         int t = tl.row0 + n;
@@ -569,23 +620,6 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 }
             }
             for (int kb = 0; kb < KB; ++kb) {
-                // MX: this stage's scale bytes (loaded before waiting for the slot)
-                uint32_t sfa[NUM_A][4], sfb[L::SFB_COLS];
-                if (MXS) {
-#pragma unroll
-                    for (int a = 0; a < NUM_A; ++a) {
-                        const uint8_t* w = (MODE1 == kSwiGLU && a == 1) ? args.w_sf1 : args.w_sf0;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            sfa[a][j] = __ldg(reinterpret_cast<const uint32_t*>(
-                                w + (sfa_row[a] + 32 * j) * kq + kb * 4));
-                    }
-#pragma unroll
-                    for (int j = 0; j < L::SFB_COLS; ++j)
-                        sfb[j] = sfb_row[j] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(
-                                                       args.tok_sf + sfb_row[j] * kq + kb * 4))
-                                                 : 0x7f7f7f7fu;
-                }
                 bool free_ok = true;
                 if (lead)
                     free_ok = mbar_wait_bounded(bempty + stage, phase ^ 1u, abort_flag,
@@ -595,22 +629,21 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     break;
                 }
                 if (MXS) {
-                    // write the scale columns of this slot (every lane quarter
-                    // holds the same copy) and order them before the slot is
-                    // published: through the loaders' barrier to the lead
-                    // thread's arrive (TMA rows), or to the next stage's
-                    // publishing barrier (gathered rows)
-                    const uint32_t t =
-                        tmem_base + L::SF_BASE + stage * L::SF_STAGE_COLS + sf_lane;
+                    // this stage's scale words (four K blocks of a row each)
+                    // into its chunks, in the stage's copy group
+                    const uint32_t sfs = smem_u32(smem + L::OFF_SFS) +
+                                         stage * (L::SF_CHUNKS * 512) + lane * 16 + wi * 4;
 #pragma unroll
-                    for (int a = 0; a < NUM_A; ++a) tmem_st_32x32b_x4(t + 4 * a, sfa[a]);
-                    if constexpr (L::SFB_COLS == 4)
-                        tmem_st_32x32b_x4(t + 4 * NUM_A, sfb);
-                    else
-                        tmem_st_32x32b_x8(t + 4 * NUM_A, sfb);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    if (!gather) loader_bar_all(true);
+                    for (int a = 0; a < NUM_A; ++a) {
+                        const uint8_t* w = (MODE1 == kSwiGLU && a == 1) ? args.w_sf1 : args.w_sf0;
+                        cp_async4(sfs + a * 512, w + sfa_row[a] * kq + kb * 4, true);
+                    }
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j) {
+                        const bool v = sfb_row[j] >= 0;
+                        cp_async4(sfs + (NUM_A + j) * 512,
+                                  args.tok_sf + (v ? sfb_row[j] * kq + kb * 4 : 0), v);
+                    }
                 }
                 uint8_t* sB = smem + L::OFF_B + stage * L::B_BYTES;
                 if (gather) {
@@ -626,16 +659,6 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                                        pol_x);
                         }
                     }
-                    cp_async_commit();
-                    // publish the previous gathered stage: this thread's copies
-                    // of it have landed (only the newest group may be in flight)
-                    if (pend >= 0) {
-                        cp_async_wait_one();
-                        fence_proxy_async_shared();
-                        loader_bar_all(true);
-                        if (lead) mbar_arrive(bfull + pend);
-                    }
-                    pend = stage;
                 } else if (lead) {
                     mbar_arrive_expect_tx(bfull + stage, n_load * L::ROW_BYTES);
                     // token rows in as few boxes as possible (128/64/32/16 rows)
@@ -651,17 +674,28 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     armed |= 1u << stage;
                     armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                 }
+                if (gather || MXS) {
+                    cp_async_commit();
+                    last = stage;
+                    // publish the oldest staged stage: this thread's copies of
+                    // it have landed (only the newest LAG - 1 groups may be in
+                    // flight) and are fenced for the tensor cores' proxy, and
+                    // the barrier orders every loader's part before the lead
+                    // thread's arrive
+                    if (++npend == LAG) {
+                        cp_async_wait_newest<LAG - 1>();
+                        publish_oldest(true);
+                    }
+                }
                 if (++stage == SB) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
         }
-        if (pend >= 0) {  // publish the last gathered stage
+        if (npend > 0) {  // publish the last staged stages
             cp_async_wait_all();
-            fence_proxy_async_shared();
-            const bool all = loader_bar_all(ok);
-            if (lead && all) mbar_arrive(bfull + pend);
+            while (npend > 0) publish_oldest(ok);
         }
         cp_async_wait_all();
         if (lead && *abort_flag) {  // let every TMA copy issued land before exit
@@ -698,6 +732,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 const uint32_t sA = smem_u32(smem + as * L::A_STAGE);
                 const uint32_t sB = smem_u32(smem + L::OFF_B + bs * L::B_BYTES);
                 const uint32_t sf = tmem_base + L::SF_BASE + bs * L::SF_STAGE_COLS;
+                if (MXS) {
+                    // the stage's scale chunks into its TMEM columns (in order
+                    // with the MMAs below)
+                    const uint32_t sfs = smem_u32(smem + L::OFF_SFS) + bs * (L::SF_CHUNKS * 512);
+#pragma unroll
+                    for (int c = 0; c < L::SF_CHUNKS; ++c)
+                        tmem_cp_32x128b_warpx4(sf + 4 * c, smem_desc_rows16(sfs + c * 512));
+                }
                 // one MMA covers 32 bytes of K (16 bf16 or 32 FP8 elements)
 #pragma unroll
                 for (int ks = 0; ks < L::ROW_BYTES / 32; ++ks) {
@@ -830,10 +872,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
                         const float a = bf16_bits_to_f32(f32_to_bf16_bits(v[c]));
-                        float m = fabsf(a);
-#pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1)
-                            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        // magnitudes order like their fp32 bit patterns
+                        const float m = __uint_as_float(
+                            __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(a))));
                         const int e = mx_block_exp(m, 8);
                         const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
                         const uint32_t code = cvt_e4m3x2(__fmul_rn(a, inv), 0.0f) & 0xffu;
