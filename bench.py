@@ -620,7 +620,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quant", action="store_true",
                     help="skip the quantized-expert measurements (FP8 rows, MXFP8, W4A8)")
+    ap.add_argument("--quant", default=",".join(Workload.QUANT),
+                    help="comma-separated quantized kinds to measure (fp8_row, mxfp8, w4a8)")
     args = ap.parse_args(argv)
+    kinds = [k for k in args.quant.split(",") if k]
+    if any(k not in Workload.QUANT for k in kinds):
+        ap.error(f"--quant takes {', '.join(Workload.QUANT)}")
     world, rank, local = dist_setup()
     cfg = workload(args.workload)
     nthreads = os.cpu_count() or 1
@@ -723,7 +728,7 @@ def main(argv=None):
     }
     if not args.no_quant:
         line["quantized"] = {}
-        for kind in Workload.QUANT:
+        for kind in kinds:
             r, nl = q_measure(wl, kind, args.steps, args.warmup, torch, barrier, peaks, peak_src,
                               world, "hbm", local)
             line["quantized"].setdefault(kind, {})[cfg.name] = r
@@ -762,7 +767,7 @@ def main(argv=None):
         }
         line["gpu_launches"] += w2.launches_per_step() * steps2
         if not args.no_quant:
-            for kind in Workload.QUANT:
+            for kind in kinds:
                 r, nl = q_measure(w2, kind, min(args.steps, 20), args.warmup, torch, barrier,
                                   peaks, peak_src, world, "tensor", local)
                 line.setdefault("quantized", {}).setdefault(kind, {})[c2.name] = r

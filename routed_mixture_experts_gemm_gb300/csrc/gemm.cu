@@ -69,7 +69,7 @@ constexpr int MAX_GROUPS = 1024;
 constexpr int NUM_THREADS = 32 * (LOADER_WARP0 + LOADER_WARPS);
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
-constexpr int kCopyLag = 2;      // token stages in flight on the cp.async path
+constexpr int kCopyLag = 2;      // token stages in flight on the cp.async path (x2 for rings of 8+)
 
 // Operand / epilogue modes of the kernel template.
 //   kSwiGLU:   A0 = W_gate rows, A1 = W_up rows of the same 128-row block;
@@ -97,8 +97,11 @@ struct Layout {
     static constexpr int B_BYTES = BN * ROW_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
     static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
-    static constexpr int SFB_COLS = BN / 32;
-    static constexpr int SF_STAGE_COLS = NUM_A * 4 + SFB_COLS;
+    // MX: per token stage one 512-byte chunk of scale words per A operand and
+    // per (up to) 128 token rows, 4 TMEM columns each
+    static constexpr int SFB_CHUNKS = (BN + 127) / 128;
+    static constexpr int SF_CHUNKS = NUM_A + SFB_CHUNKS;
+    static constexpr int SF_STAGE_COLS = 4 * SF_CHUNKS;
     static constexpr int TMEM_USED = SF_BASE + (MXS ? SB * SF_STAGE_COLS : 0);
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static constexpr int TABLE_INTS = MAX_GROUPS + 4;
@@ -111,16 +114,14 @@ struct Layout {
     static constexpr int NUM_BARS = 2 * SA + 2 * SB + 4 + 1;
     static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
     // MX: per token stage, the scale words of its TMEM columns as 512-byte
-    // chunks of 32 rows x 16 bytes (row r = the four columns of lane r): one
-    // chunk per A operand and one per 128 token rows
-    static constexpr int SF_CHUNKS = NUM_A + BN / 128;
+    // chunks of 32 rows x 16 bytes (row r = the four columns of lane r)
     static constexpr int OFF_SFS = (OFF_MISC + 16 + 127) / 128 * 128;
     static constexpr int SFS_BYTES = MXS ? SB * SF_CHUNKS * 512 : 0;
     static constexpr int END = OFF_SFS + SFS_BYTES;
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
     static_assert(TMEM_USED <= 512 && (MXS || TMEM_USED == TMEM_COLS), "TMEM columns");
     static_assert(!MXS || (EB == 1 && BK == 128), "MX stages hold four 32-element K blocks");
-    static_assert(!MXS || BN % 128 == 0, "token scale chunks of 128 rows");
+    static_assert(!MXS || BN <= 128 || BN % 128 == 0, "token scale chunks of 128 rows");
     static_assert(A_STAGE % 1024 == 0 && B_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(ROW_BYTES == 128 || (EB == 2 && ROW_BYTES == 64),
                   "stage K is one 128- or 64-byte swizzled row");
@@ -529,7 +530,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         // oldest published once a new one is issued; with LAG <= SB a stage
         // is always published before the lead thread waits for a slot that
         // needs it consumed
-        constexpr int LAG = SB < kCopyLag ? SB : kCopyLag;
+        constexpr int LAG = SB >= 8 ? 2 * kCopyLag : kCopyLag;
         int npend = 0, last = 0;        // unpublished staged stages: the npend up to `last`
         auto publish_oldest = [&](bool go) {
             const int old = (last - (npend - 1) + SB) % SB;
@@ -596,14 +597,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 }
             }
             // MX: the scale rows this thread stages
-            int64_t sfa_row[NUM_A], sfb_row[BN / 128];
+            int64_t sfa_row[NUM_A], sfb_row[L::SFB_CHUNKS];
             if (MXS) {
                 const int a_row = tl.p * args.R + tl.rblk * WROWS1;
 #pragma unroll
                 for (int a = 0; a < NUM_A; ++a)
                     sfa_row[a] = a_row + (MODE1 == kDownPair ? a * BM : 0) + 32 * wi + lane;
 #pragma unroll
-                for (int j = 0; j < BN / 128; ++j) {
+                for (int j = 0; j < L::SFB_CHUNKS; ++j) {
                     const int n = 32 * (wi + 4 * j) + lane;
                     sfb_row[j] = -1;
                     if (n < tl.n_valid) {
@@ -639,7 +640,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                         cp_async4(sfs + a * 512, w + sfa_row[a] * kq + kb * 4, true);
                     }
 #pragma unroll
-                    for (int j = 0; j < BN / 128; ++j) {
+                    for (int j = 0; j < L::SFB_CHUNKS; ++j) {
                         const bool v = sfb_row[j] >= 0;
                         cp_async4(sfs + (NUM_A + j) * 512,
                                   args.tok_sf + (v ? sfb_row[j] * kq + kb * 4 : 0), v);
@@ -961,11 +962,18 @@ using Gemm2PairF8 = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK8, 1>;
 #define GEMM1_LARGE_F8 grouped_gemm_kernel<2, 256, kG1L_A, kG1L_B, kSwiGLU, 1, kBK8, 1>
 #define GEMM2_PAIR_F8 grouped_gemm_kernel<2, 128, kG2P_A, kG2P_B, kDownPair, 2, kBK8, 1>
 // MX block scales: 128-token tiles with one accumulator buffer (the scale
-// columns of the four token stages take the rest of TMEM)
+// columns of the four token stages take the rest of TMEM); for groups of at
+// most 32 rows on average (decode), 32-token tiles with two accumulator
+// buffers, 5 weight stages and 8 small token stages of which 4 are in flight
 constexpr int kMx_A = 4, kMx_B = 4;
+constexpr int kMxD_A = 5, kMxD_B = 8;
+constexpr long kMxDecodeRows = 32;
 using GemmMx = Layout<2, 128, kMx_A, kMx_B, 1, kBK8, 1, 1>;
+using GemmMxDec = Layout<2, 32, kMxD_A, kMxD_B, 2, kBK8, 1, 1>;
 #define GEMM1_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kSwiGLU, 1, kBK8, 1, 1>
 #define GEMM2_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kDownPair, 1, kBK8, 1, 1>
+#define GEMM1_MX_DEC grouped_gemm_kernel<2, 32, kMxD_A, kMxD_B, kSwiGLU, 2, kBK8, 1, 1>
+#define GEMM2_MX_DEC grouped_gemm_kernel<2, 32, kMxD_A, kMxD_B, kDownPair, 2, kBK8, 1, 1>
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1048,6 +1056,8 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_PAIR_F8, a, Gemm2PairF8::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX, a, GemmMx::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX, a, GemmMx::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_DEC, a, GemmMxDec::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_DEC, a, GemmMxDec::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) g_attr_done[device] = true;
     return cudaSuccess;
@@ -1224,8 +1234,13 @@ int launch_gemm_gateup_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* r
     a.out_sf = as;
     a.a_fmt = w_fmt == kMxE2M1 ? 5u : 0u;
     const FusedArgs none{0, 0, nullptr, nullptr};
-    const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
-    GEMM1_MX<<<grid, NUM_THREADS, GemmMx::SMEM_BYTES, s>>>(m, m, a, none);
+    if (n_rows <= kMxDecodeRows * groups) {
+        const int grid = grid_for(groups, n_rows, I, 32, ctx.num_sms);
+        GEMM1_MX_DEC<<<grid, NUM_THREADS, GemmMxDec::SMEM_BYTES, s>>>(m, m, a, none);
+    } else {
+        const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
+        GEMM1_MX<<<grid, NUM_THREADS, GemmMx::SMEM_BYTES, s>>>(m, m, a, none);
+    }
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 
@@ -1244,8 +1259,13 @@ int launch_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* off
     a.w_sf0 = sd;
     a.a_fmt = w_fmt == kMxE2M1 ? 5u : 0u;
     const FusedArgs none{0, 0, nullptr, nullptr};
-    const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
-    GEMM2_MX<<<grid, NUM_THREADS, GemmMx::SMEM_BYTES, s>>>(m, m, a, none);
+    if (n_rows <= kMxDecodeRows * groups) {
+        const int grid = grid_for(groups, n_rows, H / 2, 32, ctx.num_sms);
+        GEMM2_MX_DEC<<<grid, NUM_THREADS, GemmMxDec::SMEM_BYTES, s>>>(m, m, a, none);
+    } else {
+        const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
+        GEMM2_MX<<<grid, NUM_THREADS, GemmMx::SMEM_BYTES, s>>>(m, m, a, none);
+    }
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
 }
 
