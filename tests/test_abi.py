@@ -124,3 +124,58 @@ def test_log2phy_validation(lib):
     c0 = cnt.copy()
     c0[1] = 0      # a logical expert left unplaced
     assert lib.gbmoe_validate_log2phy(l2p.ctypes.data, c0.ctypes.data, E, R, P) == 1
+
+
+def test_quantized_entry_points_reject_bad_arguments_on_host(lib):
+    fake, odd4, odd16 = (ctypes.c_void_p(a) for a in (0x1000, 0x1004, 0x1010))
+    # FP8 rows: K a multiple of 8, H % 256 for the GEMMs, known activations
+    assert lib.moe_quantize_fp8_rows(fake, 4, 100, fake, fake, None) == 2
+    assert lib.moe_gemm_gateup_act_fp8(fake, fake, fake, 8, fake, 4, 16, 384, 128, fake, fake,
+                                       fake, fake, 0, fake, None) == 2
+    assert lib.moe_gemm_gateup_act_fp8(fake, fake, fake, 8, fake, 4, 16, 512, 128, fake, fake,
+                                       fake, fake, 9, fake, None) == 2
+    assert lib.moe_gemm_down_fp8(fake, fake, fake, 4, 16, 512, 100, fake, fake, fake, None) == 2
+    # MX quantizer: unknown format, K % 32, misaligned codes; n = 0 is a no-op
+    assert lib.moe_quantize_mx_rows(fake, 4, 256, 7, fake, fake, None) == 2
+    assert lib.moe_quantize_mx_rows(fake, 4, 48, 0, fake, fake, None) == 2
+    assert lib.moe_quantize_mx_rows(fake, 4, 256, 0, odd4, fake, None) == 1
+    assert lib.moe_quantize_mx_rows(None, 0, 256, 0, None, None, None) == 0
+    # MX GEMMs: H % 256, unknown weight format, E2M1 weights 32-byte aligned,
+    # weight scales 16-byte aligned, known activations, missing outputs
+    gu = lambda H, fmt, wg, sg, act, aq: lib.moe_gemm_gateup_act_mx(  # noqa: E731
+        fake, fake, fake, 8, fake, 4, 16, H, 128, fmt, wg, sg, fake, fake, act, aq, fake, None)
+    assert gu(384, 0, fake, fake, 0, fake) == 2
+    assert gu(512, 3, fake, fake, 0, fake) == 2
+    assert gu(512, 1, odd16, fake, 0, fake) == 1
+    assert gu(512, 0, fake, odd4, 0, fake) == 1
+    assert gu(512, 0, fake, fake, 9, fake) == 2
+    assert gu(512, 0, fake, fake, 0, None) == 1
+    dn = lambda H, I, fmt, sd: lib.moe_gemm_down_mx(  # noqa: E731
+        fake, fake, fake, 4, 16, H, I, fmt, fake, sd, fake, None)
+    assert dn(384, 128, 0, fake) == 2
+    assert dn(512, 96, 0, fake) == 2
+    assert dn(512, 128, 2, fake) == 2
+    assert dn(512, 128, 1, odd4) == 1
+
+
+def test_quantized_layers_validate_and_size_their_workspace(lib):
+    from routed_mixture_experts_gemm_gb300 import _lib
+    c = _cfg()
+    base = [c, 256, 128, 0, 0x1000, None, None, None, 0, None, None, 1]
+    bf16 = _lib.Layer(*base, 0x1000, 0x1000, 0x1000, None, None, None)
+    fp8 = _lib.Layer(*base, None, None, None, None, None, None, 0, *([0x1000] * 6))
+    mx = _lib.Layer(*base, None, None, None, None, None, None, 0, *([None] * 6), 1,
+                    *([0x1000] * 6))
+    a, b, m = (lib.gbmoe_forward_workspace_size(ctypes.byref(L), 64) for L in (bf16, fp8, mx))
+    assert 0 < a < b and a < m        # quantized tokens / activations on top
+    # an MX layer with an unknown format, E2M1 weights off a 32-byte boundary,
+    # or H % 256 != 0 is rejected (size 0)
+    bad_fmt = _lib.Layer(*base, None, None, None, None, None, None, 0, *([None] * 6), 5,
+                         *([0x1000] * 6))
+    bad_al = _lib.Layer(*base, None, None, None, None, None, None, 0, *([None] * 6), 1,
+                        0x1010, *([0x1000] * 5))
+    base_h = [c, 384] + base[2:]
+    bad_h = _lib.Layer(*base_h, None, None, None, None, None, None, 0, *([None] * 6), 0,
+                       *([0x1000] * 6))
+    for L in (bad_fmt, bad_al, bad_h):
+        assert lib.gbmoe_forward_workspace_size(ctypes.byref(L), 64) == 0
