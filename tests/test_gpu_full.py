@@ -122,3 +122,105 @@ def test_full_size(gb, name):
     assert err.max() <= 2 * 2.0 ** -8 * np.abs(exp).max()
     del case, out
     torch.cuda.empty_cache()
+
+
+# ---- quantized routed experts at full size (FP8 rows; MX E4M3 / E2M1)
+QKINDS = {"fp8_row": None, "mxfp8": "e4m3", "w4a8": "e2m1"}
+
+
+def _quantized_layer(gb, case, kind):
+    dv = case.dev
+    kw = dict(router_bias=dv["router_bias"], corr_bias=dv["corr_bias"], tid2eid=dv["tid2eid"],
+              log2phy=dv["log2phy"], replica_cnt=dv["replica_cnt"], shared=dv["shared"])
+    fmt = QKINDS[kind]
+    if fmt is None:
+        q = [gb.quantize_experts_fp8(dv[n]) for n in ("w_gate", "w_up", "w_down")]
+        layer = gb.MoELayer(case.layer.cfg, dv["w_router"], None, None, None,
+                            fp8=[a for pair in q for a in pair], **kw)
+    else:
+        q = [gb.quantize_experts_mx(dv[n], fmt) for n in ("w_gate", "w_up", "w_down")]
+        layer = gb.MoELayer(case.layer.cfg, dv["w_router"], None, None, None,
+                            mx=[fmt] + [a for pair in q for a in pair], **kw)
+    return layer, q
+
+
+def _oracle_quantized_rows(cfg, d, kind, q_dev, need, tokens):
+    """y of the sampled (token, slot) pairs from the oracle's quantized MLP,
+    expert by expert, after checking the GPU's weight codes of each expert."""
+    fmt = QKINDS[kind]
+    xs_rows = d["x"][tokens]
+    pos = {t: i for i, t in enumerate(tokens)}
+    if fmt is None:
+        xq, xsc = oracle.quantize_rows(xs_rows)
+    else:
+        xq, xsc = oracle.mx_quantize_rows(xs_rows, "e4m3")
+    pl = d["placement"]
+
+    def one(p):
+        e = int(pl.phys_to_log[p])
+        mats = synth.expert_weights_host(cfg, e)
+        qo = []
+        for m, (wq, ws) in zip(mats, q_dev):
+            cq, cs = (oracle.quantize_rows(m) if fmt is None else oracle.mx_quantize_rows(m, fmt))
+            assert np.array_equal(_np(wq[p]), cq.reshape(wq[p].shape)), f"codes of slot {p}"
+            assert np.array_equal(_np(ws[p]).view(np.uint8), cs.reshape(ws[p].shape)
+                                  .view(np.uint8)), f"scales of slot {p}"
+            qo += [cq[None], cs[None]]
+        rows = need[p]
+        r2t = np.array([pos[t] for t, _ in rows], np.int32)
+        offs = np.array([0, len(rows)], np.int32)
+        if fmt is None:
+            _, y = oracle.ffn_grouped_fp8(xq, xsc, r2t, offs, *qo, nthreads=1)
+        else:
+            _, _, _, y = oracle.ffn_grouped_mx(xq, xsc, r2t, offs, *qo, wfmt=fmt, nthreads=1)
+        return rows, y
+
+    out = {}
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        for rows, y in ex.map(one, sorted(need)):
+            for (t, j), r in zip(rows, y):
+                out[(t, j)] = r
+    return out
+
+
+@pytest.mark.parametrize("name,kind", [("decode", "fp8_row"), ("decode", "mxfp8"),
+                                       ("decode", "w4a8"), ("prefill", "fp8_row"),
+                                       ("prefill", "w4a8")])
+def test_full_size_quantized(gb, name, kind):
+    cfg = synth.CONFIGS[name]
+    case = device_case(cfg, DEV, host_weights=False)
+    d = case.inputs
+    pl = d["placement"]
+    T, k = cfg.T, cfg.k
+    layer, q = _quantized_layer(gb, case, kind)
+    idp = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    out = gb.moe_forward(layer, case.x, input_ids=case.input_ids, ids_phys=idp, weights=w)
+    assert gb.check_device_status() == 0
+    # routing of every token, bit for bit (the router is not quantized)
+    logits = oracle.router_logits(d["x"], d["w_router"], d["router_bias"])
+    _, idp_o, w_o = oracle.route(oracle.cfg_from(cfg), logits, corr_bias=d["corr_bias"],
+                                 input_ids=d["input_ids"], tid2eid=d["tid2eid"],
+                                 log2phy=pl.log2phy, replica_cnt=pl.replica_cnt)
+    assert np.array_equal(_np(idp), idp_o)
+    assert np.array_equal(_np(w).view(np.uint32), w_o.view(np.uint32))
+    # sampled outputs, including the first and last token
+    rng = np.random.default_rng(cfg.seed + 200)
+    sample = sorted({0, T - 1, *rng.choice(T, max(2, N_SAMPLE // 2), replace=False).tolist()})
+    need = {}
+    for t in sample:
+        for j in range(k):
+            need.setdefault(int(idp_o[t, j]), []).append((t, j))
+    y = _oracle_quantized_rows(cfg, d, kind, q, need, sample)
+    exp = []
+    for t in sample:
+        yt = np.stack([y[(t, j)] for j in range(k)])
+        exp.append(oracle.combine(yt, np.arange(k, dtype=np.int32), w_o[t:t + 1], None)[0])
+    exp = synth.bf16_to_f32(np.stack(exp)).astype(np.float64)
+    got = _np(out[sample].float()).astype(np.float64)
+    err = np.abs(got - exp)
+    bad = err > 1e-2 + 1e-2 * np.abs(exp)
+    assert not bad.any(), f"{kind} {name}: {bad.sum()} of {err.size} outside, max {err.max()}"
+    assert err.max() <= 2 * 2.0 ** -8 * np.abs(exp).max()
+    del case, out, layer, q
+    torch.cuda.empty_cache()
