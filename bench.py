@@ -488,7 +488,8 @@ def q_measure(wl, kind, steps, warmup, torch, barrier, peaks, peak_src, world, b
     if bound == "hbm":
         hbm = peaks["hbm_gbs"]
         roof = {"kernel": kname, "bound": "hbm", "achieved": gb_ / g1 / 1e9, "peak": hbm,
-                "unit": "GB/s", "frac": gb_ / g1 / 1e9 / hbm, "traffic": None,
+                "unit": "GB/s", "frac": gb_ / g1 / 1e9 / hbm,
+                "traffic": profiled_traffic(f"{kind}_gateup", cfg.name),
                 "algorithmic_bytes": gb_,
                 "down": {"achieved": db_ / g2 / 1e9, "frac": db_ / g2 / 1e9 / hbm,
                          "algorithmic_bytes": db_},
@@ -500,7 +501,8 @@ def q_measure(wl, kind, steps, warmup, torch, barrier, peaks, peak_src, world, b
         f1 = 2.0 * cfg.N * 2 * cfg.H * cfg.I
         f2 = 2.0 * cfg.N * cfg.H * cfg.I
         roof = {"kernel": kname, "bound": "tensor", "achieved": f1 / g1 / 1e12, "peak": pk,
-                "unit": "TFLOP/s", "frac": f1 / g1 / 1e12 / pk, "traffic": None,
+                "unit": "TFLOP/s", "frac": f1 / g1 / 1e12 / pk,
+                "traffic": profiled_traffic(f"{kind}_gateup", cfg.name),
                 "down": {"achieved": f2 / g2 / 1e12, "frac": f2 / g2 / 1e12 / pk},
                 "peak_source": f"{peak_src} bf16_tflops_sustained x 2 (nominal fp8/bf16 ratio)"}
     res = {"workload": cfg.name, "T": cfg.T,
