@@ -10,7 +10,11 @@
  * combine that restores token order and applies the routing probabilities
  * (same table), and per-expert token counts for load tracking (section
  * "Stage 6: Dynamic EPLB").  On one GPU the dispatch is a local permutation:
- * no expert parallelism and no collectives.
+ * no expert parallelism and no collectives.  The same section's quantized
+ * expert paths are provided as FP8 E4M3 with per-row scales (W8A8FP) and MX
+ * block-scaled experts (MXFP8, and W4A8 read as E2M1 weights with E4M3
+ * activations); the NVIDIA LatentMoERunner page's post-MoE tail (RMSNorm,
+ * up-projection, shared-expert add) is provided for one GPU.
  *
  * Conventions shared by every entry point:
  *  - Tensor pointers are DEVICE pointers owned by the caller (except where a
