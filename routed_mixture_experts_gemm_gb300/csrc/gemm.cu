@@ -928,9 +928,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 // ----------------------------------------------------------------- host
 // Variant choice (measured on the decode, hash, skew and prefill routings):
 // gate/up uses 256-token tiles once groups average >= 96 rows; the down GEMM
-// pairs two 128-row W_down blocks over 128-token tiles with two accumulator
-// buffers whenever H % 256 == 0 (best or equal on every workload), else 128-
-// or 256-token single-block tiles.  All variants stream K in 64-wide stages
+// pairs two 128-row W_down blocks whenever H % 256 == 0, over 256-token tiles
+// (one accumulator buffer) from 96 rows per group on average and over
+// 128-token tiles with two buffers below, else 128- or 256-token
+// single-block tiles.  All variants stream K in 64-wide stages
 // (32-wide stages with the 64B swizzle were measured slower: per-stage costs
 // outweigh the extra lookahead).  Below 96 rows per group with H % 256 == 0
 // moe_forward runs the two GEMMs fused in one launch (their tiles share one
@@ -952,6 +953,8 @@ using Gemm2Pair = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK>;
 #define GEMM2_SMALL grouped_gemm_kernel<1, 128, kG2S_A, kG2S_B, kDown, 2, kBK>
 #define GEMM2_LARGE grouped_gemm_kernel<1, 256, kG2L_A, kG2L_B, kDown, 2, kBK>
 #define GEMM2_PAIR grouped_gemm_kernel<2, 128, kG2P_A, kG2P_B, kDownPair, 2, kBK>
+// paired down blocks over 256-token tiles (the gate/up 256-token layout)
+#define GEMM2_PAIR_LARGE grouped_gemm_kernel<2, 256, kG1L_A, kG1L_B, kDownPair, 1, kBK>
 #define GEMM_FUSED grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kFused, 2, kBK>
 // FP8 E4M3 operands: 128-element stages (the same 128-byte rows)
 constexpr int kBK8 = 128;
@@ -1050,6 +1053,7 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_SMALL, a, Gemm2Small::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_LARGE, a, Gemm2Large::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_PAIR, a, Gemm2Pair::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_PAIR_LARGE, a, Gemm1Large::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM_FUSED, a, Gemm1Small::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_SMALL_F8, a, Gemm1SmallF8::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_LARGE_F8, a, Gemm1LargeF8::SMEM_BYTES);
@@ -1125,7 +1129,10 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     const GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
     const FusedArgs none{0, 0, nullptr, nullptr};
-    if (H % 256 == 0) {
+    if (H % 256 == 0 && n_rows >= kLargeGateUpRows * groups) {
+        const int grid = grid_for(groups, n_rows, H / 2, 256, ctx.num_sms);
+        GEMM2_PAIR_LARGE<<<grid, NUM_THREADS, Gemm1Large::SMEM_BYTES, s>>>(m, m, a, none);
+    } else if (H % 256 == 0) {
         const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
         GEMM2_PAIR<<<grid, NUM_THREADS, Gemm2Pair::SMEM_BYTES, s>>>(m, m, a, none);
     } else if (n_rows >= 128L * groups) {
@@ -1210,6 +1217,7 @@ int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offs
     a.tok_scale = sa;
     a.w_scale0 = sd;
     const FusedArgs none{0, 0, nullptr, nullptr};
+    // (256-token paired tiles, faster for bf16, were measured slower here)
     const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
     GEMM2_PAIR_F8<<<grid, NUM_THREADS, Gemm2PairF8::SMEM_BYTES, s>>>(m, m, a, none);
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
