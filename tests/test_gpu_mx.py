@@ -178,3 +178,72 @@ def test_mx_rejects_bad_arguments(gb):
     offs = torch.tensor([0, 16], dtype=torch.int32, device=DEV)
     with pytest.raises(gb.GbmoeError):                         # H % 256 != 0
         gb.moe_gemm_gateup_act_mx(q, s, offs, w, ws, w, ws)
+
+
+@pytest.mark.parametrize("rows", [[32, 32, 32, 32], [33, 33, 33, 33], [1, 0, 0, 127]])
+@pytest.mark.parametrize("wfmt", ["e4m3", "e2m1"])
+def test_mx_variant_boundary(gb, rows, wfmt):
+    """Both sides of the decode-variant switch (32 rows per group on average)
+    and a group of 127 rows next to empty ones."""
+    H, I = 256, 128
+    c = _mx_case(H, I, rows, wfmt, 7 + sum(rows))
+    act_o, aq_o, as_o, _ = oracle.ffn_grouped_mx(
+        c["xq"], c["xs"], c["r2t"], c["offs"], c["wg"], c["sg"], c["wu"], c["su"], c["wd"],
+        c["sd"], wfmt=wfmt, nthreads=8)
+    d = {k: _dev(v) for k, v in c.items() if isinstance(v, np.ndarray)}
+    aq, as_ = gb.moe_gemm_gateup_act_mx(d["xq"], d["xs"], d["offs"], d["wg"], d["sg"], d["wu"],
+                                        d["su"], w_fmt=wfmt, row_to_token=d["r2t"])
+    y = gb.moe_gemm_down_mx(aq, as_, d["offs"], d["wd"], d["sd"], w_fmt=wfmt)
+    assert gb.check_device_status() == 0
+    check_act_codes(_np(aq), _np(as_), aq_o, as_o, act_o, f"boundary {rows} {wfmt}")
+    a = deq(_np(aq), _np(as_), "e4m3")
+    offs = c["offs"]
+    for p in range(len(rows)):
+        r0, r1 = offs[p], offs[p + 1]
+        if r0 == r1:
+            continue
+        wdd = deq(c["wd"][p], c["sd"][p], wfmt)
+        bound = np.abs(a[r0:r1]) @ np.abs(wdd).T
+        assert np.all(np.abs(_np(y)[r0:r1] - a[r0:r1] @ wdd.T) <= 2.0 ** -12 * bound + 1e-30)
+
+
+@pytest.mark.parametrize("T", [1, 2, 17])
+@pytest.mark.parametrize("kind", ["fp8_row", "w4a8"])
+def test_quantized_forward_small_batches(gb, T, kind):
+    """moe_forward with quantized experts on batches of 1, 2 and 17 tokens
+    (the tiny layer's first T tokens) against the oracle pipeline."""
+    import dataclasses
+    from synth.device import device_case
+    cfg = dataclasses.replace(synth.CONFIGS["tiny"], T=T)
+    case = device_case(cfg, DEV, host_weights=True)
+    d = case.dev
+    kw = dict(router_bias=d["router_bias"], corr_bias=d["corr_bias"], tid2eid=d["tid2eid"],
+              log2phy=d["log2phy"], replica_cnt=d["replica_cnt"], shared=d["shared"])
+    ref = oracle.run_config(cfg, inputs=case.inputs, weights=case.weights_host)
+    qo = []
+    if kind == "fp8_row":
+        q = [gb.quantize_experts_fp8(d[n]) for n in ("w_gate", "w_up", "w_down")]
+        layer = gb.MoELayer(case.layer.cfg, d["w_router"], None, None, None,
+                            fp8=[a for pair in q for a in pair], **kw)
+        for w in case.weights_host:
+            P, R, K = w.shape
+            cq, cs = oracle.quantize_rows(w.reshape(P * R, K))
+            qo += [cq.reshape(P, R, K), cs.reshape(P, R)]
+        xq, xs = oracle.quantize_rows(case.inputs["x"])
+        _, y = oracle.ffn_grouped_fp8(xq, xs, ref["row_to_token"], ref["offsets"], *qo,
+                                      nthreads=4)
+    else:
+        q = [gb.quantize_experts_mx(d[n], "e2m1") for n in ("w_gate", "w_up", "w_down")]
+        layer = gb.MoELayer(case.layer.cfg, d["w_router"], None, None, None,
+                            mx=["e2m1"] + [a for pair in q for a in pair], **kw)
+        for w in case.weights_host:
+            P, R, K = w.shape
+            cq, cs = oracle.mx_quantize_rows(w.reshape(P * R, K), "e2m1")
+            qo += [cq.reshape(P, R, -1), cs.reshape(P, R, -1)]
+        xq, xs = oracle.mx_quantize_rows(case.inputs["x"], "e4m3")
+        _, _, _, y = oracle.ffn_grouped_mx(xq, xs, ref["row_to_token"], ref["offsets"], *qo,
+                                           wfmt="e2m1", nthreads=4)
+    out = gb.moe_forward(layer, case.x)
+    assert gb.check_device_status() == 0
+    exp = oracle.combine(y, ref["flat_to_row"], ref["weights"], ref.get("ys"))
+    assert_within_tol(_bf(out), synth.bf16_to_f32(exp), f"{kind} T={T}")
