@@ -141,3 +141,22 @@ def test_grouped_mlp_matches_dense_matmuls(wfmt, act, rng):
         assert np.array_equal(aq[r0:r1], q2) and np.array_equal(as_[r0:r1], s2)
         y_ref = deq(aq[r0:r1], as_[r0:r1], "e4m3") @ wdd.T
         assert np.allclose(y[r0:r1], y_ref, rtol=1e-6, atol=1e-30)
+
+
+def test_e2m1_matches_brute_force_nearest(rng):
+    """Every value against a search over the eight magnitudes: the nearest,
+    ties to the even code, beyond 6 saturated; the sign kept (also on zero)."""
+    mids = [0.5 * (a + b) for a, b in zip(E2M1[:-1], E2M1[1:])]
+    vals = np.concatenate([rng.uniform(-8, 8, 3000), mids, [-m for m in mids], E2M1,
+                           [6.0001, 7.999, -1e-7]]).astype(np.float32)
+    mags = np.array(E2M1)
+    for v in vals:
+        a = abs(float(v))
+        if a >= 6.0:
+            k = 7
+        else:
+            dist = np.abs(mags - a)
+            cand = np.flatnonzero(dist == dist.min())
+            k = int(cand[0]) if len(cand) == 1 else int(cand[cand % 2 == 0][0])
+        want = k | (8 if np.signbit(v) else 0)
+        assert oracle.f32_to_e2m1(float(v)) == want, v
