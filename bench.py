@@ -13,10 +13,16 @@ resident in HBM.  Prints ONE JSON line (rank 0):
   e2e       the same metric through moe_forward_host with pinned host
             buffers: host->device copy of x and device->host copy of out
             inside the timed region
-  prefill   the same measurement at T=8192 (the metric's second batch size)
-  roofline  the dominant kernel (the gate/up grouped GEMM) against the
-            measured peak: HBM bytes of the touched experts for decode,
-            tensor FLOPs for prefill
+  sustained the decode step repeated for >= 1 s, with its clock samples
+  prefill   the same measurement at T=8192 (the metric's second batch size),
+  hash      at T=2048 with hash routing over 384 experts, and
+  skew      at T=4096 with Zipf-skewed load, replicated hot experts and a
+            shared expert (each timed for >= 1 s, with per-stage times)
+  roofline  the dominant kernel (the fused expert launch, or the gate/up
+            grouped GEMM) against the measured peak of its bound: HBM bytes
+            of the touched experts' weights and x when the expert groups sit
+            below the ridge (decode, hash, skew), tensor FLOPs at or above it
+            (prefill)
   cpu_baseline  the CPU oracle timed on this host on a bounded token sample
   quantized both workloads again with quantized routed experts: FP8 E4M3
             with one scale per row, MXFP8 (E4M3, a power-of-two scale per 32
@@ -414,17 +420,20 @@ def stage_times(wl, steps, torch):
 
 
 def touched_bytes(cfg, counts, fused=False):
-    """Algorithmic bytes of the gate/up GEMM: weights of experts with rows,
-    the hidden states read (each token row once: the GEMM gathers the routed
-    rows from x, repeats hit L2) and the SwiGLU output written.  Fused with
-    the down GEMM: all three weight matrices of the touched experts, plus the
-    activations read back and the fp32 expert outputs written."""
+    """Algorithmic bytes of the gate/up GEMM (the survey's definition: the
+    weights of the experts with rows, plus the hidden states read once -- the
+    GEMM gathers the routed rows from x, repeats hit L2); fused with the down
+    GEMM, all three weight matrices of the touched experts.  Returned apart:
+    the intermediate bytes the launch also moves and that are not credited
+    (the activation written; fused: read back too, and the fp32 expert
+    outputs written)."""
     touched = int((counts > 0).sum())
     w = touched * (3 if fused else 2) * cfg.I * cfg.H * 2
-    xa = cfg.T * cfg.H * 2 + cfg.N * cfg.I * 2
+    x = cfg.T * cfg.H * 2
+    inter = cfg.N * cfg.I * 2
     if fused:
-        xa += cfg.N * cfg.I * 2 + cfg.N * cfg.H * 4
-    return w + xa, touched
+        inter += cfg.N * cfg.I * 2 + cfg.N * cfg.H * 4
+    return w + x, touched, inter
 
 
 def q_stage_times(wl, steps, torch):
@@ -447,19 +456,20 @@ def q_stage_times(wl, steps, torch):
 def q_bytes(cfg, counts, kind):
     """Algorithmic bytes of the quantized gate/up and down GEMMs: weight codes
     of the experts with rows (1 byte per element, 1/2 for E2M1) and their
-    scales (fp32 per row, or one byte per 32 elements); gate/up reads each
-    token's codes and scales once (gathered, repeats hit L2) and writes the
-    activation (bf16, or MX E4M3 codes + scales); down reads the activation
-    codes and writes fp32 outputs."""
+    scales (fp32 per row, or one byte per 32 elements), plus the token
+    operand read once: gate/up reads each token's codes and scales (gathered,
+    repeats hit L2), down the activation codes and scales.  The outputs
+    written (the activation, the fp32 expert outputs) are intermediates of the
+    layer and not credited."""
     touched = int((counts > 0).sum())
     H, I, T, N = cfg.H, cfg.I, cfg.T, cfg.N
     if kind == "fp8_row":
-        g = touched * 2 * I * (H + 4) + T * (H + 4) + N * I * 2
-        d = touched * H * (I + 4) + N * (I + 4) + N * H * 4
+        g = touched * 2 * I * (H + 4) + T * (H + 4)
+        d = touched * H * (I + 4) + N * (I + 4)
     else:
         wb = 1.0 if kind == "mxfp8" else 0.5
-        g = touched * 2 * I * (H * wb + H / 32) + T * (H + H / 32) + N * (I + I / 32)
-        d = touched * H * (I * wb + I / 32) + N * (I + I / 32) + N * H * 4
+        g = touched * 2 * I * (H * wb + H / 32) + T * (H + H / 32)
+        d = touched * H * (I * wb + I / 32) + N * (I + I / 32)
     return g, d
 
 
@@ -515,6 +525,53 @@ def q_measure(wl, kind, steps, warmup, torch, barrier, peaks, peak_src, world, b
     wl.disable_quant()
     torch.cuda.empty_cache()
     return res, launches
+
+
+def sustained_run(wl, warmup, torch, barrier, local, world, seconds=1.0):
+    """The workload's forward repeated for about `seconds` (at least 3 steps)
+    with nvidia-smi clock samples over the timed region: the sustained clock
+    and power state of that step."""
+    est = time_device(wl.forward, 3, warmup, torch, barrier) / 3
+    n = max(3, int(seconds / max(est, 1e-6)))
+    with ClockSampler(local) as clk:
+        clk.mark_start()
+        secs = time_device(wl.forward, n, 1, torch, barrier)
+        clk.mark_end()
+    return {"value": world * wl.cfg.T * n / secs, "unit": UNIT,
+            "ms_per_step": 1000.0 * secs / n, "steps": n, "clocks": clk.summary()}
+
+
+def roofline_of(wl, stages, counts, peaks, peak_src):
+    """Roofline of the step's dominant kernel: the fused gate/up + down launch
+    (small groups), else the gate/up launch.  Its bound follows the expert
+    groups' arithmetic intensity: a touched expert's gate/up weights (2 I H
+    bf16) serve its rows at 2 * 2 I H flops per row, i.e. `rows` flop per
+    weight byte; at or above the ridge (measured sustained bf16 flop/s over
+    the measured copy bandwidth) the kernel is tensor-bound, below it
+    HBM-bound.  The other fraction is reported beside it."""
+    cfg = wl.cfg
+    alg_bytes, touched, inter = touched_bytes(cfg, counts, wl.fused)
+    key = "expert_mlp_fused" if wl.fused else "gemm_gateup"
+    t = stages[key] / 1000.0
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops_sustained"]
+    flops = 2.0 * cfg.N * (3 if wl.fused else 2) * cfg.H * cfg.I
+    rows = cfg.N / max(touched, 1)
+    ridge = tc * 1e12 / (hbm * 1e9)
+    gbs, tfs = alg_bytes / t / 1e9, flops / t / 1e12
+    kname = ("grouped_gemm gate/up + SwiGLU + down, one launch (tcgen05)" if wl.fused
+             else "grouped_gemm gate/up + SwiGLU (tcgen05)")
+    hbm_part = {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    tc_part = {"achieved": tfs, "peak": tc, "unit": "TFLOP/s", "frac": tfs / tc,
+               "peak_source": f"{peak_src} bf16_tflops_sustained"}
+    tensor = rows >= ridge and not wl.fused
+    main, other = (tc_part, hbm_part) if tensor else (hbm_part, tc_part)
+    roof = {"kernel": kname, "bound": "tensor" if tensor else "hbm", **main,
+            "traffic": profiled_traffic(key, cfg.name), "algorithmic_bytes": alg_bytes,
+            "uncredited_intermediate_bytes": inter, "touched_experts": touched,
+            "rows_per_touched_expert": rows, "ridge_rows": ridge,
+            "other_bound": {"bound": "hbm" if tensor else "tensor", **other}}
+    return roof, touched
 
 
 def e2e_time(wl, steps, warmup, torch):
@@ -615,8 +672,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode")
-    ap.add_argument("--secondary", default="prefill",
-                    help="second workload reported in the same line ('' to skip)")
+    ap.add_argument("--secondary", default="prefill,hash,skew",
+                    help="comma-separated further workloads reported in the same line, each "
+                         "under its own key ('' to skip); quantized experts are measured on "
+                         "the first of them")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -698,18 +757,9 @@ def main(argv=None):
     stages = stage_times(wl, min(args.steps, 20), torch)
     counts = wl.counts.cpu().numpy()
     peaks, peak_src = load_peaks()
-    alg_bytes, touched = touched_bytes(cfg, counts, wl.fused)
-    g1 = stages["expert_mlp_fused" if wl.fused else "gemm_gateup"] / 1000.0
-    hbm = peaks["hbm_gbs"]
-    kname = ("grouped_gemm gate/up + SwiGLU + down, one launch (tcgen05)" if wl.fused
-             else "grouped_gemm gate/up + SwiGLU (tcgen05)")
-    roof = {"kernel": kname, "bound": "hbm",
-            "achieved": alg_bytes / g1 / 1e9, "peak": hbm, "unit": "GB/s",
-            "frac": alg_bytes / g1 / 1e9 / hbm,
-            "traffic": profiled_traffic("expert_mlp_fused" if wl.fused else "gemm_gateup",
-                                        cfg.name),
-            "algorithmic_bytes": alg_bytes, "touched_experts": touched,
-            "peak_source": f"{peak_src} hbm_gbs"}
+    roof, touched = roofline_of(wl, stages, counts, peaks, peak_src)
+    # the same step repeated for >= 1 s: the sustained clock / power state
+    sustained = sustained_run(wl, args.warmup, torch, barrier, local, world)
     t_e2e, h2d, d2h = e2e_time(wl, args.steps, args.warmup, torch)
     e2e = {"value": world * cfg.T * args.steps / t_e2e, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -725,8 +775,8 @@ def main(argv=None):
                    "l2": "inputs larger than L2 (the step streams the touched experts' weights, "
                          f"{touched * 3 * cfg.I * cfg.H * 2 / 1e9:.1f} GB); no flush"},
         "roofline": roof, "stages_ms": stages, "e2e": e2e,
-        "gpu_launches": wl.launches_per_step() * args.steps,
-        "clocks": clocks,
+        "gpu_launches": wl.launches_per_step() * (args.steps + sustained["steps"]),
+        "clocks": clocks, "sustained": sustained,
     }
     if not args.no_quant:
         line["quantized"] = {}
@@ -738,37 +788,20 @@ def main(argv=None):
     del wl
     torch.cuda.empty_cache()
 
-    if args.secondary:
-        c2 = workload(args.secondary)
+    for i, name2 in enumerate([w for w in args.secondary.split(",") if w]):
+        c2 = workload(name2)
         w2 = Workload(c2, dev)
         w2.forward()
-        # long enough (>= ~1 s) for the clock samples to see the sustained,
-        # power-limited state of a prefill-sized step
-        est = time_device(w2.forward, 3, args.warmup, torch, barrier) / 3
-        steps2 = max(3, args.steps // 2, int(1.0 / max(est, 1e-6)))
-        with ClockSampler(local) as clk2:
-            clk2.mark_start()
-            s2 = time_device(w2.forward, steps2, 1, torch, barrier)
-            clk2.mark_end()
+        torch.cuda.synchronize()
+        res = sustained_run(w2, args.warmup, torch, barrier, local, world)
+        res = {"workload": c2.name, "T": c2.T, **res}
         stg2 = stage_times(w2, min(args.steps, 10), torch)
-        flops = 2.0 * c2.N * (3 if w2.fused else 2) * c2.H * c2.I
-        g1b = stg2["expert_mlp_fused" if w2.fused else "gemm_gateup"] / 1000.0
-        peak_t = peaks["bf16_tflops_sustained"]
-        line["prefill" if args.secondary == "prefill" else args.secondary] = {
-            "workload": c2.name, "T": c2.T,
-            "value": world * c2.T * steps2 / s2, "unit": UNIT,
-            "ms_per_step": 1000.0 * s2 / steps2, "steps": steps2, "stages_ms": stg2,
-            "clocks": clk2.summary(),
-            "layer_tflops": 2.0 * c2.N * 3 * c2.H * c2.I / (s2 / steps2) / 1e12,
-            "roofline": {"kernel": "grouped_gemm gate/up + SwiGLU (tcgen05)", "bound": "tensor",
-                         "achieved": flops / g1b / 1e12, "peak": peak_t, "unit": "TFLOP/s",
-                         "frac": flops / g1b / 1e12 / peak_t,
-                         "traffic": profiled_traffic(
-                             "expert_mlp_fused" if w2.fused else "gemm_gateup", c2.name),
-                         "peak_source": f"{peak_src} bf16_tflops_sustained"},
-        }
-        line["gpu_launches"] += w2.launches_per_step() * steps2
-        if not args.no_quant:
+        res["stages_ms"] = stg2
+        res["layer_tflops"] = 2.0 * c2.N * 3 * c2.H * c2.I / (res["ms_per_step"] / 1e3) / 1e12
+        res["roofline"], _ = roofline_of(w2, stg2, w2.counts.cpu().numpy(), peaks, peak_src)
+        line[c2.name] = res
+        line["gpu_launches"] += w2.launches_per_step() * res["steps"]
+        if i == 0 and not args.no_quant:
             for kind in kinds:
                 r, nl = q_measure(w2, kind, min(args.steps, 20), args.warmup, torch, barrier,
                                   peaks, peak_src, world, "tensor", local)

@@ -171,6 +171,23 @@ int gbmoe_validate_log2phy(const int32_t* log2phy_host, const int32_t* replica_c
 int gbmoe_check_device_status(gbmoe_stream_t stream, int* status);
 
 /*
+ * gbmoe_set_wait_limit_ns — wall-clock limit of every bounded wait inside
+ * the grouped-GEMM kernels launched after this call (the pipeline's stage
+ * waits, and the fused launch's wait for an expert's activations).  A wait
+ * that runs out records GBMOE_ERR_TIMEOUT in the device status; the launch
+ * then lets its in-flight copies and MMAs finish (under a fixed limit of its
+ * own), frees its tensor memory and returns, leaving the context usable.
+ * The vLLM-Ascend page's "Where It Breaks" section traces hangs of the MoE
+ * path; this library turns such a stall into a reported error.
+ *   ns = 0 restores the default (4 s).  Process-wide, thread-safe; launches
+ *   already enqueued keep the limit they were launched with.  A very small
+ *   limit makes healthy launches give up too (that is how the timeout path
+ *   is tested); their outputs are then unspecified.
+ * Returns the previous limit in nanoseconds.
+ */
+uint64_t gbmoe_set_wait_limit_ns(uint64_t ns);
+
+/*
  * moe_route — router scoring and expert selection ("Stage 2: Select
  * Experts"), then the logical -> physical mapping ("Stage 4", step 2: map
  * logical topk_ids through log2phy).
@@ -224,7 +241,11 @@ size_t gbmoe_permute_workspace_size(int T, int k, int E_phys);
  *   row_to_token [T*k] int32 out; flat_to_row [T*k] int32 out
  *   x_perm       [T*k, H] bf16 out (x_perm[r] = x[row_to_token[r]]), or NULL
  *   ws           device scratch of ws_bytes >= gbmoe_permute_workspace_size()
- * An id outside [0, E_phys) sets GBMOE_ERR_DEVICE and is skipped.
+ * An id outside [0, E_phys) sets GBMOE_ERR_DEVICE and is skipped: it is not
+ * counted, gets no row (its flat_to_row entry is -1), and offsets[E_phys] is
+ * then below T*k; row_to_token entries from offsets[E_phys] on are not written
+ * and those x_perm rows are zero-filled (x is read only through rows that the
+ * permutation wrote).
  */
 int moe_permute(const int32_t* ids_phys, int T, int k, int E_phys, const uint16_t* x, int H,
                 int32_t* counts, int32_t* offsets, int32_t* row_to_token, int32_t* flat_to_row,
@@ -333,6 +354,8 @@ int gbmoe_expert_mlp_fused(int E_phys, int N, int H);
  * in fp32, summed in the fixed order j = 0..k-1, then the shared term.
  *   y [T*k, H] fp32; flat_to_row [T*k]; weights [T, k] fp32;
  *   shared_y [T, H] fp32 or NULL; out [T, H] bf16.  H multiple of 8.
+ * A flat_to_row entry outside [0, T*k) (moe_permute writes -1 for a skipped
+ * id) contributes nothing and sets GBMOE_ERR_DEVICE in the device status.
  */
 int moe_combine(const float* y, const int32_t* flat_to_row, const float* weights,
                 const float* shared_y, int T, int k, int H, uint16_t* out,

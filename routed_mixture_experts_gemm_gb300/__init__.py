@@ -26,7 +26,7 @@ __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_per
            "moe_gemm_gateup_act_fp8", "moe_gemm_down_fp8", "quantize_experts_fp8",
            "moe_quantize_mx_rows", "moe_gemm_gateup_act_mx", "moe_gemm_down_mx",
            "quantize_experts_mx", "moe_latent_tail", "MoELayer", "moe_forward",
-           "moe_forward_host", "check_device_status", "library"]
+           "moe_forward_host", "check_device_status", "set_wait_limit_ns", "library"]
 
 
 class GbmoeError(RuntimeError):
@@ -440,6 +440,12 @@ def moe_forward_host(layer: MoELayer, x_host, input_ids_host=None, out_host=None
                                 _ptr(out_host), _ptr(ids_log_host), _ptr(ws), ws.numel(),
                                 _stream(stream)), "moe_forward_host")
     return out_host
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of the grouped GEMMs' bounded waits for launches made from now
+    on (0: the default, 4 s); returns the previous limit."""
+    return int(_lib.load().gbmoe_set_wait_limit_ns(int(ns)))
 
 
 def check_device_status(stream=None) -> int:

@@ -44,6 +44,7 @@ SIGNATURES = {
     "gbmoe_validate_route_cfg": (_i, [_P(RouteCfg)]),
     "gbmoe_validate_log2phy": (_i, [_vp, _vp, _i, _i, _i]),
     "gbmoe_check_device_status": (_i, [_vp, _P(_i)]),
+    "gbmoe_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "moe_route": (_i, [_P(RouteCfg), _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp,
                        _i, _vp, _vp, _vp, _vp, _vp]),
     "moe_expert_counts": (_i, [_vp, _i, _i, _i, _vp, _i, _vp]),

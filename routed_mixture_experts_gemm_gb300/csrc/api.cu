@@ -20,8 +20,8 @@ __device__ int g_status_word = 0;
 namespace {
 
 std::mutex g_ctx_mu;
-DevCtx g_ctx[64];
-bool g_ctx_ok[64];
+DevCtx g_ctx[kMaxDevices];
+bool g_ctx_ok[kMaxDevices];
 
 constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
@@ -155,9 +155,23 @@ int check_layer(const gbmoe_layer* L) {
 
 }  // namespace
 
+int check_permute_args(const int32_t* ids_phys, int T, int k, int E_phys, const uint16_t* x,
+                       int H, const int32_t* counts, const int32_t* offsets,
+                       const int32_t* row_to_token, const int32_t* flat_to_row,
+                       const uint16_t* x_perm, int64_t* N) {
+    if (T < 0 || k < 1 || E_phys < 1 || E_phys > kMaxE) return GBMOE_ERR_INVALID_ARG;
+    if (!counts || !offsets) return GBMOE_ERR_INVALID_ARG;
+    if (T > 0 && (!ids_phys || !row_to_token || !flat_to_row)) return GBMOE_ERR_INVALID_ARG;
+    if (x_perm && (!x || H <= 0 || H % 8 || !aligned16(x) || !aligned16(x_perm)))
+        return GBMOE_ERR_INVALID_ARG;
+    *N = static_cast<int64_t>(T) * k;
+    if (*N > INT32_MAX) return GBMOE_ERR_UNSUPPORTED;
+    return GBMOE_OK;
+}
+
 const DevCtx* device_ctx() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_ctx_mu);
     if (!g_ctx_ok[dev]) {
         DevCtx c;
@@ -193,6 +207,8 @@ const char* gbmoe_status_string(int status) {
 }
 
 int gbmoe_validate_route_cfg(const gbmoe_route_cfg* cfg) { return check_cfg(cfg); }
+
+uint64_t gbmoe_set_wait_limit_ns(uint64_t ns) { return set_gemm_wait_limit_ns(ns); }
 
 int gbmoe_validate_log2phy(const int32_t* log2phy_host, const int32_t* replica_cnt_host,
                            int E_log, int R_max, int E_phys) {
@@ -280,13 +296,10 @@ size_t gbmoe_permute_workspace_size(int T, int k, int E_phys) {
 int moe_permute(const int32_t* ids_phys, int T, int k, int E_phys, const uint16_t* x, int H,
                 int32_t* counts, int32_t* offsets, int32_t* row_to_token, int32_t* flat_to_row,
                 uint16_t* x_perm, void* ws, size_t ws_bytes, gbmoe_stream_t stream) {
-    if (T < 0 || k < 1 || E_phys < 1 || E_phys > kMaxE) return GBMOE_ERR_INVALID_ARG;
-    if (!counts || !offsets) return GBMOE_ERR_INVALID_ARG;
-    if (T > 0 && (!ids_phys || !row_to_token || !flat_to_row)) return GBMOE_ERR_INVALID_ARG;
-    if (x_perm && (!x || H <= 0 || H % 8 || !aligned16(x) || !aligned16(x_perm)))
-        return GBMOE_ERR_INVALID_ARG;
-    const int64_t N = static_cast<int64_t>(T) * k;
-    if (N > INT32_MAX) return GBMOE_ERR_UNSUPPORTED;
+    int64_t N = 0;
+    const int st = check_permute_args(ids_phys, T, k, E_phys, x, H, counts, offsets,
+                                      row_to_token, flat_to_row, x_perm, &N);
+    if (st) return st;
     if (N > 0 && (!ws || ws_bytes < permute_ws_bytes(N, E_phys))) return GBMOE_ERR_WORKSPACE;
     const DevCtx* ctx = device_ctx();
     if (!ctx) return GBMOE_ERR_CUDA;

@@ -42,16 +42,22 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) {
     return v;
 }
 
+// A row outside [0, n_rows) (the permutation marks a skipped id with -1)
+// contributes nothing: its slot is neither read nor added, and the device
+// status records the bad entry.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const float4* __restrict__ y, const int32_t* __restrict__ flat_to_row,
     const float* __restrict__ weights, const float4* __restrict__ shared_y, int k, int H,
-    uint4* __restrict__ out) {
+    int64_t n_rows, uint4* __restrict__ out, int* status) {
     __shared__ int64_t rows[kMaxK];
     __shared__ float wts[kMaxK];
     const int t = blockIdx.x;
     if (threadIdx.x < k) {
-        rows[threadIdx.x] = flat_to_row[static_cast<int64_t>(t) * k + threadIdx.x];
-        wts[threadIdx.x] = weights[static_cast<int64_t>(t) * k + threadIdx.x];
+        const int64_t r = flat_to_row[static_cast<int64_t>(t) * k + threadIdx.x];
+        const bool ok = r >= 0 && r < n_rows;
+        if (!ok && blockIdx.y == 0) record_error(status, GBMOE_ERR_DEVICE);
+        rows[threadIdx.x] = ok ? r : -1;
+        wts[threadIdx.x] = ok ? weights[static_cast<int64_t>(t) * k + threadIdx.x] : 0.0f;
     }
     __syncthreads();
     const int v = blockIdx.y * kCombineThreads + threadIdx.x;  // group of 8 outputs
@@ -64,7 +70,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
         float4 a[kCombineGroup], b[kCombineGroup];
 #pragma unroll
         for (int g = 0; g < kCombineGroup; ++g) {
-            if (j0 + g < k) {
+            if (j0 + g < k && rows[j0 + g] >= 0) {
                 const float4* src = y + rows[j0 + g] * v4_per_row + 2 * v;
                 a[g] = ld_stream(src);
                 b[g] = ld_stream(src + 1);
@@ -72,7 +78,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
         }
 #pragma unroll
         for (int g = 0; g < kCombineGroup; ++g)
-            if (j0 + g < k) fma8(acc, wts[j0 + g], a[g], b[g]);
+            if (j0 + g < k && rows[j0 + g] >= 0) fma8(acc, wts[j0 + g], a[g], b[g]);
     }
     if (shared_y) {
         const float4* src = shared_y + static_cast<int64_t>(t) * v4_per_row + 2 * v;
@@ -99,12 +105,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 cudaError_t launch_combine(const float* y, const int32_t* flat_to_row, const float* weights,
                            const float* shared_y, int T, int k, int H, uint16_t* out,
                            const DevCtx& ctx, cudaStream_t s) {
-    (void)ctx;
     if (T == 0) return cudaSuccess;
     const dim3 grid(T, (H / 8 + kCombineThreads - 1) / kCombineThreads);
     combine_kernel<<<grid, kCombineThreads, 0, s>>>(
         reinterpret_cast<const float4*>(y), flat_to_row, weights,
-        reinterpret_cast<const float4*>(shared_y), k, H, reinterpret_cast<uint4*>(out));
+        reinterpret_cast<const float4*>(shared_y), k, H, static_cast<int64_t>(T) * k,
+        reinterpret_cast<uint4*>(out), ctx.status);
     return cudaGetLastError();
 }
 

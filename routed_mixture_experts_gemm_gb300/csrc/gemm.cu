@@ -48,6 +48,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -67,7 +68,7 @@ constexpr int LOADER_THREADS = 32 * LOADER_WARPS;
 constexpr int LOADER_WARP0 = 2 + EPI_WARPS;
 constexpr int MAX_GROUPS = 1024;
 constexpr int NUM_THREADS = 32 * (LOADER_WARP0 + LOADER_WARPS);
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // default limit of the bounded waits
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kCopyLag = 2;      // token stages in flight on the cp.async path (x2 for rings of 8+)
 
@@ -167,6 +168,9 @@ struct GemmArgs {
     const uint8_t* w_sf1;
     uint8_t* out_sf;
     uint32_t a_fmt;
+    // wall-clock limit of every bounded pipeline wait (set at launch from the
+    // process-wide setting; the drains of the error path keep their own)
+    uint64_t wait_ns;
 };
 
 // The second GEMM of the fused mode (paired down tiles) and the per-group
@@ -338,6 +342,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = args.groups;
+    const uint64_t wait_ns = args.wait_ns;
     constexpr int WROWS1 = MODE1 == kDownPair ? 2 * BM : BM;  // weight rows per first-GEMM tile
     const int rb1 = args.R / WROWS1;
     const int rb2 = FUSED ? fz.R / (2 * BM) : 0;
@@ -471,7 +476,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait_bounded(aempty + stage, phase ^ 1u, abort_flag, args.status,
-                                       kWaitLimitNs)) {
+                                       wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -561,7 +566,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     for (uint32_t it = 0; ld_acquire_gpu(fz.ready + tl.p) < need; ++it) {
                         if ((it & 63u) == 63u) {
                             if (*abort_flag) { got = false; break; }
-                            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            if (global_timer_ns() - t0 > wait_ns) {
                                 *abort_flag = 1;
                                 record_error(args.status, GBMOE_ERR_TIMEOUT);
                                 got = false;
@@ -624,7 +629,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 bool free_ok = true;
                 if (lead)
                     free_ok = mbar_wait_bounded(bempty + stage, phase ^ 1u, abort_flag,
-                                                args.status, kWaitLimitNs);
+                                                args.status, wait_ns);
                 if (!all_agree(free_ok)) {
                     ok = false;
                     break;
@@ -718,14 +723,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const uint32_t idesc = MXS ? idesc_mx(BM, n_mma, args.a_fmt, 0u, 0u)
                                  : EB == 2 ? idesc_bf16_f32(BM, n_mma) : idesc_e4m3_f32(BM, n_mma);
             if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, args.status,
-                                   kWaitLimitNs))
+                                   wait_ns))
                 break;
             tc_fence_after();
             const uint32_t d0 = tmem_base + acc * L::ACC_COLS;
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
-                if (!mbar_wait_bounded(afull + as, aph, abort_flag, args.status, kWaitLimitNs) ||
-                    !mbar_wait_bounded(bfull + bs, bph, abort_flag, args.status, kWaitLimitNs)) {
+                if (!mbar_wait_bounded(afull + as, aph, abort_flag, args.status, wait_ns) ||
+                    !mbar_wait_bounded(bfull + bs, bph, abort_flag, args.status, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -799,7 +804,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             Tile tl;
             job(tau, second, tl);
             const bool got = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, args.status,
-                                               kWaitLimitNs);
+                                               wait_ns);
             if (!epi_bar_all(got)) break;
             tc_fence_after();
             const int mode = second ? kDownPair : MODE1;
@@ -1041,12 +1046,17 @@ bool make_gemm_maps_mx(GemmMaps* g, int fmt, const void* a0, const void* a1,
            make_map_u8(&g->b64, b, n_rows, K, 64) && make_map_u8(&g->b128, b, n_rows, K, 128);
 }
 
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+
+// Launch-time settings every grouped-GEMM launch carries.
+void stamp(GemmArgs& a) { a.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 std::mutex g_attr_mu;
-bool g_attr_done[64];
+bool g_attr_done[kMaxDevices];
 
 cudaError_t ensure_attrs(int device) {
     std::lock_guard<std::mutex> lk(g_attr_mu);
-    if (device >= 0 && device < 64 && g_attr_done[device]) return cudaSuccess;
+    if (device >= 0 && device < kMaxDevices && g_attr_done[device]) return cudaSuccess;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
     cudaError_t e = cudaFuncSetAttribute(GEMM1_SMALL, a, Gemm1Small::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_LARGE, a, Gemm1Large::SMEM_BYTES);
@@ -1063,7 +1073,7 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_DEC, a, GemmMxDec::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_DEC, a, GemmMxDec::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (device >= 0 && device < 64) g_attr_done[device] = true;
+    if (device >= 0 && device < kMaxDevices) g_attr_done[device] = true;
     return cudaSuccess;
 }
 
@@ -1090,6 +1100,10 @@ bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint
 
 int gemm_max_groups() { return MAX_GROUPS; }
 
+uint64_t set_gemm_wait_limit_ns(uint64_t ns) {
+    return g_wait_limit_ns.exchange(ns ? ns : kWaitLimitNs);
+}
+
 bool gemm_fused_eligible(int groups, int n_rows, int H) {
     return n_rows > 0 && n_rows < kLargeGateUpRows * groups && H % 256 == 0;
 }
@@ -1106,8 +1120,9 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* row_to_token, int 
                         row_to_token ? src_rows : n_rows, H))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
-    const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
-                     row_to_token, row_to_token ? x_rows : nullptr, src_rows, activation};
+    GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
+               row_to_token, row_to_token ? x_rows : nullptr, src_rows, activation};
+    stamp(a);
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
@@ -1127,7 +1142,8 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
     if (!make_gemm_maps(&m, w_down, nullptr, static_cast<uint64_t>(groups) * H, act, n_rows, I))
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
-    const GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
+    GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
+    stamp(a);
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (H % 256 == 0 && n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, H / 2, 256, ctx.num_sms);
@@ -1158,8 +1174,9 @@ int launch_gemm_mlp_fused(const uint16_t* x_rows, const int32_t* row_to_token, i
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     if (cudaMemsetAsync(ready, 0, sizeof(int) * groups, s) != cudaSuccess) return GBMOE_ERR_CUDA;
-    const GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
-                     row_to_token, row_to_token ? x_rows : nullptr, src_rows, activation};
+    GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
+               row_to_token, row_to_token ? x_rows : nullptr, src_rows, activation};
+    stamp(a);
     const FusedArgs f{H, I, y, ready};
     // every CTA must be resident (down tiles wait on gate/up tiles of other
     // CTAs): a cooperative launch of at most one CTA per SM
@@ -1190,6 +1207,7 @@ int launch_gemm_gateup_fp8(const uint8_t* xq, const float* sx, const int32_t* ro
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, I, H, act, ctx.status,
                row_to_token, row_to_token ? xq : nullptr, src_rows, activation};
+    stamp(a);
     a.tok_scale = sx;
     a.w_scale0 = sg;
     a.w_scale1 = su;
@@ -1214,6 +1232,7 @@ int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offs
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
+    stamp(a);
     a.tok_scale = sa;
     a.w_scale0 = sd;
     const FusedArgs none{0, 0, nullptr, nullptr};
@@ -1236,6 +1255,7 @@ int launch_gemm_gateup_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* r
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, I, H, aq, ctx.status,
                row_to_token, row_to_token ? xq : nullptr, src_rows, activation};
+    stamp(a);
     a.tok_sf = xs;
     a.w_sf0 = sg;
     a.w_sf1 = su;
@@ -1263,6 +1283,7 @@ int launch_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* off
         return GBMOE_ERR_CUDA;
     if (ensure_attrs(ctx.device) != cudaSuccess) return GBMOE_ERR_CUDA;
     GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
+    stamp(a);
     a.tok_sf = as;
     a.w_sf0 = sd;
     a.a_fmt = w_fmt == kMxE2M1 ? 5u : 0u;

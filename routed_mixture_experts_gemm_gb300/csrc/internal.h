@@ -11,6 +11,10 @@
 
 namespace gbmoe {
 
+// Per-device host state (contexts, kernel attributes, scratch addresses) is
+// kept for device ordinals below this bound.
+constexpr int kMaxDevices = 64;
+
 struct DevCtx {
     int device;
     int num_sms;
@@ -53,6 +57,12 @@ cudaError_t launch_expert_counts(const int32_t* ids, int64_t n, int E_phys, int3
 
 // --- permutation (permute.cu) ---
 constexpr int kPermChunk = 256;  // flat (token, slot) pairs per scatter worker
+// Argument checks shared by moe_permute and moe_permute_static (api.cu):
+// GBMOE_OK or the status the entry point returns; *N receives T * k.
+int check_permute_args(const int32_t* ids_phys, int T, int k, int E_phys, const uint16_t* x,
+                       int H, const int32_t* counts, const int32_t* offsets,
+                       const int32_t* row_to_token, const int32_t* flat_to_row,
+                       const uint16_t* x_perm, int64_t* N);
 size_t permute_ws_bytes(int64_t N, int E_phys);
 cudaError_t launch_permute(const int32_t* ids_phys, int64_t N, int k, int E_phys,
                            const uint16_t* x, int H, int32_t* counts, int32_t* offsets,
@@ -71,6 +81,9 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
                      int I, const uint16_t* w_down, float* y, const DevCtx& ctx,
                      cudaStream_t s);
 int gemm_max_groups();
+// Limit of the bounded pipeline waits of grouped-GEMM launches made from now
+// on (0: the default, 4 s); returns the previous limit.
+uint64_t set_gemm_wait_limit_ns(uint64_t ns);
 // Whether moe_forward runs both GEMMs in one fused cooperative launch (small
 // groups: decode-like batches).
 bool gemm_fused_eligible(int groups, int n_rows, int H);

@@ -18,6 +18,7 @@
 //               group is the popcount of lower lanes
 //   4. gather:  x_perm[r] = x[row_to_token[r]] with 16-byte vector copies
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -162,6 +163,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) perm_scatter_kernel(
             const int r = offsets[p] + base[p] + run[p] + rank;
             row_to_token[r] = static_cast<int32_t>(f / k);
             flat_to_row[f] = r;
+        } else if (f < N) {
+            flat_to_row[f] = -1;  // id outside [0, P): no row
         }
         __syncwarp();
         if (p >= 0 && rank == 0) run[p] += __popc(peers);
@@ -265,6 +268,8 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(
             const int r = offs[p] + h[p] + rank;
             row_to_token[r] = static_cast<int32_t>(f / k);
             flat_to_row[f] = r;
+        } else if (f < f1) {
+            flat_to_row[f] = -1;  // id outside [0, P): no row
         }
         __syncwarp();
         if (p >= 0 && rank == 0) h[p] += __popc(peers);
@@ -274,7 +279,9 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(
 
 // x_perm[r] = x[row_to_token[r]]: one warp per row, four 16-byte loads in
 // flight per lane; x rows are kept in L2 (each is read k times), x_perm is
-// streamed out.
+// streamed out.  Only the offsets[P] rows the permutation wrote carry a token
+// (ids outside [0, P) get no row): the rows after them are zero-filled and
+// x is not read for them.
 __device__ __forceinline__ uint4 ld_keep(const uint4* p, uint64_t pol) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
@@ -292,14 +299,20 @@ constexpr int kGatherWarps = 8;
 
 __global__ void __launch_bounds__(32 * kGatherWarps) perm_gather_kernel(
     const uint4* __restrict__ x, int64_t N, int vec_per_row,
-    const int32_t* __restrict__ row_to_token, uint4* __restrict__ x_perm) {
+    const int32_t* __restrict__ row_to_token, const int32_t* __restrict__ rows_written,
+    uint4* __restrict__ x_perm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+    const int64_t n_rows = min(N, static_cast<int64_t>(max(0, *rows_written)));
     for (int64_t r = static_cast<int64_t>(blockIdx.x) * kGatherWarps + warp; r < N;
          r += static_cast<int64_t>(gridDim.x) * kGatherWarps) {
+        uint4* dst = x_perm + r * vec_per_row;
+        if (r >= n_rows) {
+            for (int v = lane; v < vec_per_row; v += 32) st_stream(dst + v, make_uint4(0, 0, 0, 0), stream);
+            continue;
+        }
         const int64_t t = row_to_token[r];
         const uint4* src = x + t * vec_per_row;
-        uint4* dst = x_perm + r * vec_per_row;
         for (int v0 = 0; v0 < vec_per_row; v0 += 128) {
             uint4 buf[4];
 #pragma unroll
@@ -314,6 +327,22 @@ __global__ void __launch_bounds__(32 * kGatherWarps) perm_gather_kernel(
             }
         }
     }
+}
+
+// The small kernel's shared-memory limit is raised once per device (under a
+// lock: first calls may come from several host threads at once).
+std::mutex g_small_attr_mu;
+bool g_small_attr_done[kMaxDevices];
+
+cudaError_t ensure_small_attr(int device) {
+    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_small_attr_mu);
+    if (g_small_attr_done[device]) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(
+        perm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>(sizeof(int32_t) * 33 * kSmallPermMaxP));
+    if (e == cudaSuccess) g_small_attr_done[device] = true;
+    return e;
 }
 
 }  // namespace
@@ -335,15 +364,8 @@ cudaError_t launch_permute(const int32_t* ids_phys, int64_t N, int k, int E_phys
     }
     if (N <= kSmallPermMaxN && P <= kSmallPermMaxP) {
         const size_t smem = sizeof(int32_t) * 33 * P;
-        static bool attr_done[64];
-        if (ctx.device >= 0 && ctx.device < 64 && !attr_done[ctx.device]) {
-            cudaError_t e = cudaFuncSetAttribute(perm_small_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(sizeof(int32_t) * 33 *
-                                                                  kSmallPermMaxP));
-            if (e != cudaSuccess) return e;
-            attr_done[ctx.device] = true;
-        }
+        const cudaError_t e = ensure_small_attr(ctx.device);
+        if (e != cudaSuccess) return e;
         perm_small_kernel<<<1, 1024, smem, s>>>(ids_phys, N, k, P, counts, offsets, row_to_token,
                                                 flat_to_row, ctx.status);
     } else {
@@ -363,7 +385,7 @@ cudaError_t launch_permute(const int32_t* ids_phys, int64_t N, int k, int E_phys
         const int64_t want = (N + kGatherWarps - 1) / kGatherWarps;
         const int grid = static_cast<int>(std::min<int64_t>(want, 8L * ctx.num_sms));
         perm_gather_kernel<<<grid, 32 * kGatherWarps, 0, s>>>(
-            reinterpret_cast<const uint4*>(x), N, vec, row_to_token,
+            reinterpret_cast<const uint4*>(x), N, vec, row_to_token, offsets + P,
             reinterpret_cast<uint4*>(x_perm));
     }
     return cudaGetLastError();

@@ -33,10 +33,12 @@ constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
 static __device__ __align__(256) unsigned char g_permute_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64];
+void* g_scratch_ptr[kMaxDevices];
 
-// Device address of this device's scratch array (nullptr on failure).
+// Device address of this device's scratch array (nullptr on failure); the
+// device must be the current one.
 void* scratch_ptr(int device) {
+    if (device < 0 || device >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
     if (!g_scratch_ptr[device]) {
         void* p = nullptr;
@@ -55,14 +57,10 @@ extern "C" int moe_permute_static(const int32_t* ids_phys, int T, int k, int E_p
                                   const uint16_t* x, int H, int32_t* counts, int32_t* offsets,
                                   int32_t* row_to_token, int32_t* flat_to_row, uint16_t* x_perm,
                                   gbmoe_stream_t stream) {
-    if (T < 0 || k < 1 || E_phys < 1 || E_phys > 1024) return GBMOE_ERR_INVALID_ARG;
-    if (!counts || !offsets) return GBMOE_ERR_INVALID_ARG;
-    if (T > 0 && (!ids_phys || !row_to_token || !flat_to_row)) return GBMOE_ERR_INVALID_ARG;
-    if (x_perm && (!x || H <= 0 || H % 8 || (reinterpret_cast<uintptr_t>(x) & 15u) ||
-                   (reinterpret_cast<uintptr_t>(x_perm) & 15u)))
-        return GBMOE_ERR_INVALID_ARG;
-    const int64_t N = static_cast<int64_t>(T) * k;
-    if (N > INT32_MAX) return GBMOE_ERR_UNSUPPORTED;
+    int64_t N = 0;
+    const int st = check_permute_args(ids_phys, T, k, E_phys, x, H, counts, offsets,
+                                      row_to_token, flat_to_row, x_perm, &N);
+    if (st) return st;
     if (permute_ws_bytes(N, E_phys) > kStaticScratchBytes) return GBMOE_ERR_WORKSPACE;
     const DevCtx* ctx = device_ctx();
     if (!ctx) return GBMOE_ERR_CUDA;

@@ -615,18 +615,18 @@ using RouterSmall128 = RouterTile<4, 4, 2, 128, 6>;
 #define ROUTER_SMALL128 router_logits_tma_kernel<4, 4, 2, 128, 6>
 
 std::mutex g_route_attr_mu;
-bool g_route_attr_done[64];
+bool g_route_attr_done[kMaxDevices];
 
 cudaError_t ensure_route_attrs(int device) {
     std::lock_guard<std::mutex> lk(g_route_attr_mu);
-    if (device >= 0 && device < 64 && g_route_attr_done[device]) return cudaSuccess;
+    if (device >= 0 && device < kMaxDevices && g_route_attr_done[device]) return cudaSuccess;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
     cudaError_t e = cudaFuncSetAttribute(ROUTER_BIG256, a, RouterBig256::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ROUTER_BIG128, a, RouterBig128::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ROUTER_SMALL256, a, RouterSmall256::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ROUTER_SMALL128, a, RouterSmall128::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (device >= 0 && device < 64) g_route_attr_done[device] = true;
+    if (device >= 0 && device < kMaxDevices) g_route_attr_done[device] = true;
     return cudaSuccess;
 }
 

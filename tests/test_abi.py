@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^(?:const\s+)?(?:int|size_t|char\s*\*|const char\s*\*)\s*\**\s*(\w+)\s*\(",
+    names = re.findall(r"^(?:const\s+)?(?:int|size_t|uint64_t|char\s*\*|const char\s*\*)\s*\**\s*(\w+)\s*\(",
                        src, flags=re.M)
     return sorted(set(names))
 
@@ -179,3 +179,13 @@ def test_quantized_layers_validate_and_size_their_workspace(lib):
                        *([0x1000] * 6))
     for L in (bad_fmt, bad_al, bad_h):
         assert lib.gbmoe_forward_workspace_size(ctypes.byref(L), 64) == 0
+
+
+def test_wait_limit_setting_is_host_side(lib):
+    # process-wide limit of the GEMMs' bounded waits: returns the previous
+    # value, 0 restores the 4 s default (no device work involved)
+    default = 4_000_000_000
+    assert lib.gbmoe_set_wait_limit_ns(0) == default
+    assert lib.gbmoe_set_wait_limit_ns(12345) == default
+    assert lib.gbmoe_set_wait_limit_ns(0) == 12345
+    assert lib.gbmoe_set_wait_limit_ns(0) == default

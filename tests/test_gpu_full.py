@@ -4,9 +4,13 @@ benchmark times (one moe_forward call over the whole batch).
 For every token: router logits, expert ids (logical and physical), routing
 weights and counts are compared bit for bit with the oracle, and the
 permutation (offsets, row_to_token, flat_to_row) too.  Outputs are compared
-on a seeded sample of tokens that the oracle recomputes one by one from
-host-generated expert weights (the GPU's weights come from the bit-identical
-device generator, which is also checked here on one expert).
+on a seeded sample of tokens (at least 32 per workload, with the first and
+the last) that the oracle recomputes one by one from host-generated expert
+weights (the GPU's weights come from the bit-identical device generator,
+which is also checked here on one expert).  The expert MLP is compared row by
+row on every routed row of the two most- and the two least-loaded experts
+(activations and expert outputs, through the same kernels moe_forward runs:
+the largest groups span many token blocks and every K stage of H = 7168).
 """
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -22,7 +26,7 @@ from synth.device import device_case
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
-N_SAMPLE = int(os.environ.get("GBMOE_TEST_SAMPLE", "6"))
+N_SAMPLE = int(os.environ.get("GBMOE_TEST_SAMPLE", "32"))
 
 
 def _np(t):
@@ -68,6 +72,42 @@ def _sampled_outputs(cfg, d, tokens, ids_phys, weights):
     return np.stack(outs)
 
 
+def _assert_tol(got, exp, what):
+    got = np.asarray(got, np.float64)
+    exp = np.asarray(exp, np.float64)
+    err = np.abs(got - exp)
+    bad = err > 1e-2 + 1e-2 * np.abs(exp)
+    assert not bad.any(), f"{what}: {bad.sum()} of {err.size} outside tolerance, max {err.max()}"
+
+
+def _check_extreme_experts(gb, cfg, case, perm):
+    """Every routed row of the two most- and two least-loaded (non-empty)
+    physical experts: act and y of moe_expert_mlp (the kernels and variant
+    moe_forward runs for this shape) against the oracle's expert MLP."""
+    d = case.inputs
+    pl = d["placement"]
+    dv = case.dev
+    counts = _np(perm["counts"])
+    offs = _np(perm["offsets"])
+    r2t = _np(perm["row_to_token"])
+    ready = torch.zeros(cfg.P, dtype=torch.int32, device=DEV)
+    act, y = gb.moe_expert_mlp(case.x, perm["offsets"], dv["w_gate"], dv["w_up"], dv["w_down"],
+                               ready=ready, row_to_token=perm["row_to_token"])
+    assert gb.check_device_status() == 0
+    nz = np.nonzero(counts)[0]
+    order = nz[np.argsort(counts[nz], kind="stable")]
+    picks = sorted({*order[:2].tolist(), *order[-2:].tolist()})
+    for p in picks:
+        r0, r1 = int(offs[p]), int(offs[p + 1])
+        wg, wu, wd = synth.expert_weights_host(cfg, int(pl.phys_to_log[p]))
+        act_o, y_o = oracle.expert_ffn_rows(d["x"][r2t[r0:r1]], wg, wu, wd)
+        _assert_tol(_np(act[r0:r1].float()), synth.bf16_to_f32(act_o),
+                    f"act of slot {p} ({r1 - r0} rows)")
+        _assert_tol(_np(y[r0:r1]), y_o, f"y of slot {p} ({r1 - r0} rows)")
+    del act, y
+    return [(int(p), int(counts[p])) for p in picks]
+
+
 @pytest.mark.parametrize("name", ["decode", "prefill", "hash", "skew"])
 def test_full_size(gb, name):
     cfg = synth.CONFIGS[name]
@@ -97,6 +137,8 @@ def test_full_size(gb, name):
     assert np.array_equal(_np(perm["offsets"]), offs_o)
     assert np.array_equal(_np(perm["row_to_token"]), r2t_o)
     assert np.array_equal(_np(perm["flat_to_row"]), f2r_o)
+    picked = _check_extreme_experts(gb, cfg, case, perm)
+    assert len(picked) >= 2, picked
     rl = gb.moe_route(case.layer.cfg, x=case.x, w_router=case.dev["w_router"],
                       router_bias=case.dev["router_bias"], corr_bias=case.dev["corr_bias"],
                       input_ids=case.input_ids, tid2eid=case.dev["tid2eid"],
@@ -111,7 +153,8 @@ def test_full_size(gb, name):
 
     # sampled outputs, including the first and last token
     rng = np.random.default_rng(cfg.seed + 100)
-    sample = sorted({0, T - 1, *rng.choice(T, N_SAMPLE, replace=False).tolist()})
+    sample = sorted({0, T - 1, *rng.choice(T, min(T, N_SAMPLE), replace=False).tolist()})
+    assert len(sample) >= min(T, 32)
     exp = synth.bf16_to_f32(_sampled_outputs(cfg, d, sample, idp_o, w_o)).astype(np.float64)
     got = _np(out[sample].float()).astype(np.float64)
     err = np.abs(got - exp)
@@ -185,7 +228,8 @@ def _oracle_quantized_rows(cfg, d, kind, q_dev, need, tokens):
 
 @pytest.mark.parametrize("name,kind", [("decode", "fp8_row"), ("decode", "mxfp8"),
                                        ("decode", "w4a8"), ("prefill", "fp8_row"),
-                                       ("prefill", "w4a8")])
+                                       ("prefill", "mxfp8"), ("prefill", "w4a8"),
+                                       ("hash", "w4a8"), ("skew", "fp8_row")])
 def test_full_size_quantized(gb, name, kind):
     cfg = synth.CONFIGS[name]
     case = device_case(cfg, DEV, host_weights=False)
@@ -207,15 +251,20 @@ def test_full_size_quantized(gb, name, kind):
     # sampled outputs, including the first and last token
     rng = np.random.default_rng(cfg.seed + 200)
     sample = sorted({0, T - 1, *rng.choice(T, max(2, N_SAMPLE // 2), replace=False).tolist()})
+    ys = None
+    sw = synth.shared_weights_host(cfg)
+    if sw is not None:  # the shared expert stays bf16
+        _, ys = oracle.expert_ffn_rows(d["x"][sample], *sw)
     need = {}
     for t in sample:
         for j in range(k):
             need.setdefault(int(idp_o[t, j]), []).append((t, j))
     y = _oracle_quantized_rows(cfg, d, kind, q, need, sample)
     exp = []
-    for t in sample:
+    for i, t in enumerate(sample):
         yt = np.stack([y[(t, j)] for j in range(k)])
-        exp.append(oracle.combine(yt, np.arange(k, dtype=np.int32), w_o[t:t + 1], None)[0])
+        exp.append(oracle.combine(yt, np.arange(k, dtype=np.int32), w_o[t:t + 1],
+                                  None if ys is None else ys[i:i + 1])[0])
     exp = synth.bf16_to_f32(np.stack(exp)).astype(np.float64)
     got = _np(out[sample].float()).astype(np.float64)
     err = np.abs(got - exp)

@@ -247,3 +247,64 @@ def test_quantized_forward_small_batches(gb, T, kind):
     assert gb.check_device_status() == 0
     exp = oracle.combine(y, ref["flat_to_row"], ref["weights"], ref.get("ys"))
     assert_within_tol(_bf(out), synth.bf16_to_f32(exp), f"{kind} T={T}")
+
+
+@pytest.mark.parametrize("kind", ["fp8_row", "mxfp8", "w4a8"])
+def test_quantized_forward_with_outliers(gb, kind):
+    """moe_forward with quantized experts on hidden states holding a few
+    entries at +-20 sigma (the generator's own tails stop near 3.5 sigma): the
+    per-row amax of the FP8 scales and the MX block exponents see the outliers,
+    on both sides, and the layer still matches the oracle pipeline."""
+    from synth.device import bf16_dev, device_case
+    cfg = synth.MINI["mini_prefill"]
+    case = device_case(cfg, DEV, host_weights=True)
+    rng = np.random.default_rng(2024)
+    x = case.inputs["x"].copy()
+    T, H = x.shape
+    spots = [(int(t), int(h)) for t, h in zip(rng.choice(T, 24, replace=False),
+                                                rng.integers(0, H, 24))]
+    for i, (t, h) in enumerate(spots):
+        x[t, h] = 0x41A0 if i % 2 == 0 else 0xC1A0  # bf16 bits of +20.0 / -20.0
+    inputs = dict(case.inputs, x=x)
+    xd = bf16_dev(x, DEV)
+    d = case.dev
+    kw = dict(router_bias=d["router_bias"], corr_bias=d["corr_bias"], tid2eid=d["tid2eid"],
+              log2phy=d["log2phy"], replica_cnt=d["replica_cnt"], shared=d["shared"])
+    ref = oracle.run_config(cfg, inputs=inputs, weights=case.weights_host)
+    qo = []
+    if kind == "fp8_row":
+        q = [gb.quantize_experts_fp8(d[n]) for n in ("w_gate", "w_up", "w_down")]
+        layer = gb.MoELayer(case.layer.cfg, d["w_router"], None, None, None,
+                            fp8=[a for pair in q for a in pair], **kw)
+        for w in case.weights_host:
+            P, R, K = w.shape
+            cq, cs = oracle.quantize_rows(w.reshape(P * R, K))
+            qo += [cq.reshape(P, R, K), cs.reshape(P, R)]
+        xq, xs = oracle.quantize_rows(x)
+        _, y = oracle.ffn_grouped_fp8(xq, xs, ref["row_to_token"], ref["offsets"], *qo,
+                                      nthreads=4)
+        # the device quantizer sees the same amax per token
+        xq_d, xs_d = gb.moe_quantize_fp8_rows(xd)
+        assert np.array_equal(_np(xq_d), xq)
+        assert np.array_equal(_np(xs_d).view(np.uint32), xs.view(np.uint32))
+    else:
+        wfmt = "e4m3" if kind == "mxfp8" else "e2m1"
+        q = [gb.quantize_experts_mx(d[n], wfmt) for n in ("w_gate", "w_up", "w_down")]
+        layer = gb.MoELayer(case.layer.cfg, d["w_router"], None, None, None,
+                            mx=[wfmt] + [a for pair in q for a in pair], **kw)
+        for w in case.weights_host:
+            P, R, K = w.shape
+            cq, cs = oracle.mx_quantize_rows(w.reshape(P * R, K), wfmt)
+            qo += [cq.reshape(P, R, -1), cs.reshape(P, R, -1)]
+        xq, xs = oracle.mx_quantize_rows(x, "e4m3")
+        _, _, _, y = oracle.ffn_grouped_mx(xq, xs, ref["row_to_token"], ref["offsets"], *qo,
+                                           wfmt=wfmt, nthreads=4)
+        xq_d, xs_d = gb.moe_quantize_mx_rows(xd, "e4m3")
+        assert np.array_equal(_np(xq_d), xq)
+        assert np.array_equal(_np(xs_d), xs)
+    ids_p = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    out = gb.moe_forward(layer, xd, ids_phys=ids_p)
+    assert gb.check_device_status() == 0
+    assert np.array_equal(_np(ids_p), ref["ids_phys"])
+    exp = oracle.combine(y, ref["flat_to_row"], ref["weights"], ref.get("ys"))
+    assert_within_tol(_bf(out), synth.bf16_to_f32(exp), f"{kind} with outliers")

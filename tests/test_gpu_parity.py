@@ -400,6 +400,60 @@ def test_bad_table_entry_sets_device_status(built):
     assert gb.check_device_status() == 0  # cleared by the read
 
 
+@pytest.mark.parametrize("T", [300, 1500])  # one-block permutation; multi-kernel path
+def test_out_of_range_ids_get_no_row(built, T):
+    """Ids outside [0, P) are reported, not counted and get no row: their
+    flat_to_row entries are -1, x_perm rows past offsets[P] are zero-filled
+    (x is read only through rows the permutation wrote) and the combine adds
+    nothing for them."""
+    gb = built
+    cfg = synth.MINI["mini_decode"].with_T(T)
+    case = device_case(cfg, DEV, host_weights=False)
+    k, P, H = cfg.k, cfg.P, cfg.H
+    o = gb.moe_route(case.layer.cfg, x=case.x, w_router=case.dev["w_router"],
+                     corr_bias=case.dev["corr_bias"])
+    ids = o["ids_phys"].clone()
+    bad = [(0, 1, P + 5), (T // 2, 0, -2), (T - 1, k - 1, 1 << 20)]
+    for t, j, v in bad:
+        ids[t, j] = v
+    assert gb.check_device_status() == 0
+    perm = gb.moe_permute(ids, P, x=case.x)
+    assert gb.check_device_status() == 5  # GBMOE_ERR_DEVICE, then cleared
+    ids_h = _np(ids).reshape(-1)
+    valid = (ids_h >= 0) & (ids_h < P)
+    n_ok = int(valid.sum())
+    assert n_ok == T * k - len(bad)
+    counts = np.bincount(ids_h[valid], minlength=P)
+    assert np.array_equal(_np(perm["counts"]), counts)
+    offs = np.concatenate([[0], np.cumsum(counts)])
+    assert np.array_equal(_np(perm["offsets"]), offs)
+    # stable order over the valid flat indices
+    f_ok = np.nonzero(valid)[0]
+    order = f_ok[np.argsort(ids_h[f_ok], kind="stable")]
+    assert np.array_equal(_np(perm["row_to_token"])[:n_ok], order // k)
+    f2r = _np(perm["flat_to_row"])
+    exp_f2r = np.full(T * k, -1, np.int64)
+    exp_f2r[order] = np.arange(n_ok)
+    assert np.array_equal(f2r, exp_f2r)
+    xp = _np(perm["x_perm"].view(torch.int16))
+    xh = _np(case.x.view(torch.int16))
+    assert np.array_equal(xp[:n_ok], xh[order // k])
+    assert not xp[n_ok:].any()
+    # combine over the same flat_to_row: the bad slots contribute nothing
+    g = torch.Generator(device="cpu").manual_seed(5)
+    y = torch.randn((T * k, H), generator=g).to(DEV)
+    w = torch.rand((T, k), generator=g).to(DEV)
+    out = gb.moe_combine(y, perm["flat_to_row"], w)
+    assert gb.check_device_status() == 5
+    yh, wh = _np(y).astype(np.float64), _np(w).astype(np.float64)
+    exp = np.zeros((T, H))
+    for f in range(T * k):
+        if f2r[f] >= 0:
+            exp[f // k] += wh[f // k, f % k] * yh[f2r[f]]
+    got = _bf(out).astype(np.float64)
+    assert np.all(np.abs(got - exp) <= 2.0 ** -7 * np.abs(exp) + 1e-5)
+
+
 def test_device_generator_matches_host(built):
     cfg = synth.MINI["mini_decode"]
     n = cfg.I * cfg.H
@@ -519,3 +573,31 @@ def test_expert_mlp_fused_and_separate(built, shape, fused, gather):
                 rpb = 16 * math.ceil(math.ceil(r / math.ceil(r / 128)) / 16)
                 return math.ceil(r / rpb)
             assert _np(ready).tolist() == [(I // 128) * blocks(r) for r in rows]
+
+
+@pytest.mark.parametrize("shape,fused", [MLP_SHAPES[2], MLP_SHAPES[3]])
+def test_bounded_waits_report_timeout_and_context_survives(built, shape, fused):
+    """A wait limit far below a stage's copy time makes the GEMMs' bounded
+    waits run out (every role gives up, drains its in-flight copies and MMAs,
+    frees tensor memory): the launch reports GBMOE_ERR_TIMEOUT through the
+    device status, and the next launch with the default limit is correct."""
+    gb = built
+    H, I, rows = shape
+    d, act_o, _ = _gemm_case(shape)
+    ready = torch.zeros((len(rows),), dtype=torch.int32, device=DEV)
+    assert gb.check_device_status() == 0
+    prev = gb.set_wait_limit_ns(1000)
+    try:
+        gb.moe_expert_mlp(d["x"], d["offs"], d["wg"], d["wu"], d["wd"], ready=ready)
+        assert gb.check_device_status() == 6  # GBMOE_ERR_TIMEOUT
+    finally:
+        assert gb.set_wait_limit_ns(prev) == 1000
+    assert gb.set_wait_limit_ns(0) == prev  # 0 restores the default
+    act, y = gb.moe_expert_mlp(d["x"], d["offs"], d["wg"], d["wu"], d["wd"], ready=ready)
+    assert gb.check_device_status() == 0
+    assert_within_tol(_bf(act), synth.bf16_to_f32(act_o), f"act after timeout {shape}")
+    # the full layer still runs on this context
+    case, ref = case_and_ref("mini_decode")
+    out = gb.moe_forward(case.layer, case.x)
+    assert gb.check_device_status() == 0
+    assert_within_tol(_bf(out), synth.bf16_to_f32(ref["out"]), "forward after timeout")
