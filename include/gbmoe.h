@@ -182,7 +182,10 @@ int gbmoe_check_device_status(gbmoe_stream_t stream, int* status);
  *   ns = 0 restores the default (4 s).  Process-wide, thread-safe; launches
  *   already enqueued keep the limit they were launched with.  A very small
  *   limit makes healthy launches give up too (that is how the timeout path
- *   is tested); their outputs are then unspecified.
+ *   is tested); their outputs are then unspecified.  Waits on a pipeline
+ *   barrier compare the clock between suspended polls of the barrier, so
+ *   their effective limit can exceed a very small setting; the fused
+ *   launch's wait for an expert's activations polls memory and keeps to it.
  * Returns the previous limit in nanoseconds.
  */
 uint64_t gbmoe_set_wait_limit_ns(uint64_t ns);

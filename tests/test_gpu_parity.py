@@ -472,6 +472,11 @@ GEMM_SHAPES = [
     (512, 128, [40, 3, 17, 0, 90]),     # 128-token gate/up; paired down
     (256, 384, [260, 140]),             # 256-token gate/up; paired down
     (768, 256, [513, 129]),             # several token blocks per group; paired down
+    # CTA-pair tiles (groups averaging >= 96 rows): gate/up with I % 256 == 0,
+    # down with H % 512 == 0; ragged groups leave the odd CTA of a pair some,
+    # or none, of a tile's token rows
+    (1024, 512, [300, 5, 0, 400, 129]),
+    (512, 256, [97, 33, 700, 1]),
 ]
 
 
@@ -522,6 +527,7 @@ MLP_SHAPES = [
     ((1024, 512, [20 + (p * 7) % 23 for p in range(64)]), True),
     ((768, 256, [513, 129]), False),
     ((384, 128, [40, 3, 17, 0, 90]), False),
+    ((1024, 512, [300, 5, 0, 400, 129]), False),  # CTA-pair tiles for both GEMMs
 ]
 
 
@@ -575,13 +581,19 @@ def test_expert_mlp_fused_and_separate(built, shape, fused, gather):
             assert _np(ready).tolist() == [(I // 128) * blocks(r) for r in rows]
 
 
-@pytest.mark.parametrize("shape,fused", [MLP_SHAPES[2], MLP_SHAPES[3]])
-def test_bounded_waits_report_timeout_and_context_survives(built, shape, fused):
-    """A wait limit far below a stage's copy time makes the GEMMs' bounded
-    waits run out (every role gives up, drains its in-flight copies and MMAs,
-    frees tensor memory): the launch reports GBMOE_ERR_TIMEOUT through the
-    device status, and the next launch with the default limit is correct."""
+def test_bounded_waits_report_timeout_and_context_survives(built):
+    """A wait limit of 1 us on the fused launch (64 groups, more tiles than
+    SMs): a down tile's wait for its expert's activations -- a poll of a
+    counter that the other CTAs' gate/up tiles publish -- runs out, the CTA
+    gives up (every role stops, drains its in-flight copies and MMAs, frees
+    tensor memory), the CTAs waiting on its unpublished tiles give up too,
+    and the launch reports GBMOE_ERR_TIMEOUT through the device status; the
+    next launch with the default limit is correct.  (The pipeline's mbarrier
+    waits check the clock between suspended polls, so a tiny limit does not
+    reliably trip them in a short launch.)"""
     gb = built
+    shape, fused = MLP_SHAPES[2]
+    assert fused
     H, I, rows = shape
     d, act_o, _ = _gemm_case(shape)
     ready = torch.zeros((len(rows),), dtype=torch.int32, device=DEV)
