@@ -41,6 +41,18 @@
 // boundary (its weights already stream while it waits: the A ring does not
 // depend on the activations).
 //
+// CTA pairs (prefill-sized groups): two CTAs of a cluster compute one tile
+// with tcgen05.mma.cta_group::2 (M = 256 per A operand), issued by the even
+// CTA.  Each CTA stages its own 128 rows of every A operand and half of the
+// tile's token rows, so a stage per CTA is 48 KB instead of 64 KB (four
+// stages fit) and the tensor cores read the B operand once for two SMs.  The
+// odd CTA's TMA copies complete on the even CTA's full barriers, whose
+// expected byte count the even CTA sets for both halves (no arrival from the
+// odd CTA on the critical path); gathered token rows of the odd CTA are
+// announced by one relaxed remote arrival once they have landed and been
+// fenced; the MMA commits multicast to both CTAs' empty and accumulator
+// barriers.  Each CTA's epilogue drains its own 128 rows for all tokens.
+//
 // Every pipeline wait is bounded (wall-clock limit); a wait that gives up
 // raises an abort flag seen by all roles, records GBMOE_ERR_TIMEOUT, lets
 // in-flight copies and MMAs finish, frees TMEM and returns.
@@ -70,6 +82,10 @@ constexpr int MAX_GROUPS = 1024;
 constexpr int NUM_THREADS = 32 * (LOADER_WARP0 + LOADER_WARPS);
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // default limit of the bounded waits
 constexpr uint64_t kDrainLimitNs = 200000000ull;
+// A CTA pair's odd CTA lands its copies on the even CTA's barriers, so on
+// the error path neither CTA can observe all of the pair's copies complete:
+// both wait this long (copies take microseconds) before the pair exits.
+constexpr uint64_t kPairSettleNs = 2000000ull;
 constexpr int kCopyLag = 2;      // token stages in flight on the cp.async path (x2 for rings of 8+)
 
 // Operand / epilogue modes of the kernel template.
@@ -90,12 +106,19 @@ constexpr int kSwiGLU = 0, kDown = 1, kDownPair = 2, kFused = 3;
 // token rows.  Column j of a group holds, in lane r of every lane quarter,
 // the four scale bytes (the stage's four 32-element K blocks, byte b = block
 // b) of row 32j + r of that operand.
-template <int NUM_A, int BN, int SA, int SB, int ACC_BUFS, int BK, int EB = 2, int MXS = 0>
+//
+// CTA pairs (CG = 2): a tile is computed by two CTAs of a cluster with one
+// tcgen05.mma of M = 256 per A operand, issued by the even CTA; each CTA
+// stages its own 128 rows of every A operand and half of the tile's token
+// rows (BN / 2 per stage), and holds its 128 output rows for all BN tokens in
+// its own tensor memory.
+template <int NUM_A, int BN, int SA, int SB, int ACC_BUFS, int BK, int EB = 2, int MXS = 0,
+          int CG = 1>
 struct Layout {
     static constexpr int ROW_BYTES = BK * EB;
     static constexpr int A_BYTES = BM * ROW_BYTES;
     static constexpr int A_STAGE = NUM_A * A_BYTES;
-    static constexpr int B_BYTES = BN * ROW_BYTES;
+    static constexpr int B_BYTES = (BN / CG) * ROW_BYTES;
     static constexpr int ACC_COLS = NUM_A * BN;
     static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
     // MX: per token stage one 512-byte chunk of scale words per A operand and
@@ -129,6 +152,7 @@ struct Layout {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(SA >= 2 && SB >= 2 && SA <= 16 && SB <= 16, "ring depth");
     static_assert(BN % BOX_ROWS == 0 && BN % (2 * EPI_COLS) == 0 && BN <= 256, "tile width");
+    static_assert(CG == 1 || (CG == 2 && MXS == 0 && BN % 64 == 0), "CTA-pair tiles");
 };
 
 // Tensor maps of one GEMM: the weight operand (a0, a1) and the token operand
@@ -186,21 +210,22 @@ struct Tile {
 };
 
 // A group of cnt rows is cut into token blocks of equal size (a multiple of
-// 16, at most BN): blocks of one weight tile then take the same time and
-// the CTAs running them stay in step, sharing the weight tile through L2.
-__device__ __forceinline__ int block_rows(int cnt, int BN) {
+// G = 16, or 32 for CTA pairs, at most BN): blocks of one weight tile then
+// take the same time and the CTAs running them stay in step, sharing the
+// weight tile through L2.
+__device__ __forceinline__ int block_rows(int cnt, int BN, int G) {
     const int tb = (cnt + BN - 1) / BN;
-    return tb == 0 ? BN : ((cnt + tb - 1) / tb + 15) / 16 * 16;
+    return tb == 0 ? BN : ((cnt + tb - 1) / tb + G - 1) / G * G;
 }
-__device__ __forceinline__ int token_blocks(int cnt, int BN) {
-    const int rpb = block_rows(cnt, BN);
+__device__ __forceinline__ int token_blocks(int cnt, int BN, int G) {
+    const int rpb = block_rows(cnt, BN, G);
     return (cnt + rpb - 1) / rpb;
 }
 
 // Tile tau of a GEMM with `rb` weight blocks per group; tbs[p] is the number
 // of token blocks of groups < p, so group p owns tiles [tbs[p]*rb, tbs[p+1]*rb).
 __device__ __forceinline__ Tile decode_tile(int tau, const int* tbs, const int* gstart,
-                                            const int* gcnt, int P, int rb, int BN) {
+                                            const int* gcnt, int P, int rb, int BN, int G) {
     int lo = 0, hi = P;  // largest p with tbs[p] * rb <= tau
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -208,7 +233,7 @@ __device__ __forceinline__ Tile decode_tile(int tau, const int* tbs, const int* 
     }
     const int p = lo;
     const int cnt = gcnt[p];
-    const int rpb = block_rows(cnt, BN);
+    const int rpb = block_rows(cnt, BN, G);
     const int tb = (cnt + rpb - 1) / rpb;
     const int local = tau - tbs[p] * rb;
     Tile t;
@@ -312,7 +337,7 @@ __device__ __forceinline__ float gated_act(int act, float g, float u) {
 }
 
 template <int NUM_A, int BN, int SA, int SB, int MODE, int ACC_BUFS, int BK, int EB = 2,
-          int MXS = 0>
+          int MXS = 0, int CG = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__ GemmMaps m2,
                     const GemmArgs args, const FusedArgs fz) {
@@ -320,7 +345,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     constexpr int MODE1 = FUSED ? kSwiGLU : MODE;  // mode of the first GEMM's tiles
     static_assert(MODE1 != kDown || NUM_A == 1, "down tiles have one A operand");
     static_assert(MODE1 == kDown || NUM_A == 2, "gate/up and paired tiles have two");
-    using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK, EB, MXS>;
+    constexpr bool PAIR = CG == 2;
+    static_assert(!PAIR || (!FUSED && !MXS && EB == 2), "CTA pairs run the bf16 two-launch GEMMs");
+    constexpr int TG = 16 * CG;  // token-block granularity (an MMA N step per CTA of the tile)
+    using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK, EB, MXS, CG>;
     static_assert(EB == 2 || !FUSED, "the FP8 path runs its GEMMs as two launches");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -343,12 +371,24 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = args.groups;
     const uint64_t wait_ns = args.wait_ns;
-    constexpr int WROWS1 = MODE1 == kDownPair ? 2 * BM : BM;  // weight rows per first-GEMM tile
+    // CTA pairs: cluster rank (the even CTA issues the MMAs) and the tile
+    // stream shared by the pair
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = crank == 0u;
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    constexpr int CROWS1 = MODE1 == kDownPair ? 2 * BM : BM;  // weight rows per CTA and tile
+    constexpr int WROWS1 = CROWS1 * CG;                       // weight rows per first-GEMM tile
     const int rb1 = args.R / WROWS1;
     const int rb2 = FUSED ? fz.R / (2 * BM) : 0;
 
     // ---- set-up: barriers, TMEM, tile table
     if (tid == 0) {
+        // CTA pairs: the odd CTA's copies complete on the even CTA's full
+        // barriers (whose expected bytes the even CTA sets for both halves);
+        // gathered token stages also count the odd CTA's publication, and the
+        // accumulator barriers the odd CTA's epilogue warps
+        const uint32_t peer = (PAIR && leader) ? 1u : 0u;
         for (int s = 0; s < SA; ++s) {
             mbar_init(afull + s, 1);
             mbar_init(aempty + s, 1);
@@ -357,12 +397,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         // thread's (with the copies' bytes) and the published scale columns
         const uint32_t bfull_count = (MXS && args.gather_rows == nullptr) ? 2u : 1u;
         for (int s = 0; s < SB; ++s) {
-            mbar_init(bfull + s, bfull_count);
+            mbar_init(bfull + s, bfull_count + (args.gather_rows != nullptr ? peer : 0u));
             mbar_init(bempty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + b, 1);
-            mbar_init(tempty + b, EPI_WARPS);
+            mbar_init(tempty + b, EPI_WARPS * (1 + peer));
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -378,8 +418,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_base_s, L::TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(tmem_base_s, L::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_base_s, L::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     {
         // tbs[p] = token blocks of groups < p
@@ -399,7 +444,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             }
             gstart[p] = off;
             gcnt[p] = cnt;
-            local += token_blocks(cnt, BN);
+            local += token_blocks(cnt, BN, TG);
         }
         scan[tid] = local;
         __syncthreads();
@@ -416,12 +461,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         int run = scan[tid];
         for (int p = s0; p < s1; ++p) {
             tbs[p] = run;
-            run += token_blocks(gcnt[p], BN);
+            run += token_blocks(gcnt[p], BN, TG);
         }
         if (tid == 0) tbs[P] = scan[NUM_THREADS];
     }
     tc_fence_before();
     __syncthreads();
+    // a pair's barriers are initialised before either CTA arrives on the other's
+    if (PAIR) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_s;
     const int T1 = tbs[P] * rb1;                    // tiles of the first GEMM
@@ -430,8 +477,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     // tile tau -> (which GEMM, tile); the second GEMM exists only when fused
     auto job = [&](int tau, bool& second, Tile& tl) {
         second = FUSED && tau >= T1;
-        tl = second ? decode_tile(tau - T1, tbs, gstart, gcnt, P, rb2, BN)
-                    : decode_tile(tau, tbs, gstart, gcnt, P, rb1, BN);
+        tl = second ? decode_tile(tau - T1, tbs, gstart, gcnt, P, rb2, BN, TG)
+                    : decode_tile(tau, tbs, gstart, gcnt, P, rb1, BN, TG);
     };
 
     // ---------------------------------------------------------- roles
@@ -458,18 +505,20 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             if (MODE1 == kSwiGLU)
                 prefetch_l2_bulk(args.w_sf1 + row * kq, static_cast<uint32_t>(BM * kq));
         };
-        prefetch_sf(blockIdx.x);
-        for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
+        prefetch_sf(unit);
+        for (int tau = unit; tau < total && !*abort_flag; tau += nunits) {
             bool second;
             Tile tl;
             job(tau, second, tl);
-            prefetch_sf(tau + gridDim.x);
+            prefetch_sf(tau + nunits);
             const GemmMaps& m = second ? m2 : m1;
             const int mode = second ? kDownPair : MODE1;
             const int R = second ? fz.R : args.R;
             const int KB = (second ? fz.K : args.K) / BK;
-            const int a_row = tl.p * R + tl.rblk * (mode == kDownPair ? 2 * BM : BM);
-            const uint64_t pol_w = token_blocks(gcnt[tl.p], BN) > 1 ? pol_shared : pol_once;
+            // this CTA's weight rows of the tile (a pair's odd CTA: the second half)
+            const int crows = mode == kDownPair ? 2 * BM : BM;
+            const int a_row = tl.p * R + (tl.rblk * CG + static_cast<int>(crank)) * crows;
+            const uint64_t pol_w = token_blocks(gcnt[tl.p], BN, TG) > 1 ? pol_shared : pol_once;
             // an E2M1 box lands as one byte per element (16 codes in the first
             // 8 bytes of every 16) but completes with its packed size
             const uint32_t a_tx = (MXS && args.a_fmt == 5u) ? L::A_BYTES / 2 : L::A_BYTES;
@@ -480,13 +529,25 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(afull + stage, NUM_A * a_tx);
                 uint8_t* sA = smem + stage * L::A_STAGE;
-                tma_load_2d(sA, &m.a0, afull + stage, kb * BK, a_row, pol_w);
-                if (mode == kSwiGLU)
-                    tma_load_2d(sA + L::A_BYTES, &m.a1, afull + stage, kb * BK, a_row, pol_w);
-                if (mode == kDownPair)
-                    tma_load_2d(sA + L::A_BYTES, &m.a0, afull + stage, kb * BK, a_row + BM, pol_w);
+                if (PAIR && !leader) {
+                    // the odd CTA's half lands here and completes on the even
+                    // CTA's barrier, which expects it
+                    const uint32_t lb = mapa_shared(smem_u32(afull + stage), 0u);
+                    tma_load_2d_pair(sA, &m.a0, lb, kb * BK, a_row, pol_w);
+                    if (mode == kSwiGLU)
+                        tma_load_2d_pair(sA + L::A_BYTES, &m.a1, lb, kb * BK, a_row, pol_w);
+                    if (mode == kDownPair)
+                        tma_load_2d_pair(sA + L::A_BYTES, &m.a0, lb, kb * BK, a_row + BM, pol_w);
+                } else {
+                    mbar_arrive_expect_tx(afull + stage, NUM_A * a_tx * CG);
+                    tma_load_2d(sA, &m.a0, afull + stage, kb * BK, a_row, pol_w);
+                    if (mode == kSwiGLU)
+                        tma_load_2d(sA + L::A_BYTES, &m.a1, afull + stage, kb * BK, a_row, pol_w);
+                    if (mode == kDownPair)
+                        tma_load_2d(sA + L::A_BYTES, &m.a0, afull + stage, kb * BK, a_row + BM,
+                                    pol_w);
+                }
                 armed |= 1u << stage;
                 armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
                 if (++stage == SA) {
@@ -496,10 +557,24 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             }
             if (!ok) break;
         }
-        if (*abort_flag) {  // let every copy this thread issued land before exit
+        if (*abort_flag && PAIR) {
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < kPairSettleNs) {
+            }
+        } else if (*abort_flag) {  // let every copy this thread issued land before exit
             for (int s = 0; s < SA; ++s)
                 if ((armed >> s) & 1u)
                     mbar_wait_timeout(afull + s, (armed_phase >> s) & 1u, kDrainLimitNs);
+        } else if (PAIR) {
+            // every stage consumed: the even CTA's MMA commits to this CTA's
+            // barriers have all landed before the pair exits
+            for (int i = 0; i < SA; ++i) {
+                mbar_wait_timeout(aempty + stage, phase ^ 1u, kDrainLimitNs);
+                if (++stage == SA) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
         }
     } else if (warp >= LOADER_WARP0) {
         // B loaders: token rows, by TMA (lead thread) or gathered by cp.async
@@ -518,8 +593,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         const int chunk = li & 7;       // 16-byte column of the 128-byte row
         const int rbase = li >> 3;      // rows rbase + 16u
         constexpr int RSTEP = LOADER_THREADS / 8;
-        constexpr int RPT = BN / RSTEP;  // rows per thread
-        static_assert(BN % RSTEP == 0, "loader rows");
+        constexpr int RPT = (BN / CG) / RSTEP;  // rows per thread
+        static_assert((BN / CG) % RSTEP == 0, "loader rows");
         const uint64_t pol_x = l2_policy_evict_last();
         // without gathered rows the lead thread alone streams the B ring
         // (with MX block scales every loader thread also stages scale words)
@@ -541,16 +616,26 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const int old = (last - (npend - 1) + SB) % SB;
             fence_proxy_async_shared();
             const bool all = loader_bar_all(go);
-            if (lead && all) mbar_arrive(bfull + old);
+            if (lead && all) {
+                if (PAIR && !leader)  // the pair's MMA waits on the even CTA's barrier
+                    mbar_arrive_remote_relaxed(mapa_shared(smem_u32(bfull + old), 0u));
+                else
+                    mbar_arrive(bfull + old);
+            }
             --npend;
         };
         uint32_t armed = 0, armed_phase = 0;  // TMA-armed stages (lead thread)
         bool ok = !solo || lead;
-        for (int tau = blockIdx.x; ok && tau < total; tau += gridDim.x) {
+        for (int tau = unit; ok && tau < total; tau += nunits) {
             bool second;
             Tile tl;
             job(tau, second, tl);
             const bool gather = !second && args.gather_rows != nullptr && L::ROW_BYTES == 128;
+            // this CTA's token rows of the tile: all of them, or for a CTA
+            // pair one half of the MMA's N (the odd CTA the second)
+            const int n_mma = (tl.n_valid + TG - 1) / TG * TG;
+            const int my0 = static_cast<int>(crank) * (n_mma / CG);
+            const int my_valid = max(0, min(n_mma / CG, tl.n_valid - my0));
             if (FUSED && second) {
                 // publish the pending gathered stages before waiting: the MMA
                 // needs them to finish the very gate/up tiles waited for
@@ -561,7 +646,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 // all gate/up tiles of this group must have published their rows
                 bool got = true;
                 if (lead) {
-                    const int need = rb1 * token_blocks(gcnt[tl.p], BN);
+                    const int need = rb1 * token_blocks(gcnt[tl.p], BN, TG);
                     const uint64_t t0 = global_timer_ns();
                     for (uint32_t it = 0; ld_acquire_gpu(fz.ready + tl.p) < need; ++it) {
                         if ((it & 63u) == 63u) {
@@ -583,7 +668,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             }
             const GemmMaps& m = second ? m2 : m1;
             const int KB = (second ? fz.K : args.K) / BK;
-            const int n_load = (tl.n_valid + BOX_ROWS - 1) / BOX_ROWS * BOX_ROWS;
+            const int n_load = (my_valid + BOX_ROWS - 1) / BOX_ROWS * BOX_ROWS;
             // gathered rows of this thread: source element offsets (-1: none)
             int64_t src[RPT];
             if (gather) {
@@ -591,8 +676,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 for (int u = 0; u < RPT; ++u) {
                     const int r = rbase + RSTEP * u;
                     src[u] = -1;
-                    if (r < tl.n_valid) {
-                        int t = args.gather_rows[tl.row0 + r];
+                    if (r < my_valid) {
+                        int t = args.gather_rows[tl.row0 + my0 + r];
                         if (t < 0 || t >= args.src_rows) {
                             record_error(args.status, GBMOE_ERR_DEVICE);
                             t = 0;
@@ -666,15 +751,29 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                         }
                     }
                 } else if (lead) {
-                    mbar_arrive_expect_tx(bfull + stage, n_load * L::ROW_BYTES);
+                    // the even CTA of a pair expects both halves' bytes; the
+                    // odd CTA's copies complete on that barrier
+                    const uint32_t lb = mapa_shared(smem_u32(bfull + stage), 0u);
+                    if (!PAIR || leader) {
+                        int n_all = n_load;
+                        if (PAIR) {
+                            const int pv = max(0, min(n_mma / CG, tl.n_valid - n_mma / CG));
+                            n_all += (pv + BOX_ROWS - 1) / BOX_ROWS * BOX_ROWS;
+                        }
+                        mbar_arrive_expect_tx(bfull + stage, n_all * L::ROW_BYTES);
+                    }
                     // token rows in as few boxes as possible (128/64/32/16 rows)
                     for (int off = 0; off < n_load;) {
                         const int rem = n_load - off;
                         const int box = rem >= 128 ? 128 : rem >= 64 ? 64 : rem >= 32 ? 32 : 16;
                         const CUtensorMap* mb = box == 128 ? &m.b128 : box == 64 ? &m.b64
                                               : box == 32 ? &m.b32 : &m.b16;
-                        tma_load_2d(sB + off * L::ROW_BYTES, mb, bfull + stage, kb * BK,
-                                    tl.row0 + off, pol_x);
+                        if (PAIR && !leader)
+                            tma_load_2d_pair(sB + off * L::ROW_BYTES, mb, lb, kb * BK,
+                                             tl.row0 + my0 + off, pol_x);
+                        else
+                            tma_load_2d(sB + off * L::ROW_BYTES, mb, bfull + stage, kb * BK,
+                                        tl.row0 + my0 + off, pol_x);
                         off += box;
                     }
                     armed |= 1u << stage;
@@ -704,33 +803,59 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             while (npend > 0) publish_oldest(ok);
         }
         cp_async_wait_all();
-        if (lead && *abort_flag) {  // let every TMA copy issued land before exit
+        if (lead && *abort_flag && PAIR) {
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < kPairSettleNs) {
+            }
+        } else if (lead && *abort_flag) {  // let every TMA copy issued land before exit
             for (int s = 0; s < SB; ++s)
                 if ((armed >> s) & 1u)
                     mbar_wait_timeout(bfull + s, (armed_phase >> s) & 1u, kDrainLimitNs);
+        } else if (PAIR && lead) {
+            // every stage consumed (the even CTA's commits have landed here)
+            for (int i = 0; i < SB; ++i) {
+                mbar_wait_timeout(bempty + stage, phase ^ 1u, kDrainLimitNs);
+                if (++stage == SB) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
         }
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer
+    } else if (warp == 1 && lane == 0 && leader) {
+        // MMA issuer (for a pair: the even CTA, M = 256 over both CTAs'
+        // shared memory; its commits signal the stage and accumulator
+        // barriers of both CTAs)
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            return mbar_wait_bounded(bar, parity, abort_flag, args.status, wait_ns);
+        };
+        auto commit = [&](uint64_t* bar) {
+            if (PAIR)
+                umma_commit_pair_mc(bar, 0x3);
+            else
+                umma_commit(bar);
+        };
         int as = 0, bs = 0, acc = 0;
         uint32_t aph = 0, bph = 0, acc_phase = 0;
         bool issued = false;
-        for (int tau = blockIdx.x; tau < total && !*abort_flag; tau += gridDim.x) {
+        for (int tau = unit; tau < total && !*abort_flag; tau += nunits) {
             bool second;
             Tile tl;
             job(tau, second, tl);
             const int KB = (second ? fz.K : args.K) / BK;
-            const int n_mma = ((tl.n_valid + 15) / 16) * 16;
+            const int n_mma = ((tl.n_valid + TG - 1) / TG) * TG;
             const uint32_t idesc = MXS ? idesc_mx(BM, n_mma, args.a_fmt, 0u, 0u)
-                                 : EB == 2 ? idesc_bf16_f32(BM, n_mma) : idesc_e4m3_f32(BM, n_mma);
-            if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, args.status,
-                                   wait_ns))
+                                 : EB == 2 ? idesc_bf16_f32(BM * CG, n_mma)
+                                           : idesc_e4m3_f32(BM, n_mma);
+            // the accumulator is free once both CTAs' epilogues have drained it
+            if (!(PAIR ? mbar_wait_bounded_cluster(tempty + acc, acc_phase ^ 1u, abort_flag,
+                                                   args.status, wait_ns)
+                       : wait(tempty + acc, acc_phase ^ 1u)))
                 break;
             tc_fence_after();
             const uint32_t d0 = tmem_base + acc * L::ACC_COLS;
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
-                if (!mbar_wait_bounded(afull + as, aph, abort_flag, args.status, wait_ns) ||
-                    !mbar_wait_bounded(bfull + bs, bph, abort_flag, args.status, wait_ns)) {
+                if (!wait(afull + as, aph) || !wait(bfull + bs, bph)) {
                     ok = false;
                     break;
                 }
@@ -754,22 +879,23 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     for (int a = 0; a < NUM_A; ++a) {
                         const uint64_t adesc =
                             smem_desc_kmajor<L::ROW_BYTES / 2>(sA + a * L::A_BYTES + ks * 32);
+                        const uint32_t accum = (kb > 0 || ks > 0) ? 1u : 0u;
                         if (MXS)
                             umma_mx(d0 + a * BN, adesc, bdesc,
                                     idesc | (static_cast<uint32_t>(ks) << 4) |
                                         (static_cast<uint32_t>(ks) << 29),
-                                    sf + 4 * a, sf + 4 * NUM_A, (kb > 0 || ks > 0) ? 1u : 0u);
+                                    sf + 4 * a, sf + 4 * NUM_A, accum);
+                        else if (PAIR)
+                            umma_bf16_pair(d0 + a * BN, adesc, bdesc, idesc, accum);
                         else if (EB == 2)
-                            umma_bf16(d0 + a * BN, adesc, bdesc, idesc,
-                                      (kb > 0 || ks > 0) ? 1u : 0u);
+                            umma_bf16(d0 + a * BN, adesc, bdesc, idesc, accum);
                         else
-                            umma_e4m3(d0 + a * BN, adesc, bdesc, idesc,
-                                      (kb > 0 || ks > 0) ? 1u : 0u);
+                            umma_e4m3(d0 + a * BN, adesc, bdesc, idesc, accum);
                     }
                 }
                 issued = true;
-                umma_commit(aempty + as);
-                umma_commit(bempty + bs);
+                commit(aempty + as);
+                commit(bempty + bs);
                 if (++as == SA) {
                     as = 0;
                     aph ^= 1u;
@@ -780,14 +906,17 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 }
             }
             if (!ok) break;
-            umma_commit(tfull + acc);
+            commit(tfull + acc);
             if (++acc == ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
         if (*abort_flag && issued) {  // wait for the MMAs in flight before TMEM is freed
-            umma_commit(drain);
+            if (PAIR)
+                umma_commit_pair_mc(drain, 0x1);
+            else
+                umma_commit(drain);
             mbar_wait_timeout(drain, 0u, kDrainLimitNs);
         }
     } else if (warp >= 2 && warp < LOADER_WARP0) {
@@ -799,7 +928,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         const int r = q * 32 + lane;            // weight row within the tile
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tau = blockIdx.x; tau < total; tau += gridDim.x) {
+        for (int tau = unit; tau < total; tau += nunits) {
             bool second;
             Tile tl;
             job(tau, second, tl);
@@ -821,7 +950,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 #pragma unroll 1
             for (int ob = 0; ob < nout; ++ob) {
                 const int nr = min(EPI_COLS, tl.n_valid - c0);
-                const size_t col = static_cast<size_t>(tl.rblk) * wrows + ob * BM + r;
+                // output column: this CTA's weight rows of the tile (the odd
+                // CTA of a pair holds the second half)
+                const size_t col = static_cast<size_t>(tl.rblk * CG + static_cast<int>(crank)) *
+                                       wrows + ob * BM + r;
                 uint32_t g[16], u[16];
                 tmem_ld_32x32b_x16(tb + ob * BN + c0, g);
                 if (swiglu) tmem_ld_32x32b_x16(tb + BN + c0, u);
@@ -906,7 +1038,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty + acc);
+            if (lane == 0) {
+                if (PAIR && !leader)  // the pair's MMA waits on the even CTA's barrier
+                    mbar_arrive_remote(mapa_shared(smem_u32(tempty + acc), 0u));
+                else
+                    mbar_arrive(tempty + acc);
+            }
             if (FUSED && !second) {
                 // publish this gate/up tile: its activations are in global memory
                 __threadfence();
@@ -921,12 +1058,17 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         }
     }
 
-    // ---- teardown
+    // ---- teardown (a pair: neither CTA leaves while the other may still
+    // signal its barriers or read its shared memory)
     __syncthreads();
+    if (PAIR) cluster_sync_all();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, L::TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, L::TMEM_COLS);
     }
 }
 
@@ -961,6 +1103,13 @@ using Gemm2Pair = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK>;
 // paired down blocks over 256-token tiles (the gate/up 256-token layout)
 #define GEMM2_PAIR_LARGE grouped_gemm_kernel<2, 256, kG1L_A, kG1L_B, kDownPair, 1, kBK>
 #define GEMM_FUSED grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kFused, 2, kBK>
+// CTA pairs (prefill-sized groups, I % 256 == 0 / H % 512 == 0): gate/up
+// tiles of 2 x 128 gate and up rows x 256 tokens, and down tiles of 2 x 256
+// W_down rows x 256 tokens, each CTA staging 128 token rows per stage
+constexpr int kPr_A = 4, kPr_B = 4;
+using GemmPairLarge = Layout<2, 256, kPr_A, kPr_B, 1, kBK, 2, 0, 2>;
+#define GEMM1_CTA_PAIR grouped_gemm_kernel<2, 256, kPr_A, kPr_B, kSwiGLU, 1, kBK, 2, 0, 2>
+#define GEMM2_CTA_PAIR grouped_gemm_kernel<2, 256, kPr_A, kPr_B, kDownPair, 1, kBK, 2, 0, 2>
 // FP8 E4M3 operands: 128-element stages (the same 128-byte rows)
 constexpr int kBK8 = 128;
 using Gemm1SmallF8 = Layout<2, 128, kG1S_A, kG1S_B, 2, kBK8, 1>;
@@ -1072,6 +1221,8 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX, a, GemmMx::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_DEC, a, GemmMxDec::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_DEC, a, GemmMxDec::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_CTA_PAIR, a, GemmPairLarge::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_CTA_PAIR, a, GemmPairLarge::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < kMaxDevices) g_attr_done[device] = true;
     return cudaSuccess;
@@ -1080,6 +1231,41 @@ cudaError_t ensure_attrs(int device) {
 int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
     const long bound = static_cast<long>(R / BM) * ((n_rows + BN - 1) / BN + groups);
     return static_cast<int>(std::max<long>(1, std::min<long>(bound, num_sms)));
+}
+
+// Launch of a CTA-pair kernel as clusters of two CTAs, as many clusters as
+// can be resident at once (one CTA per SM), at most one per tile.  The
+// residency limit is queried once per device and kernel.
+std::mutex g_pair_mu;
+int g_pair_clusters[kMaxDevices][2];
+
+template <class K>
+int launch_pair(K kernel, int slot, int smem, long tiles, const GemmMaps& m, const GemmArgs& a,
+                const DevCtx& ctx, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(std::max(2, ctx.num_sms / 2 * 2));
+    int clusters = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_pair_mu);
+        int& c = g_pair_clusters[ctx.device][slot];
+        if (c == 0 && cudaOccupancyMaxActiveClusters(&c, kernel, &cfg) != cudaSuccess) c = 0;
+        clusters = c;
+    }
+    if (clusters < 1) return GBMOE_ERR_CUDA;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max<long>(1, std::min<long>(clusters, tiles))));
+    const FusedArgs none{0, 0, nullptr, nullptr};
+    return cudaLaunchKernelEx(&cfg, kernel, m, m, a, none) == cudaSuccess ? GBMOE_OK
+                                                                          : GBMOE_ERR_CUDA;
 }
 
 }  // namespace
@@ -1124,7 +1310,10 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* row_to_token, int 
                row_to_token, row_to_token ? x_rows : nullptr, src_rows, activation};
     stamp(a);
     const FusedArgs none{0, 0, nullptr, nullptr};
-    if (n_rows >= kLargeGateUpRows * groups) {
+    if (n_rows >= kLargeGateUpRows * groups && I % 256 == 0) {
+        const long tiles = static_cast<long>(I / 256) * ((n_rows + 255) / 256 + groups);
+        return launch_pair(GEMM1_CTA_PAIR, 0, GemmPairLarge::SMEM_BYTES, tiles, m, a, ctx, s);
+    } else if (n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
         GEMM1_LARGE<<<grid, NUM_THREADS, Gemm1Large::SMEM_BYTES, s>>>(m, m, a, none);
     } else {
@@ -1145,7 +1334,10 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
     GemmArgs a{offsets, groups, n_rows, H, I, y, ctx.status, nullptr, nullptr, 0, 0};
     stamp(a);
     const FusedArgs none{0, 0, nullptr, nullptr};
-    if (H % 256 == 0 && n_rows >= kLargeGateUpRows * groups) {
+    if (H % 512 == 0 && n_rows >= kLargeGateUpRows * groups) {
+        const long tiles = static_cast<long>(H / 512) * ((n_rows + 255) / 256 + groups);
+        return launch_pair(GEMM2_CTA_PAIR, 1, GemmPairLarge::SMEM_BYTES, tiles, m, a, ctx, s);
+    } else if (H % 256 == 0 && n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, H / 2, 256, ctx.num_sms);
         GEMM2_PAIR_LARGE<<<grid, NUM_THREADS, Gemm1Large::SMEM_BYTES, s>>>(m, m, a, none);
     } else if (H % 256 == 0) {

@@ -187,9 +187,85 @@ def _quantized_layer(gb, case, kind):
     return layer, q
 
 
+# Activation codes that either of two valid computations can give.  The
+# GPU sums g and u in fp32 in its own order, the oracle exactly and then
+# rounds once, so f(g, u) can land on the other side of a bf16 rounding
+# boundary when it lies within a few fp32 ulps of one; if the two bf16
+# neighbours quantize to different codes (at the top of an E4M3 binade the
+# codes differ by 1/8 of the value, or the row's scale moves when the element
+# is the row maximum), both outputs are correct quantizations of a correctly
+# rounded activation.  The output check allows, per element, the sum of the
+# changes that such alternatives make through W_down, each computed by the
+# oracle's own quantizer on the alternative activation row -- from oracle
+# values only, nothing from the GPU.
+_E4M3_LUT = np.array([oracle.e4m3_to_f32(c) for c in range(256)], np.float64)
+_E2M1_LUT = np.array([oracle.e2m1_to_f32(c) for c in range(16)], np.float64)
+# fp32 summation error allowed on g and u, relative to the sum of the
+# magnitudes of their K products (16 fp32 ulps of that scale, several times
+# the random-walk error of a sum of K = 7168 terms): f(g, u) within the
+# propagated error of a bf16 rounding boundary is treated as a tie
+_SUM_ERR = 2.0 ** -20
+
+
+def _deq_mx(codes, scales, fmt):
+    """Dequantized MX rows [R, K] from codes (E4M3 [R, K] or E2M1 packed [R, K/2])
+    and UE8M0 scale bytes [R, K/32]."""
+    if fmt == "e4m3":
+        v = _E4M3_LUT[codes]
+    else:
+        v = np.empty((codes.shape[0], codes.shape[1] * 2))
+        v[:, 0::2] = _E2M1_LUT[codes & 0xF]
+        v[:, 1::2] = _E2M1_LUT[codes >> 4]
+    return v * np.repeat(2.0 ** (scales.astype(np.float64) - 127.0), 32, axis=1)
+
+
+def _deq_rows(codes, scales):
+    """Dequantized FP8 rows [R, K] (E4M3 codes and one fp32 scale per row)."""
+    return _E4M3_LUT[codes] * scales.astype(np.float64)[:, None]
+
+
+def _alt_code_margin(kind, x_deq, wg_deq, wu_deq, wd_deq, act_bits):
+    """Per routed row: sum over its activations that sit at a bf16 tie of
+    |y(alternative row) - y(oracle row)| ([n, H]); x_deq [n, H] and the
+    weights dequantized in float64."""
+    g = (x_deq @ wg_deq.T).astype(np.float32).astype(np.float64)
+    u = (x_deq @ wu_deq.T).astype(np.float32).astype(np.float64)
+    ax = np.abs(x_deq)
+    dg = _SUM_ERR * (ax @ np.abs(wg_deq).T)
+    du = _SUM_ERR * (ax @ np.abs(wu_deq).T)
+    sg = 1.0 / (1.0 + np.exp(-g))
+    f = g * sg * u
+    df = np.abs(u * sg * (1.0 + g * (1.0 - sg))) * dg + np.abs(g * sg) * du
+    b = synth.bf16_to_f32(act_bits).astype(np.float64)
+    # the bf16 neighbour of the oracle's activation on the side of f
+    bits = act_bits.astype(np.int32)
+    up = f > b
+    nb = bits + np.where(up ^ ((bits & 0x8000) != 0), 1, -1)
+    zero = (bits & 0x7FFF) == 0
+    nb = np.where(zero, np.where(up, 0x0001, 0x8001), nb)
+    nb_bits = nb.astype(np.uint16)
+    nbv = synth.bf16_to_f32(nb_bits).astype(np.float64)
+    mid = 0.5 * (b + nbv)
+    tie = np.abs(f - mid) <= df
+    quant = (lambda r: _deq_rows(*oracle.quantize_rows(r))) if kind == "fp8_row" else \
+        (lambda r: _deq_mx(*oracle.mx_quantize_rows(r, "e4m3"), "e4m3"))
+    margin = np.zeros((act_bits.shape[0], wd_deq.shape[0]))
+    for r in np.nonzero(tie.any(axis=1))[0]:
+        base = quant(act_bits[r:r + 1])[0]
+        for i in np.nonzero(tie[r])[0]:
+            alt = act_bits[r:r + 1].copy()
+            alt[0, i] = nb_bits[r, i]
+            d = quant(alt)[0] - base
+            nz = np.nonzero(d)[0]
+            if len(nz):
+                margin[r] += np.abs(wd_deq[:, nz] @ d[nz])
+    return margin
+
+
 def _oracle_quantized_rows(cfg, d, kind, q_dev, need, tokens):
     """y of the sampled (token, slot) pairs from the oracle's quantized MLP,
-    expert by expert, after checking the GPU's weight codes of each expert."""
+    expert by expert, after checking the GPU's weight codes of each expert;
+    with each row's margin for ambiguous activation codes."""
     fmt = QKINDS[kind]
     xs_rows = d["x"][tokens]
     pos = {t: i for i, t in enumerate(tokens)}
@@ -213,17 +289,22 @@ def _oracle_quantized_rows(cfg, d, kind, q_dev, need, tokens):
         r2t = np.array([pos[t] for t, _ in rows], np.int32)
         offs = np.array([0, len(rows)], np.int32)
         if fmt is None:
-            _, y = oracle.ffn_grouped_fp8(xq, xsc, r2t, offs, *qo, nthreads=1)
+            act, y = oracle.ffn_grouped_fp8(xq, xsc, r2t, offs, *qo, nthreads=1)
+            deq = [_deq_rows(qo[2 * m][0], qo[2 * m + 1][0]) for m in range(3)]
+            xd = _deq_rows(xq[r2t], xsc[r2t])
         else:
-            _, _, _, y = oracle.ffn_grouped_mx(xq, xsc, r2t, offs, *qo, wfmt=fmt, nthreads=1)
-        return rows, y
+            act, _, _, y = oracle.ffn_grouped_mx(xq, xsc, r2t, offs, *qo, wfmt=fmt, nthreads=1)
+            deq = [_deq_mx(qo[2 * m][0], qo[2 * m + 1][0], fmt) for m in range(3)]
+            xd = _deq_mx(xq[r2t], xsc[r2t], "e4m3")
+        return rows, y, _alt_code_margin(kind, xd, *deq, act)
 
-    out = {}
+    out, margin = {}, {}
     with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
-        for rows, y in ex.map(one, sorted(need)):
-            for (t, j), r in zip(rows, y):
+        for rows, y, mg in ex.map(one, sorted(need)):
+            for (t, j), r, m in zip(rows, y, mg):
                 out[(t, j)] = r
-    return out
+                margin[(t, j)] = m
+    return out, margin
 
 
 @pytest.mark.parametrize("name,kind", [("decode", "fp8_row"), ("decode", "mxfp8"),
@@ -259,17 +340,27 @@ def test_full_size_quantized(gb, name, kind):
     for t in sample:
         for j in range(k):
             need.setdefault(int(idp_o[t, j]), []).append((t, j))
-    y = _oracle_quantized_rows(cfg, d, kind, q, need, sample)
-    exp = []
+    y, ymargin = _oracle_quantized_rows(cfg, d, kind, q, need, sample)
+    exp, margin = [], []
     for i, t in enumerate(sample):
         yt = np.stack([y[(t, j)] for j in range(k)])
         exp.append(oracle.combine(yt, np.arange(k, dtype=np.int32), w_o[t:t + 1],
                                   None if ys is None else ys[i:i + 1])[0])
+        margin.append(sum(abs(float(w_o[t, j])) * ymargin[(t, j)] for j in range(k)))
     exp = synth.bf16_to_f32(np.stack(exp)).astype(np.float64)
+    margin = np.stack(margin)
     got = _np(out[sample].float()).astype(np.float64)
     err = np.abs(got - exp)
-    bad = err > 1e-2 + 1e-2 * np.abs(exp)
+    tol = 1e-2 + 1e-2 * np.abs(exp)
+    # ambiguous activation codes may move an element by up to its margin (and
+    # the output's bf16 rounding by one more ulp of the moved value)
+    allowed = tol + margin + 2.0 ** -8 * (np.abs(exp) + margin)
+    bad = err > allowed
     assert not bad.any(), f"{kind} {name}: {bad.sum()} of {err.size} outside, max {err.max()}"
-    assert err.max() <= 2 * 2.0 ** -8 * np.abs(exp).max()
+    # the margin is needed only where an ambiguous code sits; everywhere else
+    # the plain tolerance holds
+    outside_tol = err > tol
+    assert outside_tol.mean() <= 1e-3, f"{kind} {name}: {outside_tol.sum()} beyond the tolerance"
+    assert err[~outside_tol].max() <= 2 * 2.0 ** -8 * np.abs(exp).max()
     del case, out, layer, q
     torch.cuda.empty_cache()
