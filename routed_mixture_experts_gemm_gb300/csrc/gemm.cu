@@ -616,11 +616,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const int old = (last - (npend - 1) + SB) % SB;
             fence_proxy_async_shared();
             const bool all = loader_bar_all(go);
+            // relaxed arrivals: every loader's copies of the stage have landed
+            // and been fenced before the barrier, and a release here would
+            // also wait for the newer stage's copies in flight
             if (lead && all) {
                 if (PAIR && !leader)  // the pair's MMA waits on the even CTA's barrier
                     mbar_arrive_remote_relaxed(mapa_shared(smem_u32(bfull + old), 0u));
                 else
-                    mbar_arrive(bfull + old);
+                    mbar_arrive_relaxed(bfull + old);
             }
             --npend;
         };
