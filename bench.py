@@ -677,6 +677,9 @@ def main(argv=None):
                          "under its own key ('' to skip); quantized experts are measured on "
                          "the first of them")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--sustained-s", type=float, default=1.0,
+                    help="seconds of the sustained runs (decode companion, further workloads); "
+                         "0 runs them for 3 steps (short launch lists under a profiler)")
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quant", action="store_true",
@@ -759,7 +762,7 @@ def main(argv=None):
     peaks, peak_src = load_peaks()
     roof, touched = roofline_of(wl, stages, counts, peaks, peak_src)
     # the same step repeated for >= 1 s: the sustained clock / power state
-    sustained = sustained_run(wl, args.warmup, torch, barrier, local, world)
+    sustained = sustained_run(wl, args.warmup, torch, barrier, local, world, args.sustained_s)
     t_e2e, h2d, d2h = e2e_time(wl, args.steps, args.warmup, torch)
     e2e = {"value": world * cfg.T * args.steps / t_e2e, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -793,7 +796,7 @@ def main(argv=None):
         w2 = Workload(c2, dev)
         w2.forward()
         torch.cuda.synchronize()
-        res = sustained_run(w2, args.warmup, torch, barrier, local, world)
+        res = sustained_run(w2, args.warmup, torch, barrier, local, world, args.sustained_s)
         res = {"workload": c2.name, "T": c2.T, **res}
         stg2 = stage_times(w2, min(args.steps, 10), torch)
         res["stages_ms"] = stg2
