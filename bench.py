@@ -311,6 +311,9 @@ class Workload:
             self.wq = [a for pair in q for a in pair]
             self.layer_q = self.gb.MoELayer(c.layer.cfg, d["w_router"], None, None, None,
                                             mx=[self.wfmt] + self.wq, **kw)
+            # the GEMMs called stage by stage take the weight scales tiled
+            self.wq = [self.gb.moe_mx_tile_scales(a) if i % 2 else a
+                       for i, a in enumerate(self.wq)]
             self.xs, self.as_ = e(T, cfg.H // 32, dt=u8), e(cfg.N, cfg.I // 32, dt=u8)
         self.ws_q = self.layer_q.workspace(T)
         self.xq = e(T, cfg.H, dt=u8)

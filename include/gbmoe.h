@@ -141,11 +141,11 @@ typedef struct gbmoe_layer {
      * 0.  The shared expert stays bf16. */
     int mx_format;
     const uint8_t* w_gate_mx;     /* [E_phys, I, H] (E4M3) or [E_phys, I, H/2] (E2M1) */
-    const uint8_t* sf_gate;       /* [E_phys, I, H/32] */
+    const uint8_t* sf_gate;       /* [E_phys, I, H/32], tiled (moe_mx_tile_scales) */
     const uint8_t* w_up_mx;       /* as w_gate_mx */
-    const uint8_t* sf_up;         /* [E_phys, I, H/32] */
+    const uint8_t* sf_up;         /* [E_phys, I, H/32], tiled */
     const uint8_t* w_down_mx;     /* [E_phys, H, I] (E4M3) or [E_phys, H, I/2] (E2M1) */
-    const uint8_t* sf_down;       /* [E_phys, H, I/32] */
+    const uint8_t* sf_down;       /* [E_phys, H, I/32], tiled */
 } gbmoe_layer;
 
 /* Text for a status code (static storage). */
@@ -422,6 +422,25 @@ int moe_quantize_mx_rows(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* 
                          uint8_t* scales, gbmoe_stream_t stream);
 
 /*
+ * moe_mx_tile_scales — rearranges MX weight scale bytes from the row-major
+ * layout of moe_quantize_mx_rows ([rows, K/32]) into the tiled layout that
+ * the MX grouped GEMMs read for their weights (the weight scale arguments of
+ * moe_gemm_gateup_act_mx / moe_gemm_down_mx and gbmoe_layer's sf_gate, sf_up,
+ * sf_down): for each block of 128 rows rb and K stage ks of 128 elements,
+ * 512 contiguous bytes at offset (rb * (K/128) + ks) * 512 whose byte
+ * r*16 + j*4 + b is the scale of row rb*128 + 32*j + r for the K block
+ * 4*ks + b (r < 32, j < 4, b < 4) -- the order of the tensor-memory columns
+ * the block-scaled MMA reads them from, so that a GEMM stage's weight scales
+ * arrive as one 512-byte copy per 128-row block.  The output has the size of
+ * the input.  A layer's weight scales are converted once, when it is loaded.
+ *   sf_rows [rows, K/32] uint8, 4-byte aligned; sf_tiled the same number of
+ *   bytes, 16-byte aligned, not overlapping sf_rows.  rows and K multiples of
+ *   128 (else UNSUPPORTED).
+ */
+int moe_mx_tile_scales(const uint8_t* sf_rows, int64_t rows, int K, uint8_t* sf_tiled,
+                       gbmoe_stream_t stream);
+
+/*
  * moe_gemm_gateup_act_mx / moe_gemm_down_mx — the grouped GEMMs with MX
  * block-scaled operands on the tensor cores (tcgen05 kind::mxf8f6f4 with
  * block scales): weights in format w_fmt (E4M3: MXFP8; E2M1: W4A8), tokens
@@ -433,9 +452,11 @@ int moe_quantize_mx_rows(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* 
  *   (the quantization is fused into the GEMM's epilogue);
  *   y[r, h] = sum_i a[r,i] wd[p,h,i]  (fp32).
  *   xq [T or N, H] codes + xs [T or N, H/32] (t = row_to_token[r], or r with
- *   row_to_token NULL); wgq / wuq [E_phys, I, H or H/2] + sg / su
- *   [E_phys, I, H/32]; aq [N, I] + as [N, I/32]; wdq [E_phys, H, I or I/2] +
- *   sd [E_phys, H, I/32].  H % 256 == 0, I % 128 == 0 (else UNSUPPORTED);
+ *   row_to_token NULL); wgq / wuq [E_phys, I, H or H/2] + sg / su, the
+ *   [E_phys, I, H/32] scale bytes in the tiled layout of moe_mx_tile_scales
+ *   (rows = E_phys * I, K = H); aq [N, I] + as [N, I/32] (row-major); wdq
+ *   [E_phys, H, I or I/2] + sd, [E_phys, H, I/32] tiled (rows = E_phys * H,
+ *   K = I).  H % 256 == 0, I % 128 == 0 (else UNSUPPORTED);
  *   code arrays 16-byte aligned (E2M1 weights 32-byte aligned); weight scale
  *   arrays 16-byte aligned, token / activation scale arrays 4-byte aligned.
  */

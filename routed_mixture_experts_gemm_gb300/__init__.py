@@ -24,7 +24,8 @@ __all__ = ["GbmoeError", "route_cfg", "moe_route", "moe_expert_counts", "moe_per
            "moe_gemm_gateup_act", "moe_gemm_gateup_act_rows", "moe_gemm_down", "moe_expert_mlp", "expert_mlp_fused",
            "moe_combine", "moe_quantize_fp8_rows",
            "moe_gemm_gateup_act_fp8", "moe_gemm_down_fp8", "quantize_experts_fp8",
-           "moe_quantize_mx_rows", "moe_gemm_gateup_act_mx", "moe_gemm_down_mx",
+           "moe_quantize_mx_rows", "moe_mx_tile_scales", "moe_gemm_gateup_act_mx",
+           "moe_gemm_down_mx",
            "quantize_experts_mx", "moe_latent_tail", "MoELayer", "moe_forward",
            "moe_forward_host", "check_device_status", "set_wait_limit_ns", "library"]
 
@@ -300,13 +301,31 @@ def quantize_experts_mx(w, fmt="e4m3", stream=None):
     return q.reshape(E, R, -1), sc.reshape(E, R, K // 32)
 
 
+def moe_mx_tile_scales(sf, stream=None):
+    """MX weight scale bytes [..., R, K/32] (row-major, as moe_quantize_mx_rows
+    writes them) -> the same bytes in the tiled layout the MX GEMMs read
+    (moe_mx_tile_scales of the C ABI), as a new tensor of the same shape."""
+    lib = _lib.load()
+    K = sf.shape[-1] * 32
+    rows = sf.numel() // (K // 32)
+    out = torch.empty_like(sf)
+    _check(lib.moe_mx_tile_scales(_ptr(sf), rows, K, _ptr(out), _stream(stream)),
+           "moe_mx_tile_scales")
+    return out
+
+
 def moe_gemm_gateup_act_mx(xq, xs, offsets, wgq, sg, wuq, su, w_fmt="e4m3", row_to_token=None,
-                           act_q=None, act_s=None, activation="swiglu", stream=None):
+                           act_q=None, act_s=None, activation="swiglu", stream=None,
+                           scales_tiled=False):
     """MX gate/up GEMM: act = bf16(f(x wg^T, x wu^T)) over the dequantized MX
     operands, returned quantized to MX E4M3: (codes uint8 [N, I], scale bytes
     [N, I/32]).  xq [T, H] codes + xs [T, H/32] gathered through row_to_token
-    [N] (or the N permuted rows); weights in format w_fmt."""
+    [N] (or the N permuted rows); weights in format w_fmt with row-major
+    scale bytes sg / su (tiled here by moe_mx_tile_scales), or already tiled
+    with scales_tiled=True."""
     lib = _lib.load()
+    if not scales_tiled:
+        sg, su = moe_mx_tile_scales(sg, stream), moe_mx_tile_scales(su, stream)
     P, I = wgq.shape[0], wgq.shape[1]
     H = xq.shape[1]
     if row_to_token is None:
@@ -324,9 +343,13 @@ def moe_gemm_gateup_act_mx(xq, xs, offsets, wgq, sg, wuq, su, w_fmt="e4m3", row_
     return act_q, act_s
 
 
-def moe_gemm_down_mx(aq, as_, offsets, wdq, sd, w_fmt="e4m3", y=None, stream=None):
-    """MX down GEMM: y = a . wd^T over the dequantized MX operands, fp32 [N, H]."""
+def moe_gemm_down_mx(aq, as_, offsets, wdq, sd, w_fmt="e4m3", y=None, stream=None,
+                     scales_tiled=False):
+    """MX down GEMM: y = a . wd^T over the dequantized MX operands, fp32 [N, H];
+    sd row-major (tiled here) or tiled with scales_tiled=True."""
     lib = _lib.load()
+    if not scales_tiled:
+        sd = moe_mx_tile_scales(sd, stream)
     N, I = aq.shape
     P, H = wdq.shape[0], wdq.shape[1]
     if y is None:
@@ -375,8 +398,12 @@ class MoELayer:
         w_down may then be None.
         mx = (fmt, w_gate_mx, sf_gate, w_up_mx, sf_up, w_down_mx, sf_down): MX
         block-scaled routed experts ("e4m3" or "e2m1" codes and UE8M0 scale
-        bytes per 32 elements along K, e.g. from quantize_experts_mx)."""
+        bytes per 32 elements along K, row-major as from quantize_experts_mx;
+        the layer keeps copies in the GEMMs' tiled layout)."""
         self.cfg = cfg
+        if mx:
+            mx = [mx[0], mx[1], moe_mx_tile_scales(mx[2]), mx[3], moe_mx_tile_scales(mx[4]),
+                  mx[5], moe_mx_tile_scales(mx[6])]
         self._keep = [w_router, w_gate, w_up, w_down, router_bias, corr_bias, tid2eid, log2phy,
                       replica_cnt] + list(shared or []) + list(fp8 or []) + list(mx or [])[1:]
         if w_gate is not None:

@@ -64,6 +64,7 @@ SIGNATURES = {
                                      _i, _vp, _vp]),
     "moe_gemm_down_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "moe_quantize_mx_rows": (_i, [_vp, _i64, _i, _i, _vp, _vp, _vp]),
+    "moe_mx_tile_scales": (_i, [_vp, _i64, _i, _vp, _vp]),
     "moe_gemm_gateup_act_mx": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                                     _vp, _i, _vp, _vp, _vp]),
     "moe_gemm_down_mx": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),

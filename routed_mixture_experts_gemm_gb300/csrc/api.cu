@@ -471,6 +471,22 @@ int moe_quantize_mx_rows(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* 
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_mx_tile_scales(const uint8_t* sf_rows, int64_t rows, int K, uint8_t* sf_tiled,
+                       gbmoe_stream_t stream) {
+    if (rows < 0 || K <= 0) return GBMOE_ERR_INVALID_ARG;
+    if (rows % 128 || K % 128) return GBMOE_ERR_UNSUPPORTED;
+    if (rows == 0) return GBMOE_OK;
+    if (!sf_rows || !sf_tiled || !aligned4(sf_rows) || !aligned16(sf_tiled))
+        return GBMOE_ERR_INVALID_ARG;
+    const size_t bytes = static_cast<size_t>(rows) * (K / 32);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(sf_rows), b = reinterpret_cast<uintptr_t>(sf_tiled);
+    if (a < b + bytes && b < a + bytes) return GBMOE_ERR_INVALID_ARG;  // must not overlap
+    const DevCtx* ctx = device_ctx();
+    if (!ctx) return GBMOE_ERR_CUDA;
+    return status_from(launch_mx_tile_scales(sf_rows, rows, K, sf_tiled, *ctx,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_gemm_gateup_act_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* row_to_token,
                            int T, const int32_t* offsets, int E_phys, int N, int H, int I,
                            int w_fmt, const uint8_t* wgq, const uint8_t* sg, const uint8_t* wuq,

@@ -137,11 +137,16 @@ struct Layout {
     static constexpr int OFF_BARS = OFF_SCAN + NUM_THREADS * 4 + 16;
     static constexpr int NUM_BARS = 2 * SA + 2 * SB + 4 + 1;
     static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
-    // MX: per token stage, the scale words of its TMEM columns as 512-byte
-    // chunks of 32 rows x 16 bytes (row r = the four columns of lane r)
+    // MX: the scale words of a stage's TMEM columns as 512-byte chunks of 32
+    // rows x 16 bytes (row r = the four columns of lane r): the token rows'
+    // chunks with each token stage (staged by the loaders), the weights'
+    // chunks with each weight stage (copied whole by the weight producer from
+    // the pre-tiled scale arrays)
     static constexpr int OFF_SFS = (OFF_MISC + 16 + 127) / 128 * 128;
-    static constexpr int SFS_BYTES = MXS ? SB * SF_CHUNKS * 512 : 0;
-    static constexpr int END = OFF_SFS + SFS_BYTES;
+    static constexpr int SFS_BYTES = MXS ? SB * SFB_CHUNKS * 512 : 0;
+    static constexpr int OFF_ASF = OFF_SFS + SFS_BYTES;
+    static constexpr int ASF_BYTES = MXS ? SA * NUM_A * 512 : 0;
+    static constexpr int END = OFF_ASF + ASF_BYTES;
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
     static_assert(TMEM_USED <= 512 && (MXS || TMEM_USED == TMEM_COLS), "TMEM columns");
     static_assert(!MXS || (EB == 1 && BK == 128), "MX stages hold four 32-element K blocks");
@@ -296,9 +301,15 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool va
                  "r"(valid ? 4 : 0)
                  : "memory");
 }
-// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global into shared memory, completing its bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -491,26 +502,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         uint32_t phase = 0;
         uint32_t armed = 0;          // bit s: stage s has been armed at least once
         uint32_t armed_phase = 0;    // bit s: parity of its last armed phase
-        // MX: a tile's weight scale rows (one contiguous run per A operand)
-        // are prefetched into L2 a tile ahead: the token loaders read them in
-        // 4-byte pieces on their critical path
-        auto prefetch_sf = [&](int tau) {
-            if (!MXS || tau >= total) return;
-            bool sec;
-            Tile t;
-            job(tau, sec, t);
-            const size_t kq = static_cast<size_t>(args.K / 32);
-            const size_t row = static_cast<size_t>(t.p) * args.R + static_cast<size_t>(t.rblk) * WROWS1;
-            prefetch_l2_bulk(args.w_sf0 + row * kq, static_cast<uint32_t>(WROWS1 * kq));
-            if (MODE1 == kSwiGLU)
-                prefetch_l2_bulk(args.w_sf1 + row * kq, static_cast<uint32_t>(BM * kq));
-        };
-        prefetch_sf(unit);
         for (int tau = unit; tau < total && !*abort_flag; tau += nunits) {
             bool second;
             Tile tl;
             job(tau, second, tl);
-            prefetch_sf(tau + nunits);
             const GemmMaps& m = second ? m2 : m1;
             const int mode = second ? kDownPair : MODE1;
             const int R = second ? fz.R : args.R;
@@ -521,7 +516,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const uint64_t pol_w = token_blocks(gcnt[tl.p], BN, TG) > 1 ? pol_shared : pol_once;
             // an E2M1 box lands as one byte per element (16 codes in the first
             // 8 bytes of every 16) but completes with its packed size
-            const uint32_t a_tx = (MXS && args.a_fmt == 5u) ? L::A_BYTES / 2 : L::A_BYTES;
+            const uint32_t a_tx = ((MXS && args.a_fmt == 5u) ? L::A_BYTES / 2 : L::A_BYTES) +
+                                  (MXS ? 512u : 0u);
+            // MX: the weight scale chunks of this tile's 128-row blocks, one
+            // 512-byte run per (row block, K stage) in the pre-tiled arrays
+            const int ks_per_row = args.K / BK;
+            const size_t sf_tile0 = static_cast<size_t>(a_row / BM) * ks_per_row;
             bool ok = true;
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait_bounded(aempty + stage, phase ^ 1u, abort_flag, args.status,
@@ -547,6 +547,18 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     if (mode == kDownPair)
                         tma_load_2d(sA + L::A_BYTES, &m.a0, afull + stage, kb * BK, a_row + BM,
                                     pol_w);
+                    if (MXS) {
+                        uint8_t* sf = smem + L::OFF_ASF + stage * (NUM_A * 512);
+                        // gate/up: the gate's and the up's chunks of the same
+                        // rows; paired down: the two consecutive row blocks
+                        const size_t c0 = (sf_tile0 + kb) * 512;
+                        bulk_load(sf, args.w_sf0 + c0, 512, afull + stage, pol_w);
+                        if (mode == kSwiGLU)
+                            bulk_load(sf + 512, args.w_sf1 + c0, 512, afull + stage, pol_w);
+                        if (mode == kDownPair)
+                            bulk_load(sf + 512, args.w_sf0 + c0 + static_cast<size_t>(ks_per_row) * 512,
+                                      512, afull + stage, pol_w);
+                    }
                 }
                 armed |= 1u << stage;
                 armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -689,13 +701,9 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     }
                 }
             }
-            // MX: the scale rows this thread stages
-            int64_t sfa_row[NUM_A], sfb_row[L::SFB_CHUNKS];
+            // MX: the token scale rows this thread stages
+            int64_t sfb_row[L::SFB_CHUNKS];
             if (MXS) {
-                const int a_row = tl.p * args.R + tl.rblk * WROWS1;
-#pragma unroll
-                for (int a = 0; a < NUM_A; ++a)
-                    sfa_row[a] = a_row + (MODE1 == kDownPair ? a * BM : 0) + 32 * wi + lane;
 #pragma unroll
                 for (int j = 0; j < L::SFB_CHUNKS; ++j) {
                     const int n = 32 * (wi + 4 * j) + lane;
@@ -723,19 +731,14 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     break;
                 }
                 if (MXS) {
-                    // this stage's scale words (four K blocks of a row each)
-                    // into its chunks, in the stage's copy group
+                    // this stage's token scale words (four K blocks of a row
+                    // each) into its chunks, in the stage's copy group
                     const uint32_t sfs = smem_u32(smem + L::OFF_SFS) +
-                                         stage * (L::SF_CHUNKS * 512) + lane * 16 + wi * 4;
-#pragma unroll
-                    for (int a = 0; a < NUM_A; ++a) {
-                        const uint8_t* w = (MODE1 == kSwiGLU && a == 1) ? args.w_sf1 : args.w_sf0;
-                        cp_async4(sfs + a * 512, w + sfa_row[a] * kq + kb * 4, true);
-                    }
+                                         stage * (L::SFB_CHUNKS * 512) + lane * 16 + wi * 4;
 #pragma unroll
                     for (int j = 0; j < L::SFB_CHUNKS; ++j) {
                         const bool v = sfb_row[j] >= 0;
-                        cp_async4(sfs + (NUM_A + j) * 512,
+                        cp_async4(sfs + j * 512,
                                   args.tok_sf + (v ? sfb_row[j] * kq + kb * 4 : 0), v);
                     }
                 }
@@ -869,10 +872,16 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 if (MXS) {
                     // the stage's scale chunks into its TMEM columns (in order
                     // with the MMAs below)
-                    const uint32_t sfs = smem_u32(smem + L::OFF_SFS) + bs * (L::SF_CHUNKS * 512);
+                    // weight chunks from the weight stage, token chunks from
+                    // the token stage
+                    const uint32_t asf = smem_u32(smem + L::OFF_ASF) + as * (NUM_A * 512);
+                    const uint32_t sfs = smem_u32(smem + L::OFF_SFS) + bs * (L::SFB_CHUNKS * 512);
 #pragma unroll
-                    for (int c = 0; c < L::SF_CHUNKS; ++c)
-                        tmem_cp_32x128b_warpx4(sf + 4 * c, smem_desc_rows16(sfs + c * 512));
+                    for (int a = 0; a < NUM_A; ++a)
+                        tmem_cp_32x128b_warpx4(sf + 4 * a, smem_desc_rows16(asf + a * 512));
+#pragma unroll
+                    for (int c = 0; c < L::SFB_CHUNKS; ++c)
+                        tmem_cp_32x128b_warpx4(sf + 4 * (NUM_A + c), smem_desc_rows16(sfs + c * 512));
                 }
                 // one MMA covers 32 bytes of K (16 bf16 or 32 FP8 elements)
 #pragma unroll

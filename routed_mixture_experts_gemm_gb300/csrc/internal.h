@@ -129,6 +129,11 @@ cudaError_t launch_quantize_rows(const uint16_t* x, int64_t n, int K, uint8_t* q
 cudaError_t launch_mx_quantize(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* q,
                                uint8_t* sc, const DevCtx& ctx, cudaStream_t st);
 
+// MX weight scales row-major [rows, K/32] -> the GEMMs' tiled layout
+// (rows % 128 == 0, K % 128 == 0)
+cudaError_t launch_mx_tile_scales(const uint8_t* sf_rows, int64_t rows, int K, uint8_t* tiled,
+                                  const DevCtx& ctx, cudaStream_t st);
+
 // --- latent-MoE tail (tail.cu) ---
 size_t latent_tail_ws_bytes(int T, int L, int Hm);
 int launch_latent_tail(const uint16_t* latent, int T, int L, const uint16_t* norm_w, float eps,

@@ -113,7 +113,43 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint4* __restric
     }
 }
 
+// MX weight scale bytes, row-major [rows, K/32] (as 32-bit words: the four
+// K blocks of one 128-element K stage of a row) -> the tiled layout of the
+// grouped GEMMs: for row block rb (128 rows) and K stage ks, 512 bytes at
+// chunk rb * KS + ks whose 16-byte row r holds, in word j, the four scale
+// bytes of row rb*128 + 32j + r -- the tensor-memory column order of the
+// block-scaled MMA (lane r, column j).  One thread per 16-byte row.
+__global__ void __launch_bounds__(256) mx_tile_scales_kernel(const uint32_t* __restrict__ rows_w,
+                                                            int64_t n16, int ks_n,
+                                                            uint4* __restrict__ tiled) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i & 31);
+        const int64_t chunk = i >> 5;
+        const int ks = static_cast<int>(chunk % ks_n);
+        const int64_t row0 = (chunk / ks_n) * 128 + r;
+        uint4 o;
+        o.x = rows_w[(row0 + 0) * ks_n + ks];
+        o.y = rows_w[(row0 + 32) * ks_n + ks];
+        o.z = rows_w[(row0 + 64) * ks_n + ks];
+        o.w = rows_w[(row0 + 96) * ks_n + ks];
+        tiled[i] = o;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_mx_tile_scales(const uint8_t* sf_rows, int64_t rows, int K, uint8_t* tiled,
+                                  const DevCtx& ctx, cudaStream_t st) {
+    const int ks_n = K / 128;
+    const int64_t n16 = (rows / 128) * ks_n * 32;
+    if (n16 == 0) return cudaSuccess;
+    const int64_t want = (n16 + 255) / 256;
+    const int grid = static_cast<int>(want < 16L * ctx.num_sms ? want : 16L * ctx.num_sms);
+    mx_tile_scales_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(sf_rows), n16,
+                                                ks_n, reinterpret_cast<uint4*>(tiled));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_mx_quantize(const uint16_t* x, int64_t n, int K, int fmt, uint8_t* q,
                                uint8_t* sc, const DevCtx& ctx, cudaStream_t st) {

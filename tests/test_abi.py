@@ -189,3 +189,16 @@ def test_wait_limit_setting_is_host_side(lib):
     assert lib.gbmoe_set_wait_limit_ns(12345) == default
     assert lib.gbmoe_set_wait_limit_ns(0) == 12345
     assert lib.gbmoe_set_wait_limit_ns(0) == default
+
+
+def test_mx_tile_scales_validates_on_the_host(lib):
+    # rows and K multiples of 128, the source 4-byte and the destination
+    # 16-byte aligned, the two not overlapping; rows = 0 enqueues nothing
+    a, b = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
+    assert lib.moe_mx_tile_scales(a, 100, 256, b, None) == 2
+    assert lib.moe_mx_tile_scales(a, 128, 96, b, None) == 2
+    assert lib.moe_mx_tile_scales(ctypes.c_void_p(0x100002), 128, 256, b, None) == 1
+    assert lib.moe_mx_tile_scales(a, 128, 256, ctypes.c_void_p(0x200004), None) == 1
+    assert lib.moe_mx_tile_scales(a, 128, 256, ctypes.c_void_p(0x100200), None) == 1  # overlap
+    assert lib.moe_mx_tile_scales(None, 0, 256, None, None) == 0
+    assert lib.moe_mx_tile_scales(a, -128, 256, b, None) == 1

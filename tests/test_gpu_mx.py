@@ -38,6 +38,17 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
+@pytest.mark.parametrize("rows,K", [(128, 128), (384, 7168), (256, 2048)])
+def test_mx_tile_scales_is_the_documented_rearrangement(gb, rows, K, rng):
+    """Tiled weight scales: for row block rb and K stage ks, 512 bytes whose byte
+    r*16 + j*4 + b is the scale of row rb*128 + 32j + r, K block 4ks + b."""
+    sf = rng.integers(0, 256, (rows, K // 32), dtype=np.uint8)
+    got = _np(gb.moe_mx_tile_scales(_dev(sf))).reshape(-1)
+    exp = (sf.reshape(rows // 128, 4, 32, K // 128, 4)   # rb, j, r, ks, b
+             .transpose(0, 3, 2, 1, 4).reshape(-1))         # rb, ks, r, j, b
+    assert np.array_equal(got, exp)
+
+
 @pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
 def test_mx_quantize_bit_exact(gb, fmt, rng):
     x = rng.standard_normal((300, 512)) * np.exp(rng.uniform(-20, 20, (300, 16))).repeat(32, 1)
