@@ -150,7 +150,7 @@ struct Layout {
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
     static_assert(TMEM_USED <= 512 && (MXS || TMEM_USED == TMEM_COLS), "TMEM columns");
     static_assert(!MXS || (EB == 1 && BK == 128), "MX stages hold four 32-element K blocks");
-    static_assert(!MXS || BN <= 128 || BN % 128 == 0, "token scale chunks of 128 rows");
+    static_assert(!MXS || BN <= 256, "at most two chunks of 128 token rows' scales");
     static_assert(A_STAGE % 1024 == 0 && B_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(ROW_BYTES == 128 || (EB == 2 && ROW_BYTES == 64),
                   "stage K is one 128- or 64-byte swizzled row");
@@ -1130,15 +1130,20 @@ using Gemm2PairF8 = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK8, 1>;
 #define GEMM1_SMALL_F8 grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kSwiGLU, 2, kBK8, 1>
 #define GEMM1_LARGE_F8 grouped_gemm_kernel<2, 256, kG1L_A, kG1L_B, kSwiGLU, 1, kBK8, 1>
 #define GEMM2_PAIR_F8 grouped_gemm_kernel<2, 128, kG2P_A, kG2P_B, kDownPair, 2, kBK8, 1>
-// MX block scales: 128-token tiles with one accumulator buffer (the scale
-// columns of the four token stages take the rest of TMEM); for groups of at
-// most 32 rows on average (decode), 32-token tiles with two accumulator
-// buffers, 5 weight stages and 8 small token stages of which 4 are in flight
+// MX block scales: 224-token tiles for groups averaging >= 96 rows (two
+// accumulators of 224 columns and three token stages' scale columns fill
+// TMEM), else 128-token tiles with one accumulator buffer (the scale columns
+// of the four token stages take the rest of TMEM); for groups of at most 32
+// rows on average (decode), 32-token tiles with two accumulator buffers, 5
+// weight stages and 8 small token stages of which 4 are in flight
 constexpr int kMx_A = 4, kMx_B = 4;
 constexpr int kMxD_A = 5, kMxD_B = 8;
 constexpr long kMxDecodeRows = 32;
 using GemmMx = Layout<2, 128, kMx_A, kMx_B, 1, kBK8, 1, 1>;
 using GemmMxDec = Layout<2, 32, kMxD_A, kMxD_B, 2, kBK8, 1, 1>;
+using GemmMxL = Layout<2, 224, 3, 3, 1, kBK8, 1, 1>;
+#define GEMM1_MX_L grouped_gemm_kernel<2, 224, 3, 3, kSwiGLU, 1, kBK8, 1, 1>
+#define GEMM2_MX_L grouped_gemm_kernel<2, 224, 3, 3, kDownPair, 1, kBK8, 1, 1>
 #define GEMM1_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kSwiGLU, 1, kBK8, 1, 1>
 #define GEMM2_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kDownPair, 1, kBK8, 1, 1>
 #define GEMM1_MX_DEC grouped_gemm_kernel<2, 32, kMxD_A, kMxD_B, kSwiGLU, 2, kBK8, 1, 1>
@@ -1233,6 +1238,8 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX, a, GemmMx::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_DEC, a, GemmMxDec::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_DEC, a, GemmMxDec::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_L, a, GemmMxL::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_L, a, GemmMxL::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_CTA_PAIR, a, GemmPairLarge::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_CTA_PAIR, a, GemmPairLarge::SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -1469,6 +1476,9 @@ int launch_gemm_gateup_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* r
     if (n_rows <= kMxDecodeRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 32, ctx.num_sms);
         GEMM1_MX_DEC<<<grid, NUM_THREADS, GemmMxDec::SMEM_BYTES, s>>>(m, m, a, none);
+    } else if (n_rows >= kLargeGateUpRows * groups) {
+        const int grid = grid_for(groups, n_rows, I, 224, ctx.num_sms);
+        GEMM1_MX_L<<<grid, NUM_THREADS, GemmMxL::SMEM_BYTES, s>>>(m, m, a, none);
     } else {
         const int grid = grid_for(groups, n_rows, I, 128, ctx.num_sms);
         GEMM1_MX<<<grid, NUM_THREADS, GemmMx::SMEM_BYTES, s>>>(m, m, a, none);
@@ -1495,6 +1505,9 @@ int launch_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* off
     if (n_rows <= kMxDecodeRows * groups) {
         const int grid = grid_for(groups, n_rows, H / 2, 32, ctx.num_sms);
         GEMM2_MX_DEC<<<grid, NUM_THREADS, GemmMxDec::SMEM_BYTES, s>>>(m, m, a, none);
+    } else if (n_rows >= kLargeGateUpRows * groups) {
+        const int grid = grid_for(groups, n_rows, H / 2, 224, ctx.num_sms);
+        GEMM2_MX_L<<<grid, NUM_THREADS, GemmMxL::SMEM_BYTES, s>>>(m, m, a, none);
     } else {
         const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
         GEMM2_MX<<<grid, NUM_THREADS, GemmMx::SMEM_BYTES, s>>>(m, m, a, none);
