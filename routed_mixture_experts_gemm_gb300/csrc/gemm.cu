@@ -357,7 +357,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     static_assert(MODE1 != kDown || NUM_A == 1, "down tiles have one A operand");
     static_assert(MODE1 == kDown || NUM_A == 2, "gate/up and paired tiles have two");
     constexpr bool PAIR = CG == 2;
-    static_assert(!PAIR || (!FUSED && !MXS && EB == 2), "CTA pairs run the bf16 two-launch GEMMs");
+    static_assert(!PAIR || (!FUSED && !MXS), "CTA pairs run the bf16 / FP8-row two-launch GEMMs");
     constexpr int TG = 16 * CG;  // token-block granularity (an MMA N step per CTA of the tile)
     using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK, EB, MXS, CG>;
     static_assert(EB == 2 || !FUSED, "the FP8 path runs its GEMMs as two launches");
@@ -851,7 +851,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             const int n_mma = ((tl.n_valid + TG - 1) / TG) * TG;
             const uint32_t idesc = MXS ? idesc_mx(BM, n_mma, args.a_fmt, 0u, 0u)
                                  : EB == 2 ? idesc_bf16_f32(BM * CG, n_mma)
-                                           : idesc_e4m3_f32(BM, n_mma);
+                                           : idesc_e4m3_f32(BM * CG, n_mma);
             // the accumulator is free once both CTAs' epilogues have drained it
             if (!(PAIR ? mbar_wait_bounded_cluster(tempty + acc, acc_phase ^ 1u, abort_flag,
                                                    args.status, wait_ns)
@@ -897,8 +897,10 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                                     idesc | (static_cast<uint32_t>(ks) << 4) |
                                         (static_cast<uint32_t>(ks) << 29),
                                     sf + 4 * a, sf + 4 * NUM_A, accum);
-                        else if (PAIR)
+                        else if (PAIR && EB == 2)
                             umma_bf16_pair(d0 + a * BN, adesc, bdesc, idesc, accum);
+                        else if (PAIR)
+                            umma_e4m3_pair(d0 + a * BN, adesc, bdesc, idesc, accum);
                         else if (EB == 2)
                             umma_bf16(d0 + a * BN, adesc, bdesc, idesc, accum);
                         else
@@ -1130,6 +1132,10 @@ using Gemm2PairF8 = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK8, 1>;
 #define GEMM1_SMALL_F8 grouped_gemm_kernel<2, 128, kG1S_A, kG1S_B, kSwiGLU, 2, kBK8, 1>
 #define GEMM1_LARGE_F8 grouped_gemm_kernel<2, 256, kG1L_A, kG1L_B, kSwiGLU, 1, kBK8, 1>
 #define GEMM2_PAIR_F8 grouped_gemm_kernel<2, 128, kG2P_A, kG2P_B, kDownPair, 2, kBK8, 1>
+// ... and the gate/up GEMM on CTA pairs for prefill-sized groups (as bf16)
+using GemmPairLargeF8 = Layout<2, 256, kPr_A, kPr_B, 1, kBK8, 1, 0, 2>;
+#define GEMM1_CTA_PAIR_F8 grouped_gemm_kernel<2, 256, kPr_A, kPr_B, kSwiGLU, 1, kBK8, 1, 0, 2>
+
 // MX block scales: 224-token tiles for groups averaging >= 96 rows (two
 // accumulators of 224 columns and three token stages' scale columns fill
 // TMEM), else 128-token tiles with one accumulator buffer (the scale columns
@@ -1234,6 +1240,9 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_SMALL_F8, a, Gemm1SmallF8::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_LARGE_F8, a, Gemm1LargeF8::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_PAIR_F8, a, Gemm2PairF8::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(GEMM1_CTA_PAIR_F8, a, GemmPairLargeF8::SMEM_BYTES);
+
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX, a, GemmMx::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX, a, GemmMx::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_DEC, a, GemmMxDec::SMEM_BYTES);
@@ -1256,7 +1265,7 @@ int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
 // can be resident at once (one CTA per SM), at most one per tile.  The
 // residency limit is queried once per device and kernel.
 std::mutex g_pair_mu;
-int g_pair_clusters[kMaxDevices][2];
+int g_pair_clusters[kMaxDevices][3];
 
 template <class K>
 int launch_pair(K kernel, int slot, int smem, long tiles, const GemmMaps& m, const GemmArgs& a,
@@ -1423,7 +1432,10 @@ int launch_gemm_gateup_fp8(const uint8_t* xq, const float* sx, const int32_t* ro
     a.w_scale0 = sg;
     a.w_scale1 = su;
     const FusedArgs none{0, 0, nullptr, nullptr};
-    if (n_rows >= kLargeGateUpRows * groups) {
+    if (n_rows >= kLargeGateUpRows * groups && I % 256 == 0) {
+        const long tiles = static_cast<long>(I / 256) * ((n_rows + 255) / 256 + groups);
+        return launch_pair(GEMM1_CTA_PAIR_F8, 2, GemmPairLargeF8::SMEM_BYTES, tiles, m, a, ctx, s);
+    } else if (n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 256, ctx.num_sms);
         GEMM1_LARGE_F8<<<grid, NUM_THREADS, Gemm1LargeF8::SMEM_BYTES, s>>>(m, m, a, none);
     } else {
@@ -1447,7 +1459,8 @@ int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offs
     a.tok_scale = sa;
     a.w_scale0 = sd;
     const FusedArgs none{0, 0, nullptr, nullptr};
-    // (256-token paired tiles, faster for bf16, were measured slower here)
+    // (256-token paired tiles, on one SM or on CTA pairs, both faster for
+    // bf16, were measured slower here: 1.37 and 1.30 vs 1.22 ms at prefill)
     const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
     GEMM2_PAIR_F8<<<grid, NUM_THREADS, Gemm2PairF8::SMEM_BYTES, s>>>(m, m, a, none);
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
