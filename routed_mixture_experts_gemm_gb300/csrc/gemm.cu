@@ -372,8 +372,13 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     uint64_t* afull = bars;
     uint64_t* aempty = afull + SA;
     uint64_t* bfull = aempty + SA;
-    uint64_t* bempty = bfull + SB;
-    uint64_t* tfull = bempty + SB;
+    // with rings of equal depth the two rings advance in lockstep: one
+    // barrier frees a weight stage and a token stage (one MMA commit less per
+    // K stage; every tcgen05 instruction costs the issuing thread tens of
+    // cycles)
+    constexpr bool ONE_EMPTY = SA == SB;
+    uint64_t* bempty = ONE_EMPTY ? aempty : bfull + SB;
+    uint64_t* tfull = bfull + 2 * SB;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
@@ -409,7 +414,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         const uint32_t bfull_count = (MXS && args.gather_rows == nullptr) ? 2u : 1u;
         for (int s = 0; s < SB; ++s) {
             mbar_init(bfull + s, bfull_count + (args.gather_rows != nullptr ? peer : 0u));
-            mbar_init(bempty + s, 1);
+            if (!ONE_EMPTY) mbar_init(bempty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + b, 1);
@@ -909,7 +914,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 }
                 issued = true;
                 commit(aempty + as);
-                commit(bempty + bs);
+                if (!ONE_EMPTY) commit(bempty + bs);
                 if (++as == SA) {
                     as = 0;
                     aph ^= 1u;
