@@ -1145,10 +1145,11 @@ using GemmPairLargeF8 = Layout<2, 256, kPr_A, kPr_B, 1, kBK8, 1, 0, 2>;
 // accumulators of 224 columns and three token stages' scale columns fill
 // TMEM), else 128-token tiles with one accumulator buffer (the scale columns
 // of the four token stages take the rest of TMEM); for groups of at most 32
-// rows on average (decode), 32-token tiles with two accumulator buffers, 5
-// weight stages and 8 small token stages of which 4 are in flight
+// rows on average (decode), 32-token tiles with two accumulator buffers and
+// five weight and five token stages (equal depths: one commit per K stage --
+// issue of the tcgen05 instructions paces these stages)
 constexpr int kMx_A = 4, kMx_B = 4;
-constexpr int kMxD_A = 5, kMxD_B = 8;
+constexpr int kMxD_A = 5, kMxD_B = 5;
 constexpr long kMxDecodeRows = 32;
 using GemmMx = Layout<2, 128, kMx_A, kMx_B, 1, kBK8, 1, 1>;
 using GemmMxDec = Layout<2, 32, kMxD_A, kMxD_B, 2, kBK8, 1, 1>;
