@@ -77,6 +77,16 @@ PROFILE_WORKLOADS = {
     "prefill_e32": synth.MoEConfig("prefill_e32", 24, T=1024, H=7168, I=2048, E=32, k=8,
                                    scoring="sigmoid", n_group=8, topk_group=4,
                                    routed_scaling=2.5, corr_bias_sigma=0.1, router_sigma=None),
+    # the hash workload's character: hash routing, ~43 rows per expert (the
+    # fused launch), 48 experts (4.2 GB of weights)
+    "hash_e48": synth.MoEConfig("hash_e48", 26, T=256, H=7168, I=2048, E=48, k=8,
+                                scoring="sqrtsoftplus", routed_scaling=2.5, hash_vocab=163840),
+    # the skew workload's character: Zipf(1.1) router bias, the hottest
+    # experts replicated (36 slots, ~114 rows per slot: CTA-pair gate/up below
+    # the ridge), a shared expert; 3.3 GB of weights
+    "skew_e32": synth.MoEConfig("skew_e32", 27, T=512, H=7168, I=2048, E=32, k=8,
+                                scoring="sigmoid", routed_scaling=2.5, zipf_s=1.1,
+                                n_hot_replicas=4, shared_I=2048),
     # the decode router / permutation / combine shapes with small experts
     "decode_i128": synth.MoEConfig("decode_i128", 25, T=128, H=7168, I=128, E=256, k=8,
                                    scoring="sigmoid", n_group=8, topk_group=4,
