@@ -52,6 +52,8 @@
 // announced by one relaxed remote arrival once they have landed and been
 // fenced; the MMA commits multicast to both CTAs' empty and accumulator
 // barriers.  Each CTA's epilogue drains its own 128 rows for all tokens.
+// The bf16 and FP8-row GEMMs and the MX gate/up GEMM (224-token tiles) run
+// on CTA pairs for prefill-sized groups.
 //
 // Every pipeline wait is bounded (wall-clock limit); a wait that gives up
 // raises an abort flag seen by all roles, records GBMOE_ERR_TIMEOUT, lets
@@ -111,7 +113,11 @@ constexpr int kSwiGLU = 0, kDown = 1, kDownPair = 2, kFused = 3;
 // tcgen05.mma of M = 256 per A operand, issued by the even CTA; each CTA
 // stages its own 128 rows of every A operand and half of the tile's token
 // rows (BN / 2 per stage), and holds its 128 output rows for all BN tokens in
-// its own tensor memory.
+// its own tensor memory.  With MX block scales each CTA also stages the scale
+// chunks of its own weight rows (by TMA, completing on the even CTA's weight
+// barrier) and those of all the tile's token rows; the even CTA's
+// tcgen05.cp.cta_group::2 copies each CTA's chunks into its own tensor memory,
+// where the pair's block-scaled MMA reads them.
 template <int NUM_A, int BN, int SA, int SB, int ACC_BUFS, int BK, int EB = 2, int MXS = 0,
           int CG = 1>
 struct Layout {
@@ -157,13 +163,15 @@ struct Layout {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(SA >= 2 && SB >= 2 && SA <= 16 && SB <= 16, "ring depth");
     static_assert(BN % BOX_ROWS == 0 && BN % (2 * EPI_COLS) == 0 && BN <= 256, "tile width");
-    static_assert(CG == 1 || (CG == 2 && MXS == 0 && BN % 64 == 0), "CTA-pair tiles");
+    static_assert(CG == 1 || (CG == 2 && BN % 32 == 0 && (MXS || BN % 64 == 0)), "CTA-pair tiles");
 };
 
 // Tensor maps of one GEMM: the weight operand (a0, a1) and the token operand
 // with 16/32/64/128-row boxes.
 struct GemmMaps {
     CUtensorMap a0, a1, b16, b32, b64, b128;
+    // MX on CTA pairs: the tiled weight scale chunks (512-byte rows) of a0, a1
+    CUtensorMap s0, s1;
 };
 
 struct GemmArgs {
@@ -357,7 +365,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
     static_assert(MODE1 != kDown || NUM_A == 1, "down tiles have one A operand");
     static_assert(MODE1 == kDown || NUM_A == 2, "gate/up and paired tiles have two");
     constexpr bool PAIR = CG == 2;
-    static_assert(!PAIR || (!FUSED && !MXS), "CTA pairs run the bf16 / FP8-row two-launch GEMMs");
+    static_assert(!PAIR || !FUSED, "CTA pairs run the two-launch GEMMs");
     constexpr int TG = 16 * CG;  // token-block granularity (an MMA N step per CTA of the tile)
     using L = Layout<NUM_A, BN, SA, SB, ACC_BUFS, BK, EB, MXS, CG>;
     static_assert(EB == 2 || !FUSED, "the FP8 path runs its GEMMs as two launches");
@@ -413,7 +421,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         // thread's (with the copies' bytes) and the published scale columns
         const uint32_t bfull_count = (MXS && args.gather_rows == nullptr) ? 2u : 1u;
         for (int s = 0; s < SB; ++s) {
-            mbar_init(bfull + s, bfull_count + (args.gather_rows != nullptr ? peer : 0u));
+            mbar_init(bfull + s, bfull_count + ((args.gather_rows != nullptr || MXS) ? peer : 0u));
             if (!ONE_EMPTY) mbar_init(bempty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -544,6 +552,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                         tma_load_2d_pair(sA + L::A_BYTES, &m.a1, lb, kb * BK, a_row, pol_w);
                     if (mode == kDownPair)
                         tma_load_2d_pair(sA + L::A_BYTES, &m.a0, lb, kb * BK, a_row + BM, pol_w);
+                    if (MXS) {
+                        uint8_t* sf = smem + L::OFF_ASF + stage * (NUM_A * 512);
+                        const int ch = static_cast<int>(sf_tile0) + kb;
+                        tma_load_2d_pair(sf, &m.s0, lb, 0, ch, pol_w);
+                        if (mode == kSwiGLU) tma_load_2d_pair(sf + 512, &m.s1, lb, 0, ch, pol_w);
+                    }
                 } else {
                     mbar_arrive_expect_tx(afull + stage, NUM_A * a_tx * CG);
                     tma_load_2d(sA, &m.a0, afull + stage, kb * BK, a_row, pol_w);
@@ -552,7 +566,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     if (mode == kDownPair)
                         tma_load_2d(sA + L::A_BYTES, &m.a0, afull + stage, kb * BK, a_row + BM,
                                     pol_w);
-                    if (MXS) {
+                    if (MXS && PAIR) {
+                        uint8_t* sf = smem + L::OFF_ASF + stage * (NUM_A * 512);
+                        const int ch = static_cast<int>(sf_tile0) + kb;
+                        tma_load_2d(sf, &m.s0, afull + stage, 0, ch, pol_w);
+                        if (mode == kSwiGLU) tma_load_2d(sf + 512, &m.s1, afull + stage, 0, ch, pol_w);
+                    } else if (MXS) {
                         uint8_t* sf = smem + L::OFF_ASF + stage * (NUM_A * 512);
                         // gate/up: the gate's and the up's chunks of the same
                         // rows; paired down: the two consecutive row blocks
@@ -854,7 +873,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
             job(tau, second, tl);
             const int KB = (second ? fz.K : args.K) / BK;
             const int n_mma = ((tl.n_valid + TG - 1) / TG) * TG;
-            const uint32_t idesc = MXS ? idesc_mx(BM, n_mma, args.a_fmt, 0u, 0u)
+            const uint32_t idesc = MXS ? idesc_mx(BM * CG, n_mma, args.a_fmt, 0u, 0u)
                                  : EB == 2 ? idesc_bf16_f32(BM * CG, n_mma)
                                            : idesc_e4m3_f32(BM * CG, n_mma);
             // the accumulator is free once both CTAs' epilogues have drained it
@@ -882,11 +901,21 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     const uint32_t asf = smem_u32(smem + L::OFF_ASF) + as * (NUM_A * 512);
                     const uint32_t sfs = smem_u32(smem + L::OFF_SFS) + bs * (L::SFB_CHUNKS * 512);
 #pragma unroll
-                    for (int a = 0; a < NUM_A; ++a)
-                        tmem_cp_32x128b_warpx4(sf + 4 * a, smem_desc_rows16(asf + a * 512));
+                    for (int a = 0; a < NUM_A; ++a) {
+                        if (PAIR)
+                            tmem_cp_32x128b_warpx4_pair(sf + 4 * a, smem_desc_rows16(asf + a * 512));
+                        else
+                            tmem_cp_32x128b_warpx4(sf + 4 * a, smem_desc_rows16(asf + a * 512));
+                    }
 #pragma unroll
-                    for (int c = 0; c < L::SFB_CHUNKS; ++c)
-                        tmem_cp_32x128b_warpx4(sf + 4 * (NUM_A + c), smem_desc_rows16(sfs + c * 512));
+                    for (int c = 0; c < L::SFB_CHUNKS; ++c) {
+                        if (PAIR)
+                            tmem_cp_32x128b_warpx4_pair(sf + 4 * (NUM_A + c),
+                                                        smem_desc_rows16(sfs + c * 512));
+                        else
+                            tmem_cp_32x128b_warpx4(sf + 4 * (NUM_A + c),
+                                                   smem_desc_rows16(sfs + c * 512));
+                    }
                 }
                 // one MMA covers 32 bytes of K (16 bf16 or 32 FP8 elements)
 #pragma unroll
@@ -897,7 +926,12 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                         const uint64_t adesc =
                             smem_desc_kmajor<L::ROW_BYTES / 2>(sA + a * L::A_BYTES + ks * 32);
                         const uint32_t accum = (kb > 0 || ks > 0) ? 1u : 0u;
-                        if (MXS)
+                        if (MXS && PAIR)
+                            umma_mx_pair(d0 + a * BN, adesc, bdesc,
+                                         idesc | (static_cast<uint32_t>(ks) << 4) |
+                                             (static_cast<uint32_t>(ks) << 29),
+                                         sf + 4 * a, sf + 4 * NUM_A, accum);
+                        else if (MXS)
                             umma_mx(d0 + a * BN, adesc, bdesc,
                                     idesc | (static_cast<uint32_t>(ks) << 4) |
                                         (static_cast<uint32_t>(ks) << 29),
@@ -1025,7 +1059,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                     // the activation rounded to bf16, then quantized to MX E4M3:
                     // the warp's 32 lanes are one 32-element block of each
                     // token row (max over the warp, shared exponent, codes)
-                    const int blk = (tl.rblk * BM + q * 32) / 32;
+                    const int blk = ((tl.rblk * CG + static_cast<int>(crank)) * BM + q * 32) / 32;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
                         const float a = bf16_bits_to_f32(f32_to_bf16_bits(v[c]));
@@ -1155,6 +1189,10 @@ using GemmMx = Layout<2, 128, kMx_A, kMx_B, 1, kBK8, 1, 1>;
 using GemmMxDec = Layout<2, 32, kMxD_A, kMxD_B, 2, kBK8, 1, 1>;
 using GemmMxL = Layout<2, 224, 3, 3, 1, kBK8, 1, 1>;
 #define GEMM1_MX_L grouped_gemm_kernel<2, 224, 3, 3, kSwiGLU, 1, kBK8, 1, 1>
+// MX gate/up on CTA pairs for prefill-sized groups: 2 x 128 gate and up rows
+// x 224 tokens, four stages (TMEM: 2 x 224 accumulator + 4 x 16 scale columns)
+using GemmMxPair = Layout<2, 224, 4, 4, 1, kBK8, 1, 1, 2>;
+#define GEMM1_MX_PAIR grouped_gemm_kernel<2, 224, 4, 4, kSwiGLU, 1, kBK8, 1, 1, 2>
 #define GEMM2_MX_L grouped_gemm_kernel<2, 224, 3, 3, kDownPair, 1, kBK8, 1, 1>
 #define GEMM1_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kSwiGLU, 1, kBK8, 1, 1>
 #define GEMM2_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kDownPair, 1, kBK8, 1, 1>
@@ -1254,6 +1292,7 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_DEC, a, GemmMxDec::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_DEC, a, GemmMxDec::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_L, a, GemmMxL::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_PAIR, a, GemmMxPair::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_L, a, GemmMxL::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_CTA_PAIR, a, GemmPairLarge::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_CTA_PAIR, a, GemmPairLarge::SMEM_BYTES);
@@ -1271,7 +1310,7 @@ int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
 // can be resident at once (one CTA per SM), at most one per tile.  The
 // residency limit is queried once per device and kernel.
 std::mutex g_pair_mu;
-int g_pair_clusters[kMaxDevices][3];
+int g_pair_clusters[kMaxDevices][4];
 
 template <class K>
 int launch_pair(K kernel, int slot, int smem, long tiles, const GemmMaps& m, const GemmArgs& a,
@@ -1495,6 +1534,16 @@ int launch_gemm_gateup_mx(const uint8_t* xq, const uint8_t* xs, const int32_t* r
     if (n_rows <= kMxDecodeRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 32, ctx.num_sms);
         GEMM1_MX_DEC<<<grid, NUM_THREADS, GemmMxDec::SMEM_BYTES, s>>>(m, m, a, none);
+    } else if (n_rows >= kLargeGateUpRows * groups && I % 256 == 0) {
+        // the weight scale chunks as 512-byte rows for the pair's TMA copies
+        const uint64_t chunks = static_cast<uint64_t>(groups) * (I / 128) * (H / 128);
+        if (!encode_map_2d(&m.s0, CU_TENSOR_MAP_DATA_TYPE_UINT32, sg, 128, chunks, 512, 128, 1,
+                           CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_map_2d(&m.s1, CU_TENSOR_MAP_DATA_TYPE_UINT32, su, 128, chunks, 512, 128, 1,
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GBMOE_ERR_CUDA;
+        const long tiles = static_cast<long>(I / 256) * ((n_rows + 223) / 224 + groups);
+        return launch_pair(GEMM1_MX_PAIR, 3, GemmMxPair::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, I, 224, ctx.num_sms);
         GEMM1_MX_L<<<grid, NUM_THREADS, GemmMxL::SMEM_BYTES, s>>>(m, m, a, none);
