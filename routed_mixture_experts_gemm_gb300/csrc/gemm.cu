@@ -52,8 +52,8 @@
 // announced by one relaxed remote arrival once they have landed and been
 // fenced; the MMA commits multicast to both CTAs' empty and accumulator
 // barriers.  Each CTA's epilogue drains its own 128 rows for all tokens.
-// The bf16 and FP8-row GEMMs and the MX gate/up GEMM (224-token tiles) run
-// on CTA pairs for prefill-sized groups.
+// The bf16 GEMMs, the FP8-row gate/up and both MX GEMMs (224-token tiles)
+// run on CTA pairs for prefill-sized groups.
 //
 // Every pipeline wait is bounded (wall-clock limit); a wait that gives up
 // raises an abort flag seen by all roles, records GBMOE_ERR_TIMEOUT, lets
@@ -557,6 +557,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                         const int ch = static_cast<int>(sf_tile0) + kb;
                         tma_load_2d_pair(sf, &m.s0, lb, 0, ch, pol_w);
                         if (mode == kSwiGLU) tma_load_2d_pair(sf + 512, &m.s1, lb, 0, ch, pol_w);
+                        if (mode == kDownPair)
+                            tma_load_2d_pair(sf + 512, &m.s0, lb, 0, ch + ks_per_row, pol_w);
                     }
                 } else {
                     mbar_arrive_expect_tx(afull + stage, NUM_A * a_tx * CG);
@@ -571,6 +573,8 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                         const int ch = static_cast<int>(sf_tile0) + kb;
                         tma_load_2d(sf, &m.s0, afull + stage, 0, ch, pol_w);
                         if (mode == kSwiGLU) tma_load_2d(sf + 512, &m.s1, afull + stage, 0, ch, pol_w);
+                        if (mode == kDownPair)
+                            tma_load_2d(sf + 512, &m.s0, afull + stage, 0, ch + ks_per_row, pol_w);
                     } else if (MXS) {
                         uint8_t* sf = smem + L::OFF_ASF + stage * (NUM_A * 512);
                         // gate/up: the gate's and the up's chunks of the same
@@ -1189,10 +1193,12 @@ using GemmMx = Layout<2, 128, kMx_A, kMx_B, 1, kBK8, 1, 1>;
 using GemmMxDec = Layout<2, 32, kMxD_A, kMxD_B, 2, kBK8, 1, 1>;
 using GemmMxL = Layout<2, 224, 3, 3, 1, kBK8, 1, 1>;
 #define GEMM1_MX_L grouped_gemm_kernel<2, 224, 3, 3, kSwiGLU, 1, kBK8, 1, 1>
-// MX gate/up on CTA pairs for prefill-sized groups: 2 x 128 gate and up rows
-// x 224 tokens, four stages (TMEM: 2 x 224 accumulator + 4 x 16 scale columns)
+// MX on CTA pairs for prefill-sized groups: 2 x 128 gate and up rows (or
+// 2 x 256 W_down rows) x 224 tokens, four stages (TMEM: 2 x 224 accumulator +
+// 4 x 16 scale columns)
 using GemmMxPair = Layout<2, 224, 4, 4, 1, kBK8, 1, 1, 2>;
 #define GEMM1_MX_PAIR grouped_gemm_kernel<2, 224, 4, 4, kSwiGLU, 1, kBK8, 1, 1, 2>
+#define GEMM2_MX_PAIR grouped_gemm_kernel<2, 224, 4, 4, kDownPair, 1, kBK8, 1, 1, 2>
 #define GEMM2_MX_L grouped_gemm_kernel<2, 224, 3, 3, kDownPair, 1, kBK8, 1, 1>
 #define GEMM1_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kSwiGLU, 1, kBK8, 1, 1>
 #define GEMM2_MX grouped_gemm_kernel<2, 128, kMx_A, kMx_B, kDownPair, 1, kBK8, 1, 1>
@@ -1293,6 +1299,7 @@ cudaError_t ensure_attrs(int device) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_DEC, a, GemmMxDec::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_L, a, GemmMxL::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_MX_PAIR, a, GemmMxPair::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_PAIR, a, GemmMxPair::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_MX_L, a, GemmMxL::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM1_CTA_PAIR, a, GemmPairLarge::SMEM_BYTES);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(GEMM2_CTA_PAIR, a, GemmPairLarge::SMEM_BYTES);
@@ -1310,7 +1317,7 @@ int grid_for(int groups, int n_rows, int R, int BN, int num_sms) {
 // can be resident at once (one CTA per SM), at most one per tile.  The
 // residency limit is queried once per device and kernel.
 std::mutex g_pair_mu;
-int g_pair_clusters[kMaxDevices][4];
+int g_pair_clusters[kMaxDevices][5];
 
 template <class K>
 int launch_pair(K kernel, int slot, int smem, long tiles, const GemmMaps& m, const GemmArgs& a,
@@ -1573,6 +1580,13 @@ int launch_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* off
     if (n_rows <= kMxDecodeRows * groups) {
         const int grid = grid_for(groups, n_rows, H / 2, 32, ctx.num_sms);
         GEMM2_MX_DEC<<<grid, NUM_THREADS, GemmMxDec::SMEM_BYTES, s>>>(m, m, a, none);
+    } else if (n_rows >= kLargeGateUpRows * groups && H % 512 == 0) {
+        const uint64_t chunks = static_cast<uint64_t>(groups) * (H / 128) * (I / 128);
+        if (!encode_map_2d(&m.s0, CU_TENSOR_MAP_DATA_TYPE_UINT32, sd, 128, chunks, 512, 128, 1,
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GBMOE_ERR_CUDA;
+        const long tiles = static_cast<long>(H / 512) * ((n_rows + 223) / 224 + groups);
+        return launch_pair(GEMM2_MX_PAIR, 4, GemmMxPair::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (n_rows >= kLargeGateUpRows * groups) {
         const int grid = grid_for(groups, n_rows, H / 2, 224, ctx.num_sms);
         GEMM2_MX_L<<<grid, NUM_THREADS, GemmMxL::SMEM_BYTES, s>>>(m, m, a, none);
