@@ -813,6 +813,10 @@ def main(argv=None):
         res = {"workload": c2.name, "T": c2.T, **res}
         stg2 = stage_times(w2, min(args.steps, 10), torch)
         res["stages_ms"] = stg2
+        if c2.use_hash and c2.scoring != "softmax":
+            res["stages_note"] = ("route: the stand-alone moe_route call, which writes every "
+                                  "logit; moe_forward (ms_per_step) computes only the logits "
+                                  "of each token's hashed experts")
         res["layer_tflops"] = 2.0 * c2.N * 3 * c2.H * c2.I / (res["ms_per_step"] / 1e3) / 1e12
         res["roofline"], _ = roofline_of(w2, stg2, w2.counts.cpu().numpy(), peaks, peak_src)
         line[c2.name] = res

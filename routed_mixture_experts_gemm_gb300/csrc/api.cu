@@ -24,7 +24,6 @@ DevCtx g_ctx[kMaxDevices];
 bool g_ctx_ok[kMaxDevices];
 
 constexpr int kMaxE = 1024;
-constexpr int kMaxTopK = 32;
 constexpr int kMaxGroups = 32;
 
 bool valid_activation(int a) { return a >= GBMOE_ACT_SWIGLU && a <= GBMOE_ACT_GEGLU_TANH; }
@@ -587,6 +586,7 @@ int moe_forward(const gbmoe_layer* L, const uint16_t* x, int T, const int32_t* i
     RouteArgs ra{c, T, L->H, x, L->w_router, f.logits, L->router_bias, L->corr_bias, input_ids,
                  L->tid2eid, L->tid2eid_rows, L->log2phy, L->replica_cnt, L->R_max, il, ip, wt,
                  nullptr};
+    ra.hash_logits_only = 1;  // f.logits is scratch: only the selection reads it
     st = status_from(launch_route(ra, *ctx, s));
     if (st) return st;
     // 2. dispatch: counts, offsets, stable permutation ("Stage 4" AllGather

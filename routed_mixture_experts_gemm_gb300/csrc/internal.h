@@ -14,6 +14,7 @@ namespace gbmoe {
 // Per-device host state (contexts, kernel attributes, scratch addresses) is
 // kept for device ordinals below this bound.
 constexpr int kMaxDevices = 64;
+constexpr int kMaxTopK = 32;  // largest top_k a route configuration may ask for
 
 struct DevCtx {
     int device;
@@ -50,6 +51,9 @@ struct RouteArgs {
     int32_t* ids_phys;
     float* weights;
     int32_t* counts;  // may be null; zeroed by the caller beforehand
+    // the logits are scratch (moe_forward): with hash routing and an
+    // elementwise score only the hashed experts' logits are computed
+    int hash_logits_only;
 };
 cudaError_t launch_route(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s);
 cudaError_t launch_expert_counts(const int32_t* ids, int64_t n, int E_phys, int32_t* counts,

@@ -137,6 +137,47 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
         }
 }
 
+// Hash routing with an elementwise score (sigmoid, sqrtsoftplus): the
+// selection reads only the logits of each token's k hashed experts, so only
+// those are computed -- each in the pinned order of the full router (lane j's
+// partial over h = 2j, 2j+1, 64+2j, 65+2j, ... with fused multiply-adds, the
+// pairwise tree over the 32 partials, the router bias added last), so the
+// logits, ids and weights are those of the full computation bit for bit, for
+// k / E of its work.  Block = one token, warp j = slot j (the token's x row
+// is shared through L1).  Out-of-range token ids or table entries compute
+// nothing here; the selection kernel records them.
+__global__ void __launch_bounds__(32 * kMaxTopK) router_logits_hash_kernel(const RouteArgs a) {
+    const int t = blockIdx.x, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.cfg.E_log, k = a.cfg.top_k, H = a.H;
+    if (t >= a.T || j >= k) return;
+    const int v = a.input_ids[t];
+    if (v < 0 || static_cast<int64_t>(v) >= a.tid2eid_rows) return;
+    const int e = a.tid2eid[static_cast<int64_t>(v) * k + j];
+    if (e < 0 || e >= E) return;
+    const uint16_t* xr = a.x + static_cast<size_t>(t) * H;
+    const float* wr = a.w_router + static_cast<size_t>(e) * H;
+    float acc = 0.0f;
+    const bool pairs = (H & 1) == 0 && (reinterpret_cast<uintptr_t>(a.x) & 3u) == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.w_router) & 7u) == 0;
+    if (pairs) {
+#pragma unroll 8
+        for (int h = 2 * lane; h < H; h += 64) {
+            const uint32_t xp = __ldg(reinterpret_cast<const uint32_t*>(xr + h));
+            const float2 wp = __ldg(reinterpret_cast<const float2*>(wr + h));
+            acc = __fmaf_rn(bf16_bits_to_f32(static_cast<uint16_t>(xp & 0xffffu)), wp.x, acc);
+            acc = __fmaf_rn(bf16_bits_to_f32(static_cast<uint16_t>(xp >> 16)), wp.y, acc);
+        }
+    } else {
+        for (int h0 = 2 * lane; h0 < H; h0 += 64)
+            for (int h = h0; h < h0 + 2 && h < H; ++h)
+                acc = __fmaf_rn(bf16_bits_to_f32(__ldg(xr + h)), __ldg(wr + h), acc);
+    }
+    const float sum = warp_sum_tree(acc);
+    if (lane == 0)
+        a.logits[static_cast<size_t>(t) * E + e] =
+            a.router_bias ? __fadd_rn(sum, __ldg(a.router_bias + e)) : sum;
+}
+
 // Two fp32 fused multiply-adds in one instruction (fma.rn.f32x2): each half
 // is an ordinary round-to-nearest fma, so results are those of two fmaf.
 __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
@@ -665,7 +706,14 @@ cudaError_t launch_route(const RouteArgs& a, const DevCtx& ctx, cudaStream_t s) 
     if (a.T == 0) return cudaSuccess;
     const int E = a.cfg.E_log;
     bool done = false;
-    if (a.w_router && a.H % 128 == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 &&
+    if (a.w_router && a.hash_logits_only && a.cfg.use_hash &&
+        a.cfg.scoring != GBMOE_SCORE_SOFTMAX) {
+        router_logits_hash_kernel<<<a.T, 32 * a.cfg.top_k, 0, s>>>(a);
+        const cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        done = true;
+    }
+    if (a.w_router && !done && a.H % 128 == 0 && (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 &&
         (reinterpret_cast<uintptr_t>(a.w_router) & 15u) == 0) {
         const long big_blocks =
             static_cast<long>((a.T + RouterBig256::BT - 1) / RouterBig256::BT) *
