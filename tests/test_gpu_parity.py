@@ -643,3 +643,29 @@ def test_random_forwards_match_oracle(built, name, T, act):
     assert np.array_equal(_np(idp), ref["ids_phys"])
     assert np.array_equal(_np(cnt), ref["counts"])
     assert_within_tol(_bf(out), synth.bf16_to_f32(ref["out"]), f"{name} T={T} {act}")
+
+
+@pytest.mark.parametrize("scoring", ["softmax", "sigmoid", "sqrtsoftplus"])
+def test_hash_forward_every_scoring(built, scoring):
+    """Hash routing through moe_forward with every scoring function: with an
+    elementwise score (sigmoid, sqrtsoftplus) only the logits of each token's
+    hashed experts are computed, softmax needs them all; ids, routing
+    weights and counts bit-exact against the oracle either way ([K3]
+    "Stage 2: Select Experts", hash routing through tid2eid)."""
+    import dataclasses
+    gb = built
+    cfg = dataclasses.replace(synth.MINI["mini_hash"], scoring=scoring, T=301)
+    case = device_case(cfg, DEV, host_weights=True)
+    ref = oracle.run_config(cfg, inputs=case.inputs, weights=case.weights_host)
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    idp = torch.empty_like(ids)
+    wts = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+    cnt = torch.empty(cfg.P, dtype=torch.int32, device=DEV)
+    out = gb.moe_forward(case.layer, case.x, input_ids=case.input_ids, ids_log=ids,
+                         ids_phys=idp, weights=wts, counts=cnt)
+    assert gb.check_device_status() == 0
+    assert np.array_equal(_np(ids), ref["ids_log"])
+    assert np.array_equal(_np(idp), ref["ids_phys"])
+    assert np.array_equal(_np(wts).view(np.uint32), ref["weights"].view(np.uint32))
+    assert np.array_equal(_np(cnt), ref["counts"])
+    assert_within_tol(_bf(out), synth.bf16_to_f32(ref["out"]), f"hash {scoring}")
