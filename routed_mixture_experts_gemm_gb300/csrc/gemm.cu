@@ -51,7 +51,9 @@
 // odd CTA on the critical path); gathered token rows of the odd CTA are
 // announced by one relaxed remote arrival once they have landed and been
 // fenced; the MMA commits multicast to both CTAs' empty and accumulator
-// barriers.  Each CTA's epilogue drains its own 128 rows for all tokens.
+// barriers.  Each CTA's epilogue drains its own 128 rows for all tokens; on
+// the bf16 and FP8-row pairs it writes whole 16-token blocks through shared
+// memory and TMA stores (1.84 -> 1.71 ms for the prefill down GEMM).
 // The bf16 GEMMs, the FP8-row gate/up and both MX GEMMs (224-token tiles)
 // run on CTA pairs for prefill-sized groups.
 //
@@ -152,7 +154,11 @@ struct Layout {
     static constexpr int SFS_BYTES = MXS ? SB * SFB_CHUNKS * 512 : 0;
     static constexpr int OFF_ASF = OFF_SFS + SFS_BYTES;
     static constexpr int ASF_BYTES = MXS ? SA * NUM_A * 512 : 0;
-    static constexpr int END = OFF_ASF + ASF_BYTES;
+    // CTA pairs without MX: per epilogue warp a 2 KB staging block (16 tokens
+    // x 32 outputs) for the epilogue's TMA stores
+    static constexpr bool EPI_TMA = CG == 2 && !MXS;
+    static constexpr int OFF_EPI = (OFF_ASF + ASF_BYTES + 127) / 128 * 128;
+    static constexpr int END = OFF_EPI + (EPI_TMA ? EPI_WARPS * 2048 : 0);
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
     static_assert(TMEM_USED <= 512 && (MXS || TMEM_USED == TMEM_COLS), "TMEM columns");
     static_assert(!MXS || (EB == 1 && BK == 128), "MX stages hold four 32-element K blocks");
@@ -172,6 +178,10 @@ struct GemmMaps {
     CUtensorMap a0, a1, b16, b32, b64, b128;
     // MX on CTA pairs: the tiled weight scale chunks (512-byte rows) of a0, a1
     CUtensorMap s0, s1;
+    // CTA pairs without MX: the output (the down GEMM's fp32 y or the gate/up
+    // GEMM's bf16 activation) in 16-token x 32-column boxes for the
+    // epilogue's TMA stores
+    CUtensorMap o;
 };
 
 struct GemmArgs {
@@ -309,6 +319,19 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool va
                  "r"(valid ? 4 : 0)
                  : "memory");
 }
+// TMA store of one box from shared memory (bulk async-group of this thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
 // from global into shared memory, completing its bytes on the mbarrier.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
@@ -1059,6 +1082,32 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 // outputs (128 B of fp32 / 64 B of bf16): coalesced stores
                 // straight from registers.
                 uint8_t* base = outp + (static_cast<size_t>(tl.row0 + c0) * R + col) * out_elem;
+                if (L::EPI_TMA && !quant_out && c0 + EPI_COLS <= tl.n_valid &&
+                    tl.row0 + c0 + EPI_COLS <= args.n_rows) {
+                    // a whole 16-token block: staged in shared memory and written
+                    // by one TMA store, so the warp hands its accumulator columns
+                    // back without waiting on 16 rows of global stores (a block
+                    // that would reach past the tile's rows takes the plain
+                    // stores below: other tiles own the rows after it)
+                    uint8_t* stg = smem + L::OFF_EPI + (warp - 2) * 2048;
+                    if (lane == 0) bulk_wait_read_all();  // the previous store has read it
+                    __syncwarp();
+                    if (swiglu) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            reinterpret_cast<uint16_t*>(stg)[c * 32 + lane] = f32_to_bf16_bits(v[c]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) reinterpret_cast<float*>(stg)[c * 32 + lane] = v[c];
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&m1.o, stg, static_cast<int>(col) - lane, tl.row0 + c0);
+                        bulk_commit();
+                    }
+                    continue;
+                }
                 if (quant_out) {
                     // the activation rounded to bf16, then quantized to MX E4M3:
                     // the warp's 32 lanes are one 32-element block of each
@@ -1115,6 +1164,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
         }
     }
 
+    if (L::EPI_TMA && warp >= 2 && warp < LOADER_WARP0 && lane == 0) bulk_wait_all();
     // ---- teardown (a pair: neither CTA leaves while the other may still
     // signal its barriers or read its shared memory)
     __syncthreads();
@@ -1391,6 +1441,9 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* row_to_token, int 
     stamp(a);
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (n_rows >= kLargeGateUpRows * groups && I % 256 == 0) {
+        if (!encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, I, n_rows,
+                           static_cast<uint64_t>(I) * 2, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GBMOE_ERR_CUDA;
         const long tiles = static_cast<long>(I / 256) * ((n_rows + 255) / 256 + groups);
         return launch_pair(GEMM1_CTA_PAIR, 0, GemmPairLarge::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (n_rows >= kLargeGateUpRows * groups) {
@@ -1415,6 +1468,9 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
     stamp(a);
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (H % 512 == 0 && n_rows >= kLargeGateUpRows * groups) {
+        if (!encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, H, n_rows,
+                           static_cast<uint64_t>(H) * 4, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GBMOE_ERR_CUDA;
         const long tiles = static_cast<long>(H / 512) * ((n_rows + 255) / 256 + groups);
         return launch_pair(GEMM2_CTA_PAIR, 1, GemmPairLarge::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (H % 256 == 0 && n_rows >= kLargeGateUpRows * groups) {
@@ -1485,6 +1541,9 @@ int launch_gemm_gateup_fp8(const uint8_t* xq, const float* sx, const int32_t* ro
     a.w_scale1 = su;
     const FusedArgs none{0, 0, nullptr, nullptr};
     if (n_rows >= kLargeGateUpRows * groups && I % 256 == 0) {
+        if (!encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, I, n_rows,
+                           static_cast<uint64_t>(I) * 2, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GBMOE_ERR_CUDA;
         const long tiles = static_cast<long>(I / 256) * ((n_rows + 255) / 256 + groups);
         return launch_pair(GEMM1_CTA_PAIR_F8, 2, GemmPairLargeF8::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (n_rows >= kLargeGateUpRows * groups) {
