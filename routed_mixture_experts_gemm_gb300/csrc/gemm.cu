@@ -218,6 +218,9 @@ struct GemmArgs {
     // wall-clock limit of every bounded pipeline wait (set at launch from the
     // process-wide setting; the drains of the error path keep their own)
     uint64_t wait_ns;
+    // 1: the output tensor map (maps.o) is encoded, so the epilogue may write
+    // whole 16-token blocks with TMA stores
+    int tma_out;
 };
 
 // The second GEMM of the fused mode (paired down tiles) and the per-group
@@ -1082,7 +1085,7 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
                 // outputs (128 B of fp32 / 64 B of bf16): coalesced stores
                 // straight from registers.
                 uint8_t* base = outp + (static_cast<size_t>(tl.row0 + c0) * R + col) * out_elem;
-                if (L::EPI_TMA && !quant_out && c0 + EPI_COLS <= tl.n_valid &&
+                if (L::EPI_TMA && args.tma_out && !quant_out && c0 + EPI_COLS <= tl.n_valid &&
                     tl.row0 + c0 + EPI_COLS <= args.n_rows) {
                     // a whole 16-token block: staged in shared memory and written
                     // by one TMA store, so the warp hands its accumulator columns
@@ -1444,6 +1447,7 @@ int launch_gemm_gateup(const uint16_t* x_rows, const int32_t* row_to_token, int 
         if (!encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, I, n_rows,
                            static_cast<uint64_t>(I) * 2, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
             return GBMOE_ERR_CUDA;
+        a.tma_out = 1;
         const long tiles = static_cast<long>(I / 256) * ((n_rows + 255) / 256 + groups);
         return launch_pair(GEMM1_CTA_PAIR, 0, GemmPairLarge::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (n_rows >= kLargeGateUpRows * groups) {
@@ -1471,6 +1475,7 @@ int launch_gemm_down(const uint16_t* act, const int32_t* offsets, int groups, in
         if (!encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, H, n_rows,
                            static_cast<uint64_t>(H) * 4, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
             return GBMOE_ERR_CUDA;
+        a.tma_out = 1;
         const long tiles = static_cast<long>(H / 512) * ((n_rows + 255) / 256 + groups);
         return launch_pair(GEMM2_CTA_PAIR, 1, GemmPairLarge::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (H % 256 == 0 && n_rows >= kLargeGateUpRows * groups) {
@@ -1544,6 +1549,7 @@ int launch_gemm_gateup_fp8(const uint8_t* xq, const float* sx, const int32_t* ro
         if (!encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, I, n_rows,
                            static_cast<uint64_t>(I) * 2, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
             return GBMOE_ERR_CUDA;
+        a.tma_out = 1;
         const long tiles = static_cast<long>(I / 256) * ((n_rows + 255) / 256 + groups);
         return launch_pair(GEMM1_CTA_PAIR_F8, 2, GemmPairLargeF8::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (n_rows >= kLargeGateUpRows * groups) {
@@ -1646,6 +1652,7 @@ int launch_gemm_down_mx(const uint8_t* aq, const uint8_t* as, const int32_t* off
             !encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, H, n_rows,
                            static_cast<uint64_t>(H) * 4, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
             return GBMOE_ERR_CUDA;
+        a.tma_out = 1;
         const long tiles = static_cast<long>(H / 512) * ((n_rows + 223) / 224 + groups);
         return launch_pair(GEMM2_MX_PAIR, 4, GemmMxPair::SMEM_BYTES, tiles, m, a, ctx, s);
     } else if (n_rows >= kLargeGateUpRows * groups) {
