@@ -154,9 +154,10 @@ struct Layout {
     static constexpr int SFS_BYTES = MXS ? SB * SFB_CHUNKS * 512 : 0;
     static constexpr int OFF_ASF = OFF_SFS + SFS_BYTES;
     static constexpr int ASF_BYTES = MXS ? SA * NUM_A * 512 : 0;
-    // CTA pairs: per epilogue warp a 2 KB staging block (16 tokens x 32
-    // outputs) for the epilogue's TMA stores
-    static constexpr bool EPI_TMA = CG == 2;
+    // CTA pairs and the one-SM FP8 tiles of 128 tokens: per epilogue warp a
+    // 2 KB staging block (16 tokens x 32 outputs) for the epilogue's TMA
+    // stores (used where the launch encoded the output map)
+    static constexpr bool EPI_TMA = CG == 2 || (EB == 1 && !MXS && BN == 128 && ACC_BUFS == 2);
     static constexpr int OFF_EPI = (OFF_ASF + ASF_BYTES + 127) / 128 * 128;
     static constexpr int END = OFF_EPI + (EPI_TMA ? EPI_WARPS * 2048 : 0);
     static constexpr int SMEM_BYTES = END + 1024;  // slack to align the base to 1024
@@ -1578,6 +1579,10 @@ int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offs
     const FusedArgs none{0, 0, nullptr, nullptr};
     // (256-token paired tiles, on one SM or on CTA pairs, both faster for
     // bf16, were measured slower here: 1.37 and 1.30 vs 1.22 ms at prefill)
+    if (!encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, H, n_rows,
+                       static_cast<uint64_t>(H) * 4, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return GBMOE_ERR_CUDA;
+    a.tma_out = 1;
     const int grid = grid_for(groups, n_rows, H / 2, 128, ctx.num_sms);
     GEMM2_PAIR_F8<<<grid, NUM_THREADS, Gemm2PairF8::SMEM_BYTES, s>>>(m, m, a, none);
     return cudaGetLastError() == cudaSuccess ? GBMOE_OK : GBMOE_ERR_CUDA;
