@@ -179,9 +179,11 @@ struct GemmMaps {
     CUtensorMap a0, a1, b16, b32, b64, b128;
     // MX on CTA pairs: the tiled weight scale chunks (512-byte rows) of a0, a1
     CUtensorMap s0, s1;
-    // CTA pairs: the output (the down GEMM's fp32 y or the gate/up GEMM's
-    // bf16 activation) in 16-token x 32-column boxes for the epilogue's TMA
-    // stores (not for the MX gate/up, whose epilogue writes E4M3 codes)
+    // the output (the down GEMM's fp32 y or the gate/up GEMM's bf16
+    // activation) in 16-token x 32-column boxes for the epilogue's TMA
+    // stores: encoded by the CTA-pair launches (not the MX gate/up, whose
+    // epilogue writes E4M3 codes) and the one-SM FP8-row down launch, which
+    // then set GemmArgs::tma_out
     CUtensorMap o;
 };
 
@@ -1185,10 +1187,11 @@ grouped_gemm_kernel(const __grid_constant__ GemmMaps m1, const __grid_constant__
 
 // ----------------------------------------------------------------- host
 // Variant choice (measured on the decode, hash, skew and prefill routings):
-// gate/up uses 256-token tiles once groups average >= 96 rows; the down GEMM
-// pairs two 128-row W_down blocks whenever H % 256 == 0, over 256-token tiles
-// (one accumulator buffer) from 96 rows per group on average and over
-// 128-token tiles with two buffers below, else 128- or 256-token
+// once groups average >= 96 rows, gate/up uses 256-token tiles -- on CTA
+// pairs when I % 256 == 0 -- and the down GEMM pairs two 128-row W_down
+// blocks over 256-token tiles (one accumulator buffer) -- on CTA pairs when
+// H % 512 == 0; below 96 rows the down GEMM pairs the blocks over 128-token
+// tiles with two buffers (H % 256 == 0), else 128- or 256-token
 // single-block tiles.  All variants stream K in 64-wide stages
 // (32-wide stages with the 64B swizzle were measured slower: per-stage costs
 // outweigh the extra lookahead).  Below 96 rows per group with H % 256 == 0
@@ -1233,13 +1236,14 @@ using Gemm2PairF8 = Layout<2, 128, kG2P_A, kG2P_B, 2, kBK8, 1>;
 using GemmPairLargeF8 = Layout<2, 256, kPr_A, kPr_B, 1, kBK8, 1, 0, 2>;
 #define GEMM1_CTA_PAIR_F8 grouped_gemm_kernel<2, 256, kPr_A, kPr_B, kSwiGLU, 1, kBK8, 1, 0, 2>
 
-// MX block scales: 224-token tiles for groups averaging >= 96 rows (two
+// MX block scales: 224-token tiles for groups averaging >= 96 rows -- on CTA
+// pairs (below) when I % 256 == 0 / H % 512 == 0, else on one SM (two
 // accumulators of 224 columns and three token stages' scale columns fill
-// TMEM), else 128-token tiles with one accumulator buffer (the scale columns
-// of the four token stages take the rest of TMEM); for groups of at most 32
-// rows on average (decode), 32-token tiles with two accumulator buffers and
-// five weight and five token stages (equal depths: one commit per K stage --
-// issue of the tcgen05 instructions paces these stages)
+// TMEM) -- else 128-token tiles with one accumulator buffer (the scale
+// columns of the four token stages take the rest of TMEM); for groups of at
+// most 32 rows on average (decode), 32-token tiles with two accumulator
+// buffers and five weight and five token stages (equal depths: one commit
+// per K stage)
 constexpr int kMx_A = 4, kMx_B = 4;
 constexpr int kMxD_A = 5, kMxD_B = 5;
 constexpr long kMxDecodeRows = 32;
@@ -1578,7 +1582,8 @@ int launch_gemm_down_fp8(const uint8_t* aq, const float* sa, const int32_t* offs
     a.w_scale0 = sd;
     const FusedArgs none{0, 0, nullptr, nullptr};
     // (256-token paired tiles, on one SM or on CTA pairs, both faster for
-    // bf16, were measured slower here: 1.37 and 1.30 vs 1.22 ms at prefill)
+    // bf16, were measured slower here: 1.37 and 1.30 vs 1.22 ms at prefill;
+    // these 128-token tiles on CTA pairs gained nothing)
     if (!encode_map_2d(&m.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, H, n_rows,
                        static_cast<uint64_t>(H) * 4, 32, EPI_COLS, CU_TENSOR_MAP_SWIZZLE_NONE))
         return GBMOE_ERR_CUDA;
