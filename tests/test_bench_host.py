@@ -64,3 +64,26 @@ def test_algorithmic_bytes_formulas():
     assert dm - d4 == 2 * H * I * 0.5
     assert gm == 2 * 2 * I * (H + H / 32) + 4 * (H + H / 32)
     assert dm == 2 * H * (I + I / 32) + 8 * (I + I / 32)
+
+
+def test_traffic_profile_covers_every_roofline_kernel():
+    """Every roofline the bench line reports has a DRAM-traffic entry, all
+    taken on one kernel source, each a scaled-up measurement that reads the
+    algorithmic bytes at least about once (ratios below 1 would mean the
+    twin's traffic was not the launch's)."""
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        d = json.load(f)
+    keys = ["expert_mlp_fused/decode", "gemm_gateup/prefill", "expert_mlp_fused/hash",
+            "gemm_gateup/skew"]
+    keys += [f"{k}_gateup/{w}" for k in ("fp8_row", "mxfp8", "w4a8") for w in ("decode", "prefill")]
+    hashes = set()
+    for k in keys:
+        assert k in d, k
+        e = d[k]
+        hashes.add(e["source_hash"])
+        assert e["bytes_per_launch"] > 0
+        assert 0.98 <= e["ratio"] <= 1.25, (k, e["ratio"])
+        scaled = e["measured_small_case_bytes"] * e["full_case_algorithmic_bytes"] / \
+            e["small_case_algorithmic_bytes"]
+        assert abs(scaled - e["bytes_per_launch"]) <= 1e-6 * scaled + 1, k
+    assert len(hashes) == 1, hashes
