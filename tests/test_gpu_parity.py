@@ -516,6 +516,12 @@ def test_gemm_tile_variants(built, shape):
     assert gb.check_device_status() == 0
     assert_within_tol(_bf(act), synth.bf16_to_f32(act_o), f"act {shape}")
     assert_within_tol(_np(y), y_o, f"y {shape}")
+    # run-to-run determinism (bitwise), here also for the CTA-pair kernels'
+    # TMA-store epilogues (blocks of 16 token rows written through shared memory)
+    act2 = gb.moe_gemm_gateup_act(d["x"], d["offs"], d["wg"], d["wu"])
+    y2 = gb.moe_gemm_down(bf16_dev(act_o, DEV), d["offs"], d["wd"])
+    assert torch.equal(act.view(torch.int16), act2.view(torch.int16))
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
 
 
 # both GEMMs through moe_expert_mlp: fused in one launch (groups averaging
