@@ -127,6 +127,13 @@ def test_mx_gemms(gb, shape, wfmt, act):
     # down GEMM on the GPU's own activation codes
     y = gb.moe_gemm_down_mx(aq1, as1, d["offs"], d["wd"], d["sd"], w_fmt=wfmt)
     assert gb.check_device_status() == 0
+    # run-to-run determinism (bitwise), also on the CTA-pair kernels
+    aq3, as3 = gb.moe_gemm_gateup_act_mx(d["xq"], d["xs"], d["offs"], d["wg"], d["sg"], d["wu"],
+                                         d["su"], w_fmt=wfmt, row_to_token=d["r2t"],
+                                         activation=act)
+    y3 = gb.moe_gemm_down_mx(aq1, as1, d["offs"], d["wd"], d["sd"], w_fmt=wfmt)
+    assert torch.equal(aq1, aq3) and torch.equal(as1, as3)
+    assert torch.equal(y.view(torch.int32), y3.view(torch.int32))
     a = deq(_np(aq1), _np(as1), "e4m3")
     y_h = _np(y).astype(np.float64)
     offs = c["offs"]
